@@ -1,0 +1,114 @@
+"""Seeded synthetic inputs shaped like expanded-token MoE activations.
+
+This module only draws random numbers: it holds none of the SwiGLU or
+quantization arithmetic, so both the CUDA path's tests and the CPU oracle can
+take their inputs from here without sharing any of the method.
+
+The workloads follow the MoE setting of "TileKernels从入门到精通" (zhichai.net/
+topic/177618752), ch.2: each row of ``x [T, 2H]`` is one (token, expert) pair
+after top-k expansion, gate half first, with one top-k routing weight per row.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int                      # expanded-token rows
+    H: int                      # output width; x has 2H columns
+    group: int                  # 0 = one scale per row, else columns per scale
+    scale_fmt: str              # "fp32" | "ue8m0"
+    out_fmt: str                # "e4m3" | "e2m1"
+    x_dist: str                 # "normal" | "row_lognormal" | "outliers"
+    x_sigma: float = 1.0
+    w_dist: str | None = None   # None | "topk8_norm" | "uniform"
+    clamp: float | None = None
+    seed: int = 0
+
+    @property
+    def groups_per_row(self) -> int:
+        return 1 if self.group == 0 else self.H // self.group
+
+    def algo_bytes(self, rows: int | None = None) -> int:
+        """Minimum HBM bytes one pass moves: bf16 input, codes, scales, weights."""
+        T = self.T if rows is None else rows
+        q = T * self.H if self.out_fmt == "e4m3" else T * self.H // 2
+        s = T * self.groups_per_row * (4 if self.scale_fmt == "fp32" else 1)
+        w = 4 * T if self.w_dist else 0
+        return 4 * T * self.H + q + s + w
+
+    def with_rows(self, T: int) -> "Workload":
+        return Workload(**{**self.__dict__, "T": T})
+
+
+# The five configurations, smallest first. Distributions: "normal" is
+# N(0, sigma^2); "row_lognormal" multiplies each whole row (both halves) by one
+# LogNormal(0, 1) factor; "outliers" multiplies 0.1% of elements, at uniform
+# positions, by 50. "topk8_norm" weights are U(0,1) normalised to sum 1 over
+# each consecutive run of 8 rows (one token's top-8 experts).
+WORKLOADS = {
+    "per_token_T256_H512": Workload("per_token_T256_H512", 256, 512, 0, "fp32", "e4m3",
+                                    "normal", seed=1001),
+    "moe_T8192_H2048_g128": Workload("moe_T8192_H2048_g128", 8192, 2048, 128, "fp32", "e4m3",
+                                     "row_lognormal", w_dist="topk8_norm", seed=1002),
+    "moe_T32768_H2048_g128_ue8m0_clamp7": Workload(
+        "moe_T32768_H2048_g128_ue8m0_clamp7", 32768, 2048, 128, "ue8m0", "e4m3",
+        "outliers", w_dist="topk8_norm", clamp=7.0, seed=1003),
+    "ragged_T100003_H3072_g128": Workload("ragged_T100003_H3072_g128", 100003, 3072, 128,
+                                          "fp32", "e4m3", "normal", x_sigma=0.5,
+                                          w_dist="uniform", seed=1004),
+    "fp4_T65536_H2048_g32_ue8m0_clamp7": Workload(
+        "fp4_T65536_H2048_g32_ue8m0_clamp7", 65536, 2048, 32, "ue8m0", "e2m1",
+        "row_lognormal", w_dist="topk8_norm", clamp=7.0, seed=1005),
+}
+
+ORDER = list(WORKLOADS)
+
+_CHUNK_ROWS = 4096
+
+
+def make_inputs(wl: Workload, device: str | torch.device = "cpu"):
+    """Return (x bf16 [T, 2H], w fp32 [T] or None) for a workload, drawn from
+    one torch.Generator seeded with wl.seed on ``device``. Rows are drawn in
+    chunks of 4096 so that peak memory stays bounded at large T."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(wl.seed)
+    T, H = wl.T, wl.H
+    x = torch.empty((T, 2 * H), dtype=torch.bfloat16, device=device)
+    for r0 in range(0, T, _CHUNK_ROWS):
+        r1 = min(T, r0 + _CHUNK_ROWS)
+        n = r1 - r0
+        v = torch.randn((n, 2 * H), generator=gen, device=device, dtype=torch.float32)
+        if wl.x_sigma != 1.0:
+            v.mul_(wl.x_sigma)
+        if wl.x_dist == "row_lognormal":
+            v.mul_(torch.randn((n, 1), generator=gen, device=device).exp_())
+        elif wl.x_dist == "outliers":
+            hit = torch.rand((n, 2 * H), generator=gen, device=device) < 1e-3
+            v = torch.where(hit, v * 50.0, v)
+        elif wl.x_dist != "normal":
+            raise ValueError(wl.x_dist)
+        x[r0:r1] = v.to(torch.bfloat16)
+    w = None
+    if wl.w_dist is not None:
+        w = torch.rand((T,), generator=gen, device=device, dtype=torch.float32)
+        if wl.w_dist == "topk8_norm":
+            full = (T // 8) * 8
+            if full:
+                blk = w[:full].view(-1, 8)
+                w[:full] = (blk / blk.sum(dim=1, keepdim=True)).reshape(-1)
+            if full < T:
+                w[full:] = w[full:] / w[full:].sum()
+        elif wl.w_dist != "uniform":
+            raise ValueError(wl.w_dist)
+    return x, w
+
+
+def bf16_bits(x: torch.Tensor):
+    """View a bf16 tensor's bit patterns as a numpy uint16 array (host copy)."""
+    return x.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")

@@ -1,0 +1,357 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix, never against the oracle itself.
+
+Each pin takes a loaded oracle library and raises AssertionError on a
+mismatch. ``test_oracle_pins.py`` runs them on the real oracle;
+``test_oracle_mutants.py`` runs them on copies of the oracle with one planted
+mistake each and requires that some pin fails.
+
+Sources of truth used here:
+  * torch's CPU ``float8_e4m3fn`` cast and decode (a library routine; RNE,
+    non-saturating, so it is used below 464 only) and its ``float8_e8m0fnu``
+    cast (rounds a positive value up to a power of two) on quotients that are
+    exact;
+  * the OCP E2M1 grid {0, 0.5, 1, 1.5, 2, 3, 4, 6} and an independent
+    brute-force nearest-even search written here in numpy;
+  * textbook SwiGLU ``g * expit(g) * u * w`` with scipy's logistic function;
+  * the hand-worked rows in tests/golden/hand_rows.json;
+  * closed forms and invariants of absmax scaling.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+import torch
+from scipy.special import expit
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "hand_rows.json")
+
+E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _bf16_bits(values) -> np.ndarray:
+    t = torch.tensor(np.asarray(values, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _e4m3_grid_f64(lib) -> np.ndarray:
+    return np.array([lib.tko_e4m3_decode(c) for c in range(0x7F)], np.float64)
+
+
+# ------------------------------------------------------------------ formats
+
+def pin_e4m3_decode_vs_torch(lib):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).float().double().numpy()
+    got = np.array([lib.tko_e4m3_decode(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got)), "NaN codes differ"
+    assert np.array_equal(ref[~nan], got[~nan]), "E4M3 decode differs from torch"
+    # signed zero: code 0x80 is -0
+    assert np.signbit(got[0x80]) and not np.signbit(got[0x00])
+
+
+def _e4m3_sweep() -> np.ndarray:
+    """fp32 values: every finite grid point, every midpoint and its fp32
+    neighbours, random log-uniform magnitudes, tiny and zero values."""
+    grid = np.array([float(torch.tensor([c], dtype=torch.uint8).view(torch.float8_e4m3fn).float())
+                     for c in range(0x7F)])
+    mids = (grid[:-1] + grid[1:]) / 2
+    pts = np.concatenate([grid, mids]).astype(np.float32)
+    up = np.nextafter(pts, np.float32(np.inf))
+    dn = np.nextafter(pts, np.float32(-np.inf))
+    rng = np.random.default_rng(7)
+    rnd = np.exp2(rng.uniform(-14.0, np.log2(463.9), 6000)).astype(np.float32)
+    tiny = np.array([1e-30, 2.0 ** -126, 2.0 ** -149, 2.0 ** -11, 2.0 ** -10], np.float32)
+    v = np.concatenate([pts, up, dn, rnd, tiny, np.float32([0.0])])
+    v = v[np.abs(v) < 464.0]
+    return np.concatenate([v, -v]).astype(np.float32)
+
+
+def pin_e4m3_encode_vs_torch(lib):
+    v = _e4m3_sweep()
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([lib.tko_e4m3_encode(float(a)) for a in v], np.uint8)
+    bad = np.nonzero(ref != got)[0]
+    assert bad.size == 0, "E4M3 encode differs from torch at %r" % (v[bad[:5]],)
+
+
+def pin_e4m3_saturation_and_roundtrip(lib):
+    for a in [448.0, 449.0, 464.0, 480.0, 1e4, 3.0e38]:
+        assert lib.tko_e4m3_encode(a) == 0x7E, a
+        assert lib.tko_e4m3_encode(-a) == 0xFE, a
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue
+        assert lib.tko_e4m3_encode(lib.tko_e4m3_decode(c)) == c, hex(c)
+
+
+def pin_e2m1_decode_table(lib):
+    got = np.array([lib.tko_e2m1_decode(c) for c in range(16)])
+    assert np.array_equal(got[:8], E2M1_GRID)
+    assert np.array_equal(got[8:], -E2M1_GRID)
+    assert np.signbit(got[8])
+
+
+def pin_e2m1_ties(lib):
+    # Ties go to the even code (even mantissa bit).
+    table = {0.25: 0.0, 0.75: 1.0, 1.25: 1.0, 1.75: 2.0, 2.5: 2.0, 3.5: 4.0, 5.0: 4.0,
+             7.0: 6.0, 100.0: 6.0, 0.2: 0.0, 0.3: 0.5, 5.01: 6.0, 4.99: 4.0}
+    for a, want in table.items():
+        for sgn in (1.0, -1.0):
+            code = lib.tko_e2m1_encode(sgn * a)
+            got = lib.tko_e2m1_decode(code)
+            assert got == sgn * want, (sgn * a, got, want)
+
+
+def pin_e2m1_encode_bruteforce(lib):
+    rng = np.random.default_rng(11)
+    mids = (E2M1_GRID[:-1] + E2M1_GRID[1:]) / 2
+    v = np.concatenate([E2M1_GRID, mids, rng.uniform(0, 8, 4000)]).astype(np.float32)
+    v = np.concatenate([v, np.nextafter(v, np.float32(9)), np.nextafter(v, np.float32(-1))])
+    v = v[v >= 0]
+    dist = np.abs(v[:, None].astype(np.float64) - E2M1_GRID[None, :])
+    # nearest; on a tie prefer the even code: sort key (distance, code parity)
+    key = dist * 4.0 + (np.arange(8) % 2)[None, :] * 1e-9
+    want = np.argmin(key, axis=1)
+    want[v >= 6.0] = 7
+    got = np.array([lib.tko_e2m1_encode(float(a)) for a in v])
+    assert np.array_equal(got, want), v[got != want][:5]
+    gotn = np.array([lib.tko_e2m1_encode(-float(a)) for a in v])
+    assert np.array_equal(gotn, want | 8)
+
+
+def pin_ue8m0(lib):
+    # amax = qmax * 2^k exactly -> exponent k; one ulp above -> k + 1.
+    for qmax in (448.0, 6.0):
+        for k in range(-120, 118, 7):
+            a = np.float32(qmax * 2.0 ** k)
+            assert lib.tko_ue8m0_byte(float(a), qmax) == k + 127, (qmax, k)
+            a_up = np.nextafter(a, np.float32(np.inf))
+            assert lib.tko_ue8m0_byte(float(a_up), qmax) == k + 128, (qmax, k)
+    assert lib.tko_ue8m0_byte(0.0, 448.0) == 127
+    # torch's e8m0 cast rounds a positive value to the nearest power of two
+    # (mantissa >= 1.5 goes up). The scale rule takes the smallest power of
+    # two not below the quotient, so on exact quotients amax / 448 = m * 2^e
+    # (1 <= m < 2) the two agree when m == 1 or m >= 1.5, and the scale rule
+    # is one above torch when 1 < m < 1.5.
+    for n in [1, 3, 5, 7, 9, 11, 13, 15, 17, 100, 127, 1000]:
+        m = n / 2.0 ** np.floor(np.log2(n))
+        for j in range(-30, 30, 3):
+            amax = np.float32(7.0 * n * 2.0 ** j)          # 448 = 7 * 64
+            quot = np.float32(n * 2.0 ** (j - 6))          # exact amax / 448
+            ref = torch.tensor([float(quot)]).to(torch.float8_e8m0fnu).view(torch.uint8).item()
+            want = ref + (1 if 1.0 < m < 1.5 else 0)
+            assert lib.tko_ue8m0_byte(float(amax), 448.0) == want, (n, j)
+    for b in [0, 1, 100, 127, 200, 254]:
+        assert lib.tko_ue8m0_value(b) == np.float32(2.0 ** (b - 127))
+
+
+# ---------------------------------------------------------------- full rows
+
+def _fmt_codes(q: np.ndarray):
+    return ["%02X" % int(c) for c in q.reshape(-1)]
+
+
+def pin_hand_rows(lib):
+    rows = json.load(open(GOLDEN))["rows"]
+    for r in rows:
+        x = _bf16_bits(np.concatenate([r["gate"], r["up"]]))[None, :]
+        w = None if r["w"] is None else np.array([r["w"]], np.float32)
+        out = oracle.swiglu_quant(x, w, r["group"], r["scale_fmt"], r["out_fmt"],
+                                  clamp=r["clamp"], lib=lib)
+        assert _fmt_codes(out["q"]) == r["q"], (r["name"], _fmt_codes(out["q"]))
+        if r["scale_fmt"] == "fp32":
+            s = float(out["scales"].reshape(-1)[0])
+            assert abs(s - r["scale_approx"]) <= 1e-6 * r["scale_approx"], (r["name"], s)
+        else:
+            assert int(out["scales"].reshape(-1)[0]) == r["scale_byte"], r["name"]
+        assert out["counts"].tolist() == r["counts"], (r["name"], out["counts"])
+
+
+def pin_clamp_limit_strict(lib):
+    # The guard fires on values strictly past the limit ("val > clamp value").
+    x = _bf16_bits([7.0, 8.0, -7.0, 7.0, -8.0, 7.0])[None, :]
+    out = oracle.swiglu_quant(x, None, 0, "fp32", "e4m3", clamp=7.0, lib=lib)
+    assert out["counts"].tolist() == [1, 1]
+    # counts accumulate into the caller's counter across calls
+    acc = np.zeros(2, np.int64)
+    q = np.zeros(3, np.uint8)
+    s = np.zeros(1, np.float32)
+    for _ in range(3):
+        lib.tko_swiglu_quant(x.ctypes.data, 1, 3, None, 0, 0, 0, 1, 7.0,
+                             q.ctypes.data, s.ctypes.data, acc.ctypes.data, None)
+    assert acc.tolist() == [3, 3]
+
+
+def _random_rows(rng, rows, H, spread=True):
+    v = rng.standard_normal((rows, 2 * H)).astype(np.float32)
+    if spread:
+        v *= np.exp(rng.standard_normal((rows, 1))).astype(np.float32)
+    return _bf16_bits(v)
+
+
+def pin_swiglu_textbook(lib):
+    rng = np.random.default_rng(3)
+    H = 256
+    x = _random_rows(rng, 24, H)
+    w = rng.uniform(0.01, 1.0, 24).astype(np.float32)
+    for clamp in (None, 3.0):
+        out = oracle.swiglu_quant(x, w, 128, "fp32", "e4m3", clamp=clamp, want_y=True, lib=lib)
+        g = _bits_to_f64(x[:, :H])
+        u = _bits_to_f64(x[:, H:])
+        cnt = [0, 0]
+        if clamp is not None:
+            cnt = [int((g > clamp).sum()), int((np.abs(u) > clamp).sum())]
+            g = np.minimum(g, clamp)
+            u = np.clip(u, -clamp, clamp)
+        ref = (g * expit(g) * u * w.astype(np.float64)[:, None]).astype(np.float32)
+        got = out["y"]
+        ulp = np.abs(got.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
+        assert ulp.max() <= 1, "activation differs from textbook SwiGLU by %d ulp" % ulp.max()
+        assert out["counts"].tolist() == cnt
+
+
+def _spacing(a: np.ndarray, out_fmt: str) -> np.ndarray:
+    """Grid spacing of the format at magnitude a (within a's binade)."""
+    a = np.abs(a).astype(np.float64)
+    if out_fmt == "e4m3":
+        e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+        return 2.0 ** (e - 3)
+    return np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+
+
+def pin_invariants(lib):
+    rng = np.random.default_rng(5)
+    H = 512
+    x = _random_rows(rng, 16, H)
+    w = rng.uniform(0.05, 1.0, 16).astype(np.float32)
+    for out_fmt, qmax in (("e4m3", 448.0), ("e2m1", 6.0)):
+        dec = (oracle.e4m3_decode_table(lib) if out_fmt == "e4m3"
+               else oracle.e2m1_decode_table(lib))
+        for scale_fmt in ("fp32", "ue8m0"):
+            for group in (32, 128, 0):
+                out = oracle.swiglu_quant(x, w, group, scale_fmt, out_fmt, want_y=True, lib=lib)
+                y = out["y"].astype(np.float64)
+                g = H if group == 0 else group
+                q = out["q"] if out_fmt == "e4m3" else oracle.unpack_e2m1(out["q"])
+                vals = dec[q]
+                sc = out["scales"].astype(np.float64)
+                if scale_fmt == "ue8m0":
+                    sc = 2.0 ** (sc - 127.0)
+                s_full = np.repeat(sc, g, axis=1)
+                assert np.all(np.abs(vals) <= qmax)
+                yq = y / s_full
+                err = np.abs(vals - yq)
+                bound = 0.5 * _spacing(yq, out_fmt) + 2.0 ** -23 * np.abs(yq)
+                assert np.all(err <= bound), (out_fmt, scale_fmt, group, err.max())
+                yg = y.reshape(y.shape[0], -1, g)
+                amax = np.abs(yg).max(axis=2)
+                ratio = amax / sc
+                if scale_fmt == "fp32":
+                    arg = np.abs(yg).argmax(axis=2)
+                    top = np.take_along_axis(vals.reshape(yg.shape), arg[..., None], axis=2)
+                    assert np.all(np.abs(top) == qmax), (out_fmt, group)
+                    assert np.allclose(ratio, qmax, rtol=2.0 ** -22)
+                else:
+                    assert np.all((ratio > qmax / 2) & (ratio <= qmax)), (out_fmt, group)
+
+
+def pin_group_indexing(lib):
+    # Each group j of each row r gets a different planted peak, so a mixed-up
+    # group or row index shows in the scales and in which code reaches max.
+    H, g, rows = 512, 128, 3
+    gate = np.full((rows, H), 4.0, np.float32)
+    up = np.full((rows, H), 0.01, np.float32)
+    peaks = {}
+    for r in range(rows):
+        for j in range(H // g):
+            col = j * g + (17 * j + 5 * r) % g
+            up[r, col] = float(2 ** (j + r + 1))
+            peaks[(r, j)] = col
+    x = _bf16_bits(np.concatenate([gate, up], axis=1))
+    out = oracle.swiglu_quant(x, None, g, "ue8m0", "e4m3", want_y=True, lib=lib)
+    silu4 = 4.0 * expit(4.0)
+    for (r, j), col in peaks.items():
+        amax = np.float32(silu4 * 2 ** (j + r + 1))
+        k = int(np.ceil(np.log2(float(amax) / 448.0)))
+        assert int(out["scales"][r, j]) == k + 127, (r, j)
+        big = [c for c in range(j * g, (j + 1) * g) if out["q"][r, c] & 0x7F >= 0x70]
+        assert big == [col], (r, j, big, col)
+
+
+def pin_zero_and_signed_zero(lib):
+    H = 64
+    for out_fmt in ("e4m3", "e2m1"):
+        for scale_fmt in ("fp32", "ue8m0"):
+            gate = np.zeros((1, H), np.float32)
+            up = np.where(np.arange(H) % 2 == 0, 1.0, -1.0).astype(np.float32)[None, :]
+            x = _bf16_bits(np.concatenate([gate, up], axis=1))
+            out = oracle.swiglu_quant(x, None, 32, scale_fmt, out_fmt, lib=lib)
+            sc = out["scales"].reshape(-1)
+            if scale_fmt == "fp32":
+                assert np.all(sc == 1.0)
+            else:
+                assert np.all(sc == 127)
+            q = out["q"] if out_fmt == "e4m3" else oracle.unpack_e2m1(out["q"])
+            sign = 0x80 if out_fmt == "e4m3" else 0x8
+            # 0 * (+1) = +0 and 0 * (-1) = -0: codes are signed zeros
+            want = np.where(np.arange(H) % 2 == 0, 0, sign)
+            assert np.array_equal(q.reshape(-1), want), (out_fmt, q)
+
+
+def pin_e2m1_packing(lib):
+    # One group of 4 values whose codes are all different: 6*[1, 0.5, -1/3, 1/6]
+    y = np.array([[6.0, 3.0, -2.0, 1.0]], np.float32)
+    q, s = oracle.quant_rows_f32(y, 0, "fp32", "e2m1", lib=lib)
+    assert float(s[0, 0]) == 1.0
+    # codes: 6 -> 0x7, 3 -> 0x5, -2 -> 0xC, 1 -> 0x2; value 2k in the low nibble
+    assert q.tolist() == [[0x57, 0x2C]], q
+
+
+def pin_quant_rows_indexing(lib):
+    # Multi-row, multi-group fp32 input: group j of row r holds one peak
+    # 2^(j + 4r) among values 0.5, so its scale is peak / 448 and the only
+    # maximal code sits at the peak's column.
+    rows, H, g = 3, 256, 64
+    y = np.full((rows, H), 0.5, np.float32)
+    cols = {}
+    for r in range(rows):
+        for j in range(H // g):
+            c = j * g + (11 * j + 7 * r) % g
+            y[r, c] = np.float32(2.0 ** (j + 4 * r))
+            cols[(r, j)] = c
+    for out_fmt, qmax, top in (("e4m3", 448.0, 0x7E), ("e2m1", 6.0, 0x7)):
+        q, sc = oracle.quant_rows_f32(y, g, "fp32", out_fmt, lib=lib)
+        q = q if out_fmt == "e4m3" else oracle.unpack_e2m1(q)
+        for (r, j), c in cols.items():
+            assert sc[r, j] == np.float32(y[r, c]) / np.float32(qmax), (out_fmt, r, j)
+            tops = [k for k in range(j * g, (j + 1) * g) if q[r, k] == top]
+            assert tops == [c], (out_fmt, r, j, tops)
+
+
+ALL_PINS = [
+    pin_e4m3_decode_vs_torch,
+    pin_e4m3_encode_vs_torch,
+    pin_e4m3_saturation_and_roundtrip,
+    pin_e2m1_decode_table,
+    pin_e2m1_ties,
+    pin_e2m1_encode_bruteforce,
+    pin_ue8m0,
+    pin_hand_rows,
+    pin_clamp_limit_strict,
+    pin_swiglu_textbook,
+    pin_invariants,
+    pin_group_indexing,
+    pin_zero_and_signed_zero,
+    pin_e2m1_packing,
+    pin_quant_rows_indexing,
+]
