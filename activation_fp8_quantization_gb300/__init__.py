@@ -1,1 +1,202 @@
-"""Fused SwiGLU + MoE top-k weight + FP8/FP4 activation cast for GB300 (sm_103a)."""
+"""Fused SwiGLU + MoE top-k weight + FP8/FP4 activation cast for GB300 (sm_103a).
+
+The computation runs in ``libtk_swiglu_quant.so`` (hand-written CUDA behind the
+C ABI of ``include/tk_swiglu_quant.h``). This module only turns torch CUDA
+tensors into device pointers and the current CUDA stream; PyTorch supplies
+device memory and streams, nothing else.
+
+    >>> op = SwigluQuant(hidden=2048, group_size=128, scale_fmt="fp32", out_fmt="e4m3")
+    >>> q, scales = op(x, topk_weights)        # x: [T, 4096] bf16 on cuda
+
+``q`` is uint8 ([T, H] E4M3 codes, or [T, H/2] packed E2M1 with value 2k in
+the low nibble); ``scales`` is float32 or uint8 (UE8M0 exponent bytes),
+[T, H / group_size] (one column when group_size == 0).
+"""
+from __future__ import annotations
+
+import threading
+
+from . import _abi
+from ._abi import (IN_DTYPES, OUT_FMTS, SCALE_FMTS, QuantCastDesc, SwigluQuantDesc, TkError,
+                   tk_last_error_message, tk_quant_cast_plan, tk_quant_cast_plan_destroy,
+                   tk_quant_cast_run, tk_quant_cast_validate, tk_status_string,
+                   tk_swiglu_quant_launch_info, tk_swiglu_quant_output_sizes, tk_swiglu_quant_plan,
+                   tk_swiglu_quant_plan_destroy, tk_swiglu_quant_run, tk_swiglu_quant_validate)
+
+__all__ = [
+    "SwigluQuant", "QuantCast", "swiglu_quant", "quant_cast", "TkError",
+    "SwigluQuantDesc", "QuantCastDesc", "tk_swiglu_quant_validate", "tk_swiglu_quant_plan",
+    "tk_swiglu_quant_plan_destroy", "tk_swiglu_quant_output_sizes", "tk_swiglu_quant_run",
+    "tk_swiglu_quant_launch_info", "tk_quant_cast_validate", "tk_quant_cast_plan",
+    "tk_quant_cast_plan_destroy", "tk_quant_cast_run", "tk_status_string",
+    "tk_last_error_message",
+]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _out_shapes(T: int, hidden: int, group_size: int, scale_fmt: str, out_fmt: str):
+    torch = _torch()
+    G = 1 if group_size == 0 else hidden // group_size
+    q_shape = (T, hidden if out_fmt == "e4m3" else hidden // 2)
+    s_dtype = torch.float32 if scale_fmt == "fp32" else torch.uint8
+    return q_shape, (T, G), s_dtype
+
+
+def _check_cuda(t, name: str, dtype, shape=None):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s (got %s)" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s (got %s)" % (name, tuple(shape), tuple(t.shape)))
+
+
+class SwigluQuant:
+    """A plan for the fused op on one device (see tk_swiglu_quant_plan)."""
+
+    def __init__(self, hidden: int, group_size: int = 128, scale_fmt: str = "fp32",
+                 out_fmt: str = "e4m3", topk_weights: bool = True,
+                 clamp_limit: float | None = None, count_clamped: bool = False,
+                 device: int | None = None):
+        torch = _torch()
+        self.hidden, self.group_size = int(hidden), int(group_size)
+        self.scale_fmt, self.out_fmt = scale_fmt, out_fmt
+        self.has_w = bool(topk_weights)
+        self.clamp_limit = clamp_limit
+        self.count_clamped = bool(count_clamped)
+        self.desc = SwigluQuantDesc(self.hidden, self.group_size, SCALE_FMTS[scale_fmt],
+                                    OUT_FMTS[out_fmt], int(self.has_w), int(clamp_limit is not None),
+                                    float(clamp_limit or 0.0), int(self.count_clamped), 0)
+        self.device = torch.cuda.current_device() if device is None else int(device)
+        self.plan = tk_swiglu_quant_plan(self.desc, self.device)
+
+    def __del__(self):
+        plan = getattr(self, "plan", None)
+        if plan:
+            try:
+                tk_swiglu_quant_plan_destroy(plan)
+            except Exception:
+                pass
+            self.plan = None
+
+    def output_shapes(self, T: int):
+        return _out_shapes(T, self.hidden, self.group_size, self.scale_fmt, self.out_fmt)
+
+    def launch_info(self, T: int) -> dict:
+        return tk_swiglu_quant_launch_info(self.plan, T)
+
+    def __call__(self, x, topk_weights=None, *, q=None, scales=None, clamped_count=None,
+                 stream=None):
+        """Enqueue on ``stream`` (default: torch's current stream); returns (q, scales)."""
+        torch = _torch()
+        T = x.shape[0]
+        _check_cuda(x, "x", torch.bfloat16, (T, 2 * self.hidden))
+        if self.has_w:
+            if topk_weights is None:
+                raise ValueError("this op was planned with top-k weights")
+            _check_cuda(topk_weights, "topk_weights", torch.float32, (T,))
+        else:
+            topk_weights = None
+        if self.count_clamped:
+            if clamped_count is None:
+                raise ValueError("this op was planned with count_clamped; pass an int64[2] tensor")
+            _check_cuda(clamped_count, "clamped_count", torch.int64, (2,))
+        else:
+            clamped_count = None
+        q_shape, s_shape, s_dtype = self.output_shapes(T)
+        if q is None:
+            q = torch.empty(q_shape, dtype=torch.uint8, device=x.device)
+        _check_cuda(q, "q", torch.uint8, q_shape)
+        if scales is None:
+            scales = torch.empty(s_shape, dtype=s_dtype, device=x.device)
+        _check_cuda(scales, "scales", s_dtype, s_shape)
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device)
+        with torch.cuda.device(x.device):
+            tk_swiglu_quant_run(self.plan, T, x, topk_weights, q, scales, clamped_count,
+                                stream.cuda_stream)
+        return q, scales
+
+
+class QuantCast:
+    """A plan for the standalone per-token / per-block cast (tk_quant_cast_plan)."""
+
+    def __init__(self, hidden: int, group_size: int = 128, scale_fmt: str = "fp32",
+                 out_fmt: str = "e4m3", in_dtype: str = "bf16", device: int | None = None):
+        torch = _torch()
+        self.hidden, self.group_size = int(hidden), int(group_size)
+        self.scale_fmt, self.out_fmt, self.in_dtype = scale_fmt, out_fmt, in_dtype
+        self.desc = QuantCastDesc(self.hidden, self.group_size, SCALE_FMTS[scale_fmt],
+                                  OUT_FMTS[out_fmt], IN_DTYPES[in_dtype])
+        self.device = torch.cuda.current_device() if device is None else int(device)
+        self.plan = tk_quant_cast_plan(self.desc, self.device)
+
+    def __del__(self):
+        plan = getattr(self, "plan", None)
+        if plan:
+            try:
+                tk_quant_cast_plan_destroy(plan)
+            except Exception:
+                pass
+            self.plan = None
+
+    def output_shapes(self, T: int):
+        return _out_shapes(T, self.hidden, self.group_size, self.scale_fmt, self.out_fmt)
+
+    def __call__(self, x, *, q=None, scales=None, stream=None):
+        torch = _torch()
+        T = x.shape[0]
+        dt = torch.bfloat16 if self.in_dtype == "bf16" else torch.float32
+        _check_cuda(x, "x", dt, (T, self.hidden))
+        q_shape, s_shape, s_dtype = self.output_shapes(T)
+        if q is None:
+            q = torch.empty(q_shape, dtype=torch.uint8, device=x.device)
+        _check_cuda(q, "q", torch.uint8, q_shape)
+        if scales is None:
+            scales = torch.empty(s_shape, dtype=s_dtype, device=x.device)
+        _check_cuda(scales, "scales", s_dtype, s_shape)
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device)
+        with torch.cuda.device(x.device):
+            tk_quant_cast_run(self.plan, T, x, q, scales, stream.cuda_stream)
+        return q, scales
+
+
+_plans: dict = {}
+_plans_lock = threading.Lock()
+
+
+def _cached(kind, key, make):
+    with _plans_lock:
+        p = _plans.get((kind, key))
+        if p is None:
+            p = _plans[(kind, key)] = make()
+        return p
+
+
+def swiglu_quant(x, topk_weights=None, *, group_size: int = 128, scale_fmt: str = "fp32",
+                 out_fmt: str = "e4m3", clamp_limit: float | None = None, clamped_count=None):
+    """Functional form: plans are cached per (shape, formats, device)."""
+    hidden = x.shape[1] // 2
+    key = (hidden, group_size, scale_fmt, out_fmt, topk_weights is not None, clamp_limit,
+           clamped_count is not None, x.device.index)
+    op = _cached("swiglu", key, lambda: SwigluQuant(
+        hidden, group_size, scale_fmt, out_fmt, topk_weights is not None, clamp_limit,
+        clamped_count is not None, x.device.index))
+    return op(x, topk_weights, clamped_count=clamped_count)
+
+
+def quant_cast(x, *, group_size: int = 128, scale_fmt: str = "fp32", out_fmt: str = "e4m3"):
+    """Functional form of the standalone cast (bf16 or fp32 input)."""
+    torch = _torch()
+    in_dtype = "bf16" if x.dtype == torch.bfloat16 else "fp32"
+    key = (x.shape[1], group_size, scale_fmt, out_fmt, in_dtype, x.device.index)
+    op = _cached("cast", key, lambda: QuantCast(x.shape[1], group_size, scale_fmt, out_fmt,
+                                                in_dtype, x.device.index))
+    return op(x)

@@ -1,0 +1,161 @@
+"""ctypes binding of include/tk_swiglu_quant.h: same names, argument
+marshalling only. Every step of the computation runs in the CUDA library;
+there is no CPU fallback. If the library is missing, loading raises."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtk_swiglu_quant.so")
+
+TK_OK = 0
+STATUS_NAMES = {0: "TK_OK", 1: "TK_ERR_INVALID_ARG", 2: "TK_ERR_UNSUPPORTED",
+                3: "TK_ERR_MISALIGNED", 4: "TK_ERR_CUDA", 5: "TK_ERR_DEVICE"}
+SCALE_FMTS = {"fp32": 0, "ue8m0": 1}
+OUT_FMTS = {"e4m3": 0, "e2m1": 1}
+IN_DTYPES = {"bf16": 0, "fp32": 1}
+
+
+class TkError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (STATUS_NAMES.get(status, status), message))
+        self.status = status
+
+
+class SwigluQuantDesc(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int64), ("group_size", ctypes.c_int32),
+                ("scale_fmt", ctypes.c_int32), ("out_fmt", ctypes.c_int32),
+                ("has_topk_weights", ctypes.c_int32), ("use_clamp", ctypes.c_int32),
+                ("clamp_limit", ctypes.c_float), ("count_clamped", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class QuantCastDesc(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int64), ("group_size", ctypes.c_int32),
+                ("scale_fmt", ctypes.c_int32), ("out_fmt", ctypes.c_int32),
+                ("in_dtype", ctypes.c_int32)]
+
+
+_VP = ctypes.c_void_p
+_P64 = ctypes.POINTER(ctypes.c_int64)
+_PINT = ctypes.POINTER(ctypes.c_int)
+_PSZ = ctypes.POINTER(ctypes.c_size_t)
+
+# name -> (restype, argtypes); mirrors the header one to one.
+SIGNATURES = {
+    "tk_swiglu_quant_validate": (ctypes.c_int, [ctypes.POINTER(SwigluQuantDesc)]),
+    "tk_swiglu_quant_plan": (ctypes.c_int, [ctypes.POINTER(SwigluQuantDesc), ctypes.c_int,
+                                            ctypes.POINTER(_VP)]),
+    "tk_swiglu_quant_plan_destroy": (ctypes.c_int, [_VP]),
+    "tk_swiglu_quant_output_sizes": (ctypes.c_int, [ctypes.POINTER(SwigluQuantDesc), ctypes.c_int64,
+                                                    _PSZ, _PSZ]),
+    "tk_swiglu_quant_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "tk_swiglu_quant_launch_info": (ctypes.c_int, [_VP, ctypes.c_int64, _PINT, _PINT, _PINT, _PINT]),
+    "tk_quant_cast_validate": (ctypes.c_int, [ctypes.POINTER(QuantCastDesc)]),
+    "tk_quant_cast_plan": (ctypes.c_int, [ctypes.POINTER(QuantCastDesc), ctypes.c_int,
+                                          ctypes.POINTER(_VP)]),
+    "tk_quant_cast_plan_destroy": (ctypes.c_int, [_VP]),
+    "tk_quant_cast_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP]),
+    "tk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "tk_last_error_message": (ctypes.c_char_p, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    "CUDA library %s is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+        return _lib
+
+
+def check(status: int) -> None:
+    if status != TK_OK:
+        msg = lib().tk_last_error_message().decode(errors="replace")
+        raise TkError(status, msg)
+
+
+def _ptr(t) -> int | None:
+    """Device address of a tensor (None stays NULL; ints pass through)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+# --------------------------------------------------------- same-name calls
+
+def tk_swiglu_quant_validate(desc: SwigluQuantDesc) -> int:
+    return lib().tk_swiglu_quant_validate(ctypes.byref(desc))
+
+
+def tk_swiglu_quant_plan(desc: SwigluQuantDesc, device: int) -> int:
+    h = _VP()
+    check(lib().tk_swiglu_quant_plan(ctypes.byref(desc), device, ctypes.byref(h)))
+    return h.value
+
+
+def tk_swiglu_quant_plan_destroy(plan: int) -> None:
+    check(lib().tk_swiglu_quant_plan_destroy(plan))
+
+
+def tk_swiglu_quant_output_sizes(desc: SwigluQuantDesc, num_tokens: int) -> tuple[int, int]:
+    qb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    check(lib().tk_swiglu_quant_output_sizes(ctypes.byref(desc), num_tokens, ctypes.byref(qb),
+                                             ctypes.byref(sb)))
+    return qb.value, sb.value
+
+
+def tk_swiglu_quant_run(plan: int, num_tokens: int, x, topk_weights, q, scales, clamped_count,
+                        stream: int | None) -> None:
+    check(lib().tk_swiglu_quant_run(plan, num_tokens, _ptr(x), _ptr(topk_weights), _ptr(q),
+                                    _ptr(scales), _ptr(clamped_count), stream))
+
+
+def tk_swiglu_quant_launch_info(plan: int, num_tokens: int) -> dict:
+    g, b, r, n = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    check(lib().tk_swiglu_quant_launch_info(plan, num_tokens, ctypes.byref(g), ctypes.byref(b),
+                                            ctypes.byref(r), ctypes.byref(n)))
+    return {"grid": g.value, "block": b.value, "rows_per_cta": r.value, "num_sms": n.value}
+
+
+def tk_quant_cast_validate(desc: QuantCastDesc) -> int:
+    return lib().tk_quant_cast_validate(ctypes.byref(desc))
+
+
+def tk_quant_cast_plan(desc: QuantCastDesc, device: int) -> int:
+    h = _VP()
+    check(lib().tk_quant_cast_plan(ctypes.byref(desc), device, ctypes.byref(h)))
+    return h.value
+
+
+def tk_quant_cast_plan_destroy(plan: int) -> None:
+    check(lib().tk_quant_cast_plan_destroy(plan))
+
+
+def tk_quant_cast_run(plan: int, num_tokens: int, x, q, scales, stream: int | None) -> None:
+    check(lib().tk_quant_cast_run(plan, num_tokens, _ptr(x), _ptr(q), _ptr(scales), stream))
+
+
+def tk_status_string(status: int) -> str:
+    return lib().tk_status_string(status).decode()
+
+
+def tk_last_error_message() -> str:
+    return lib().tk_last_error_message().decode(errors="replace")

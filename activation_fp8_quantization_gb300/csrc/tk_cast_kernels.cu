@@ -1,0 +1,51 @@
+// Instantiations of the standalone per-token / per-block cast kernel.
+#include "tk_internal.h"
+
+namespace tk {
+
+namespace {
+template <class Src, int OUT, int SCALE, bool CTA>
+const void *fn()
+{
+    return reinterpret_cast<const void *>(&row_quant_kernel<Src, OUT, SCALE, CTA>);
+}
+
+template <class Src, int OUT>
+const void *pick(int scale_fmt, bool cta)
+{
+    if (scale_fmt == kScaleF32)
+        return cta ? fn<Src, OUT, kScaleF32, true>() : fn<Src, OUT, kScaleF32, false>();
+    return cta ? fn<Src, OUT, kScaleUE8M0, true>() : fn<Src, OUT, kScaleUE8M0, false>();
+}
+
+template <class Src>
+const void *pick_out(int out_fmt, int scale_fmt, bool cta)
+{
+    if (out_fmt == kOutE4M3)
+        return pick<Src, kOutE4M3>(scale_fmt, cta);
+    if (out_fmt == kOutE2M1)
+        return pick<Src, kOutE2M1>(scale_fmt, cta);
+    return nullptr;
+}
+}  // namespace
+
+const void *cast_kernel_fn(int in_dtype, int out_fmt, int scale_fmt, bool cta_reduce)
+{
+    if (in_dtype == 0)
+        return pick_out<CastBf16Src>(out_fmt, scale_fmt, cta_reduce);
+    if (in_dtype == 1)
+        return pick_out<CastF32Src>(out_fmt, scale_fmt, cta_reduce);
+    return nullptr;
+}
+
+cudaError_t launch_cast(const void *kfn, int grid, int block, const CastArgs &a,
+                        const OutArgs &o, const RowShape &sh, cudaStream_t stream)
+{
+    CastArgs a_ = a;
+    OutArgs o_ = o;
+    RowShape sh_ = sh;
+    void *args[] = {&a_, &o_, &sh_};
+    return cudaLaunchKernel(kfn, dim3(grid), dim3(block), args, 0, stream);
+}
+
+}  // namespace tk

@@ -1,0 +1,43 @@
+// Instantiations of the fused SwiGLU + top-k weight + cast kernel.
+#include "tk_internal.h"
+
+namespace tk {
+
+namespace {
+template <int OUT, int SCALE, bool CLAMP, bool CTA>
+const void *fn()
+{
+    return reinterpret_cast<const void *>(&row_quant_kernel<SwigluSrc<CLAMP>, OUT, SCALE, CTA>);
+}
+
+template <int OUT, int SCALE>
+const void *pick(bool clamp, bool cta)
+{
+    if (clamp)
+        return cta ? fn<OUT, SCALE, true, true>() : fn<OUT, SCALE, true, false>();
+    return cta ? fn<OUT, SCALE, false, true>() : fn<OUT, SCALE, false, false>();
+}
+}  // namespace
+
+const void *swiglu_kernel_fn(int out_fmt, int scale_fmt, bool clamp, bool cta_reduce)
+{
+    if (out_fmt == kOutE4M3)
+        return scale_fmt == kScaleF32 ? pick<kOutE4M3, kScaleF32>(clamp, cta_reduce)
+                                      : pick<kOutE4M3, kScaleUE8M0>(clamp, cta_reduce);
+    if (out_fmt == kOutE2M1)
+        return scale_fmt == kScaleF32 ? pick<kOutE2M1, kScaleF32>(clamp, cta_reduce)
+                                      : pick<kOutE2M1, kScaleUE8M0>(clamp, cta_reduce);
+    return nullptr;
+}
+
+cudaError_t launch_swiglu(const void *kfn, int grid, int block, const SwigluArgs &a,
+                          const OutArgs &o, const RowShape &sh, cudaStream_t stream)
+{
+    SwigluArgs a_ = a;
+    OutArgs o_ = o;
+    RowShape sh_ = sh;
+    void *args[] = {&a_, &o_, &sh_};
+    return cudaLaunchKernel(kfn, dim3(grid), dim3(block), args, 0, stream);
+}
+
+}  // namespace tk

@@ -1,0 +1,461 @@
+#!/usr/bin/env python
+"""Benchmark of the fused SwiGLU + MoE top-k weight + FP8 cast on GB300.
+
+One step = one launch of the fused kernel over one batch of the workload
+(default: T=8192 expanded rows, H=2048, 1x128 fp32 scales, E4M3 codes, top-k
+weights; synthetic inputs from workloads.py). Prints ONE JSON line on rank 0.
+
+  value     tokens/s over all ranks, device-timed with CUDA events around K
+            back-to-back launches (replayed from a CUDA graph) on the
+            launching stream, inputs resident in HBM. L2 (129 MB) is defeated
+            by rotating several input/output sets whose total is > 2x L2, so
+            every launch reads cold inputs and also evicts the previous
+            launch's dirty outputs (steady state).
+  roofline  algorithmic bytes per launch / average launch time vs the
+            measured HBM copy bandwidth.
+  e2e       the same metric through the C ABI with pinned host buffers: every
+            step copies its inputs host->device and its codes and scales back.
+  cpu_baseline  the CPU oracle on a bounded sample of rows (rank 0, N=1).
+
+--impl reference times the CPU oracle itself (the only reference this method
+has: the pages ship no runnable code), on the same workload and metric.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (rows are
+independent, so the work shards with no collective); value sums the ranks'
+rows over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s and achieved HBM GB/s (fraction of GB300 peak) for fused SwiGLU+FP8 cast"
+DEFAULT_WORKLOAD = "moe_T8192_H2048_g128"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle sample for cpu_baseline")
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--jsonl", default=None, help="also append the JSON line to this file")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------ distributed
+
+class Dist:
+    def __init__(self, backend: str):
+        import torch.distributed as dist
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = dist if self.world > 1 else None
+        if self.dist is not None and not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, v: float, device=None) -> float:
+        if self.dist is None:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, v: float, device=None) -> float:
+        if self.dist is None:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+class RankOnly:
+    """Rank identity without a process group (the CPU reference arm)."""
+
+    def __init__(self):
+        self.rank = int(os.environ.get("RANK", "0"))
+
+
+# ----------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 50 ms while the timed region runs."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(", ") for ln in self.file.read().splitlines() if ln.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < len(CLOCK_FIELDS):
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ peaks
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def time_oracle(wl, seconds: float, seed_rows: int = 8) -> dict:
+    """Time the CPU oracle on a bounded row sample of the workload: a short
+    calibration, then a sample sized to about `seconds` of single-core work."""
+    import numpy as np
+    import oracle
+    from activation_fp8_quantization_gb300 import workloads as wls
+
+    lib = oracle.load()
+    small = wl.with_rows(max(8, seed_rows))
+    x, w = wls.make_inputs(small, "cpu")
+    xb = wls.bf16_bits(x)
+    wn = None if w is None else w.numpy()
+    t = time.perf_counter()
+    oracle.swiglu_quant(xb, wn, wl.group, wl.scale_fmt, wl.out_fmt, clamp=wl.clamp, lib=lib)
+    per_row = (time.perf_counter() - t) / small.T
+    rows = int(max(8, min(wl.T, seconds / max(per_row, 1e-9))))
+    rows = max(8, (rows // 8) * 8)
+    sample = wl.with_rows(rows)
+    x, w = wls.make_inputs(sample, "cpu")
+    xb = wls.bf16_bits(x)
+    wn = None if w is None else w.numpy()
+    t = time.perf_counter()
+    oracle.swiglu_quant(xb, wn, wl.group, wl.scale_fmt, wl.out_fmt, clamp=wl.clamp, lib=lib)
+    dt = time.perf_counter() - t
+    return {"rows": rows, "seconds": dt, "tokens_per_s": rows / dt,
+            "gbs": wl.algo_bytes(rows) / dt / 1e9}
+
+
+def run_reference(args, dist):
+    """--impl reference: the CPU oracle as it stands, on the host cores."""
+    from activation_fp8_quantization_gb300 import workloads as wls
+    import numpy as np
+    import oracle
+
+    if dist.rank != 0:
+        return 0
+    wl = wls.WORKLOADS[args.workload]
+    lib = oracle.load()
+    # one step = a bounded sample of the workload; size it so K + W steps fit in ~2 minutes
+    calib = time_oracle(wl, 0.5)
+    per_row = calib["seconds"] / calib["rows"]
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(8, min(wl.T, budget / per_row)))
+    sample = wl.with_rows(rows)
+    x, w = wls.make_inputs(sample, "cpu")
+    xb = wls.bf16_bits(x)
+    wn = None if w is None else w.numpy()
+
+    def step():
+        oracle.swiglu_quant(xb, wn, wl.group, wl.scale_fmt, wl.out_fmt, clamp=wl.clamp, lib=lib)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    value = rows * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64/f32", "data": "synthetic",
+        "config": config_of(wl, args.gpus),
+        "hbm_gbs": wl.algo_bytes(rows) * args.steps / dt / 1e9,
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d of %d rows per step, single-threaded C oracle" % (rows, wl.T)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    emit(line, args)
+    return 0
+
+
+def config_of(wl, n: int) -> dict:
+    return {"workload": wl.name, "T": wl.T, "H": wl.H, "group": wl.group, "scale_fmt": wl.scale_fmt,
+            "out_fmt": wl.out_fmt, "topk_weights": wl.w_dist is not None, "clamp": wl.clamp,
+            "parallelism": "replicas x%d" % n}
+
+
+def emit(line: dict, args):
+    s = json.dumps(line)
+    print(s, flush=True)
+    if args.jsonl:
+        with open(args.jsonl, "a") as f:
+            f.write(s + "\n")
+
+
+# ------------------------------------------------------------- GPU timing
+
+def run_ours(args, dist: Dist):
+    import torch
+    import activation_fp8_quantization_gb300 as tk
+    from activation_fp8_quantization_gb300 import _abi
+    from activation_fp8_quantization_gb300 import workloads as wls
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = dist.local_rank
+    torch.cuda.set_device(dev)
+    wl = wls.WORKLOADS[args.workload]
+    T, H = wl.T, wl.H
+    op = tk.SwigluQuant(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.w_dist is not None, wl.clamp,
+                        wl.clamp is not None, dev)
+    algo = wl.algo_bytes()
+    per_set = algo
+    n_sets = max(2, -(-3 * L2_BYTES // per_set) + 1)   # sets beyond the current one hold > 3x L2
+
+    x0, w0 = wls.make_inputs(wl, "cuda")
+    q_shape, s_shape, s_dtype = op.output_shapes(T)
+    xs, ws, qs, ss = [], [], [], []
+    for i in range(n_sets):
+        xs.append(x0 if i == 0 else x0.clone())
+        ws.append(None if w0 is None else (w0 if i == 0 else w0.clone()))
+        qs.append(torch.empty(q_shape, dtype=torch.uint8, device=dev))
+        ss.append(torch.empty(s_shape, dtype=s_dtype, device=dev))
+    counts = torch.zeros(2, dtype=torch.int64, device=dev) if op.count_clamped else None
+    lib = _abi.lib()
+    run = lib.tk_swiglu_quant_run
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    cp = None if counts is None else counts.data_ptr()
+    ptrs = [(xs[i].data_ptr(), None if ws[i] is None else ws[i].data_ptr(), qs[i].data_ptr(),
+             ss[i].data_ptr()) for i in range(n_sets)]
+
+    def launch(i):
+        xp, wp, qp, spp = ptrs[i % n_sets]
+        st = run(op.plan, T, xp, wp, qp, spp, cp, sh)
+        if st != 0:
+            raise tk.TkError(st, _abi.tk_last_error_message())
+
+    # warm-up, then a CUDA graph holding `chunk` back-to-back launches
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            launch(i)
+    stream.synchronize()
+    chunk = min(args.steps, n_sets * max(1, 600 // n_sets))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(chunk):
+            launch(i)
+    reps, rem = divmod(args.steps, chunk)
+    with torch.cuda.stream(stream):
+        graph.replay()      # one untimed replay: graph upload and clocks up
+    stream.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device()) if dist.local_rank == 0 else None
+    if clocks:
+        clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        for i in range(rem):
+            launch(i)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop() if clocks else None
+    ms_max = dist.max(ms, device=dev)
+    ms_per_step = ms_max / args.steps
+    rows_total = dist.sum(float(T * args.steps), device=dev)
+    value = rows_total / (ms_max / 1e3)
+    achieved = algo / (ms_per_step / 1e3) / 1e9
+    peaks = measured_peaks()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(op, wl, x0, w0, dev, args, dist)
+
+    cpu = None
+    if dist.rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
+        r = time_oracle(wl, args.cpu_seconds)
+        cpu = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": "%d of %d rows of the same workload, single-threaded C oracle, %.1f s"
+                         % (r["rows"], wl.T, r["seconds"])}
+    if dist.rank != 0:
+        return 0
+    traffic = load_traffic(wl.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {**config_of(wl, args.gpus),
+                   "l2": "inputs larger than L2: %d rotating input/output sets, %.0f MB" % (
+                       n_sets, n_sets * per_set / 1e6)},
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": peaks["source"], "algo_bytes_per_launch": algo},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    emit(line, args)
+    return 0
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary for this workload
+    and the current kernel, if one exists (profiles/<workload>.traffic.json)."""
+    path = os.path.join(ROOT, "profiles", "swiglu_quant_%s.traffic.json" % workload)
+    try:
+        with open(path) as f:
+            return json.load(f).get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        return None
+
+
+def measure_e2e(op, wl, x0, w0, dev, args, dist: Dist):
+    """The same metric through the public call with pinned host buffers: per
+    step, copy x (and w) host->device, run, copy codes and scales back."""
+    import torch
+
+    T = wl.T
+    x_h = x0.cpu().pin_memory()
+    w_h = None if w0 is None else w0.cpu().pin_memory()
+    q_shape, s_shape, s_dtype = op.output_shapes(T)
+    q_h = torch.empty(q_shape, dtype=torch.uint8).pin_memory()
+    s_h = torch.empty(s_shape, dtype=s_dtype).pin_memory()
+    x_d = torch.empty_like(x0)
+    w_d = None if w0 is None else torch.empty_like(w0)
+    q_d = torch.empty(q_shape, dtype=torch.uint8, device=dev)
+    s_d = torch.empty(s_shape, dtype=s_dtype, device=dev)
+    counts = torch.zeros(2, dtype=torch.int64, device=dev) if op.count_clamped else None
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        x_d.copy_(x_h, non_blocking=True)
+        if w_d is not None:
+            w_d.copy_(w_h, non_blocking=True)
+        op(x_d, w_d, q=q_d, scales=s_d, clamped_count=counts, stream=stream)
+        q_h.copy_(q_d, non_blocking=True)
+        s_h.copy_(s_d, non_blocking=True)
+
+    n = max(1, args.e2e_steps)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    stream.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(n):
+            step()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms = dist.max(ev0.elapsed_time(ev1), device=dev)
+    rows_total = dist.sum(float(T * n), device=dev)
+    h2d = x_h.numel() * x_h.element_size() + (0 if w_h is None else w_h.numel() * 4)
+    d2h = q_h.numel() + s_h.numel() * s_h.element_size()
+    return {"value": rows_total / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
+            "path": "SwigluQuant call on pinned host buffers, copies on the launch stream"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        # rank 0 alone times the CPU oracle; other ranks exit without work
+        return run_reference(args, RankOnly())
+    dist = Dist("nccl")
+    try:
+        return run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

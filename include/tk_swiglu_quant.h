@@ -1,0 +1,168 @@
+/*
+ * tk_swiglu_quant.h -- C ABI of the fused SwiGLU + MoE top-k weight +
+ * FP8/FP4 activation cast, and of the standalone per-token / per-block cast.
+ *
+ * The operation ("TileKernels从入门到精通" / "TileKernels from Beginner to
+ * Master", zhichai.net/topic/177618752 and zhichai.net/en/topic/177618752,
+ * chapter 2): every row r of x [T, 2H] (bf16, row-major) is one expanded
+ * (token, expert) pair; its gate half g = x[r, 0:H] and up half u = x[r, H:2H]
+ * ("conjoined twin" layout) give
+ *
+ *     y[r, i] = silu(g') * u' * w[r],   silu(z) = z / (1 + exp(-z)),
+ *     g' = min(g, L),  u' = clamp(u, -L, L)          (only with use_clamp),
+ *
+ * computed in fp32 registers. y is cut into groups of `group_size` columns
+ * (or one group per row); each group gets a scale from its absolute maximum
+ * amax -- fp32 s = amax / Qmax, or UE8M0 s = 2^k with k the smallest integer
+ * such that Qmax * 2^k >= amax -- and each value is stored as the
+ * round-to-nearest-even, saturating code of y / s in FP8 E4M3 (Qmax = 448) or
+ * FP4 E2M1 (Qmax = 6). Formats and granularities: "TileLang + TileKernels：
+ * DeepSeek 的 GPU 内核开发新范式" (zhichai.net/topic/177618740), section
+ * "3. Quantization", format table. Clamp guard and its counter: same chapter 2,
+ * "守门员 Clamp". The standalone cast is the same scaling and encoding applied
+ * to an input that is already the activation (ch.1, per_token_cast).
+ *
+ * Conventions for every entry point:
+ *  - Device pointers are CUDA global-memory addresses on the plan's device,
+ *    owned by the caller; the library never frees or retains them.
+ *  - Calls are stream-ordered and asynchronous: they enqueue work on `stream`
+ *    (a cudaStream_t passed as void*, NULL = the legacy default stream) and
+ *    return without synchronising. Errors detected on the host are returned
+ *    before anything is enqueued.
+ *  - A plan is immutable once made and may be used from several host threads
+ *    and streams at once. It holds host state only (the descriptor, the device
+ *    ordinal, the launch shape); destroying it does not touch device memory.
+ *  - On any status other than TK_OK, tk_last_error_message() returns a
+ *    description for the calling thread.
+ */
+#ifndef TK_SWIGLU_QUANT_H
+#define TK_SWIGLU_QUANT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tk_status {
+    TK_OK = 0,
+    TK_ERR_INVALID_ARG = 1,  /* null where a pointer is required, negative size, bad enum */
+    TK_ERR_UNSUPPORTED = 2,  /* well-formed but outside what is implemented (e.g. hidden > 16384) */
+    TK_ERR_MISALIGNED = 3,   /* a pointer breaks the alignment rules of the call */
+    TK_ERR_CUDA = 4,         /* a CUDA runtime call failed (message has the CUDA error) */
+    TK_ERR_DEVICE = 5        /* the calling thread's current device is not the plan's device */
+} tk_status;
+
+typedef enum tk_scale_fmt {
+    TK_SCALE_FP32 = 0,   /* one fp32 per group: amax / Qmax (1.0 if that is zero) */
+    TK_SCALE_UE8M0 = 1   /* one byte per group: k + 127, scale 2^k (byte 127 for amax == 0) */
+} tk_scale_fmt;
+
+typedef enum tk_out_fmt {
+    TK_OUT_E4M3 = 0,     /* one byte per value, OCP FP8 E4M3 (max 448, no inf) */
+    TK_OUT_E2M1 = 1      /* two values per byte, OCP FP4 E2M1 (max 6); value 2k in the low nibble */
+} tk_out_fmt;
+
+typedef enum tk_in_dtype {
+    TK_IN_BF16 = 0,
+    TK_IN_FP32 = 1
+} tk_in_dtype;
+
+/* ------------------------------------------------------------------------
+ * Fused SwiGLU + top-k weight + cast
+ * ---------------------------------------------------------------------- */
+
+typedef struct tk_swiglu_quant_desc {
+    int64_t hidden;            /* H: width of the output; x rows hold 2H bf16. 16 <= H <= 16384, H % 16 == 0 */
+    int32_t group_size;        /* columns per scale: 16, 32, 64, 128, 256 or 512 (dividing H); 0 = one per row */
+    int32_t scale_fmt;         /* tk_scale_fmt */
+    int32_t out_fmt;           /* tk_out_fmt */
+    int32_t has_topk_weights;  /* 1: run() takes fp32 weights [T]; 0: weight 1 */
+    int32_t use_clamp;         /* 1: gate <= clamp_limit, up in [-clamp_limit, clamp_limit] */
+    float clamp_limit;         /* finite, >= 0; read only when use_clamp */
+    int32_t count_clamped;     /* 1: run() ADDS the clamp counts into a device int64[2]; needs use_clamp */
+    int32_t reserved;          /* must be 0 */
+} tk_swiglu_quant_desc;
+
+typedef struct tk_swiglu_quant_plan_s *tk_swiglu_quant_plan_t;
+
+/* Check a descriptor on the host only (no CUDA call). TK_OK,
+ * TK_ERR_INVALID_ARG or TK_ERR_UNSUPPORTED. */
+tk_status tk_swiglu_quant_validate(const tk_swiglu_quant_desc *desc);
+
+/* Validate desc, query device `device` (SM count, occupancy) and pick the
+ * kernel and launch shape. On TK_OK *plan owns a host allocation released by
+ * tk_swiglu_quant_plan_destroy. Does not change the current device. */
+tk_status tk_swiglu_quant_plan(const tk_swiglu_quant_desc *desc, int device,
+                               tk_swiglu_quant_plan_t *plan);
+
+/* Release a plan (NULL is accepted). The plan must not be used afterwards. */
+tk_status tk_swiglu_quant_plan_destroy(tk_swiglu_quant_plan_t plan);
+
+/* Bytes of the code and scale outputs for num_tokens rows (host only):
+ * q: T*H (E4M3) or T*H/2 (E2M1); scales: T*G*4 (fp32) or T*G (UE8M0), with
+ * G = H / group_size (1 when group_size == 0). */
+tk_status tk_swiglu_quant_output_sizes(const tk_swiglu_quant_desc *desc, int64_t num_tokens,
+                                       size_t *q_bytes, size_t *scale_bytes);
+
+/* Enqueue the fused kernel.
+ *   x             [T, 2H] bf16, row-major, gate half first; 32-byte aligned
+ *   topk_weights  [T] fp32, 4-byte aligned; required iff has_topk_weights, else ignored
+ *   q             codes, [T, H] or [T, H/2] bytes, row-major; 16-byte aligned
+ *   scales        [T, G] fp32 (4-byte aligned) or uint8, row-major
+ *   clamped_count device int64[2], 8-byte aligned: [0] += gate values above
+ *                 the limit, [1] += up values outside [-L, L]; required iff
+ *                 count_clamped, else ignored. The caller zeroes it.
+ * num_tokens == 0 enqueues nothing and returns TK_OK. The calling thread's
+ * current device must be the plan's device (TK_ERR_DEVICE otherwise). Inputs
+ * and outputs must not overlap. */
+tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t num_tokens,
+                              const void *x, const float *topk_weights, void *q,
+                              void *scales, int64_t *clamped_count, void *stream);
+
+/* Launch shape the plan chose (host only): CTAs in the persistent grid, threads
+ * per CTA, rows one CTA processes per iteration, and the SM count used. */
+tk_status tk_swiglu_quant_launch_info(tk_swiglu_quant_plan_t plan, int64_t num_tokens,
+                                      int *grid, int *block, int *rows_per_cta, int *num_sms);
+
+/* ------------------------------------------------------------------------
+ * Standalone per-token / per-block cast: x [T, H] (bf16 or fp32) -> codes + scales,
+ * with the same grouping, scale and code rules as the fused call.
+ * ---------------------------------------------------------------------- */
+
+typedef struct tk_quant_cast_desc {
+    int64_t hidden;      /* H: 16 <= H <= 16384, H % 16 == 0 */
+    int32_t group_size;  /* as in tk_swiglu_quant_desc */
+    int32_t scale_fmt;   /* tk_scale_fmt */
+    int32_t out_fmt;     /* tk_out_fmt */
+    int32_t in_dtype;    /* tk_in_dtype */
+} tk_quant_cast_desc;
+
+typedef struct tk_quant_cast_plan_s *tk_quant_cast_plan_t;
+
+tk_status tk_quant_cast_validate(const tk_quant_cast_desc *desc);
+tk_status tk_quant_cast_plan(const tk_quant_cast_desc *desc, int device, tk_quant_cast_plan_t *plan);
+tk_status tk_quant_cast_plan_destroy(tk_quant_cast_plan_t plan);
+
+/* Enqueue the cast. x [T, H] row-major, 32-byte aligned; q, scales as in
+ * tk_swiglu_quant_run. num_tokens == 0 is a no-op. */
+tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t num_tokens, const void *x,
+                            void *q, void *scales, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics
+ * ---------------------------------------------------------------------- */
+
+/* Static name of a status ("TK_OK", ...). Never NULL. */
+const char *tk_status_string(tk_status status);
+
+/* Message of the last non-OK status returned on the calling thread ("" if
+ * none). Valid until the next call into this library on the same thread. */
+const char *tk_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TK_SWIGLU_QUANT_H */

@@ -1,0 +1,112 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+entry point the header declares, and its host-side checks answer without
+touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import activation_fp8_quantization_gb300 as tk
+from activation_fp8_quantization_gb300 import _abi
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "tk_swiglu_quant.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tk_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding():
+    names = declared_functions()
+    assert len(names) >= 12
+    assert set(names) == set(_abi.SIGNATURES), set(names) ^ set(_abi.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _abi.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    raw = ctypes.CDLL(_abi.LIB_PATH)
+    for name in declared_functions():
+        assert ctypes.cast(getattr(raw, name), ctypes.c_void_p).value
+
+
+def D(**kw):
+    base = dict(hidden=2048, group_size=128, scale_fmt=0, out_fmt=0, has_topk_weights=1,
+                use_clamp=0, clamp_limit=0.0, count_clamped=0, reserved=0)
+    base.update(kw)
+    return tk.SwigluQuantDesc(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, 0),
+    (dict(group_size=0), 0),
+    (dict(group_size=32, out_fmt=1, scale_fmt=1), 0),
+    (dict(hidden=16384, group_size=512), 0),
+    (dict(hidden=0), 1),
+    (dict(hidden=-16), 1),
+    (dict(hidden=2040), 2),
+    (dict(hidden=16400), 2),
+    (dict(group_size=-1), 1),
+    (dict(group_size=96), 2),
+    (dict(group_size=1024), 2),
+    (dict(hidden=2064, group_size=128), 2),
+    (dict(scale_fmt=2), 1),
+    (dict(out_fmt=5), 1),
+    (dict(has_topk_weights=2), 1),
+    (dict(use_clamp=1, clamp_limit=float("nan")), 1),
+    (dict(use_clamp=1, clamp_limit=float("inf")), 1),
+    (dict(use_clamp=1, clamp_limit=-1.0), 1),
+    (dict(use_clamp=1, clamp_limit=7.0, count_clamped=1), 0),
+    (dict(count_clamped=1), 1),
+    (dict(reserved=3), 1),
+])
+def test_validate(kw, status):
+    assert tk.tk_swiglu_quant_validate(D(**kw)) == status
+    if status:
+        assert tk.tk_last_error_message()
+
+
+def test_cast_validate():
+    C = tk.QuantCastDesc
+    assert tk.tk_quant_cast_validate(C(4096, 128, 0, 0, 0)) == 0
+    assert tk.tk_quant_cast_validate(C(4096, 0, 1, 1, 1)) == 0
+    assert tk.tk_quant_cast_validate(C(4096, 128, 0, 0, 2)) == 1
+    assert tk.tk_quant_cast_validate(C(100, 0, 0, 0, 0)) == 2
+
+
+def test_output_sizes():
+    assert tk.tk_swiglu_quant_output_sizes(D(), 8192) == (8192 * 2048, 8192 * 16 * 4)
+    assert tk.tk_swiglu_quant_output_sizes(D(group_size=32, scale_fmt=1, out_fmt=1), 65536) == (
+        65536 * 1024, 65536 * 64)
+    assert tk.tk_swiglu_quant_output_sizes(D(group_size=0), 256) == (256 * 2048, 256 * 4)
+    assert tk.tk_swiglu_quant_output_sizes(D(), 0) == (0, 0)
+    with pytest.raises(tk.TkError):
+        tk.tk_swiglu_quant_output_sizes(D(), -1)
+
+
+def test_null_handling_and_status_strings():
+    lib = _abi.lib()
+    assert lib.tk_swiglu_quant_run(None, 4, None, None, None, None, None, None) == 1
+    assert lib.tk_quant_cast_run(None, 4, None, None, None, None) == 1
+    assert lib.tk_swiglu_quant_validate(None) == 1
+    assert lib.tk_swiglu_quant_plan_destroy(None) == 0
+    assert lib.tk_swiglu_quant_plan(ctypes.byref(D()), 0, None) == 1
+    for s, n in _abi.STATUS_NAMES.items():
+        assert tk.tk_status_string(s) == n
+
+
+def test_plan_without_gpu_reports_cuda_error():
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+    except ImportError:
+        pass
+    with pytest.raises(tk.TkError) as e:
+        tk.tk_swiglu_quant_plan(D(), 0)
+    assert e.value.status in (1, 4)

@@ -1,0 +1,267 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI.
+
+Small cases take each workload's shape, formats and value distribution at a
+row count that makes every CTA of the persistent grid walk two row blocks and
+leaves a ragged tail; the oracle computes every row. Full-size cases run the
+exact launch the benchmark times and compare sampled rows (first, last and
+random ones) with the oracle, plus properties checked on every row.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import compare, unpack
+
+import activation_fp8_quantization_gb300 as tk
+from activation_fp8_quantization_gb300 import workloads as wls
+
+pytestmark = pytest.mark.gpu
+
+
+def _op(wl, count=False):
+    return tk.SwigluQuant(wl.H, wl.group, wl.scale_fmt, wl.out_fmt, wl.w_dist is not None,
+                          wl.clamp, count and wl.clamp is not None)
+
+
+def _run(op, x, w, counts=None):
+    q, s = op(x, w, clamped_count=counts)
+    torch.cuda.synchronize()
+    return q, s
+
+
+def _oracle(wl, x_cpu, w_cpu):
+    return oracle.swiglu_quant(wls.bf16_bits(x_cpu), None if w_cpu is None else w_cpu.numpy(),
+                               wl.group, wl.scale_fmt, wl.out_fmt, clamp=wl.clamp, want_y=True)
+
+
+@pytest.mark.parametrize("name", wls.ORDER)
+def test_workload_small_parity(name):
+    wl = wls.WORKLOADS[name]
+    op = _op(wl, count=True)
+    info = op.launch_info(1 << 30)
+    rows = 2 * info["grid"] * info["rows_per_cta"] + 37
+    wl_s = wl.with_rows(rows)
+    x, w = wls.make_inputs(wl_s, "cpu")
+    counts = torch.zeros(2, dtype=torch.int64, device="cuda")
+    q, s = _run(op, x.cuda(), None if w is None else w.cuda(), counts if op.count_clamped else None)
+    ref = _oracle(wl, x, w)
+    rep = compare(q.cpu().numpy(), s.cpu().numpy(), ref, wl.group, wl.scale_fmt, wl.out_fmt)
+    rep.check(name)
+    if op.count_clamped:
+        assert counts.cpu().tolist() == ref["counts"].tolist()
+    print(name, rows, "rows: identical %.6f, boundary groups %d, flips %d" % (
+        rep.identical_frac, rep.n_boundary_groups, rep.n_boundary_flips))
+
+
+def _torch_counts(x, H, L):
+    g = x[:, :H].float()
+    u = x[:, H:].float()
+    return [int((g > L).sum().item()), int((u.abs() > L).sum().item())]
+
+
+@pytest.mark.parametrize("name", wls.ORDER)
+def test_workload_full_size(name):
+    wl = wls.WORKLOADS[name]
+    op = _op(wl, count=True)
+    x, w = wls.make_inputs(wl, "cuda")
+    counts = torch.zeros(2, dtype=torch.int64, device="cuda")
+    q, s = _run(op, x, w, counts if op.count_clamped else None)
+    T, H = wl.T, wl.H
+    # properties of every row
+    qc = q.to(torch.int32)
+    if wl.out_fmt == "e4m3":
+        assert not ((qc & 0x7F) == 0x7F).any(), "NaN code written"
+    if wl.scale_fmt == "fp32":
+        assert bool((s > 0).all())
+        if wl.out_fmt == "e4m3":
+            g = H if wl.group == 0 else wl.group
+            top = ((qc & 0x7F) == 0x7E).view(T, H // g, g).any(dim=2)
+            assert bool(top.all()), "a group has no element at +-448"
+    else:
+        assert int(s.max()) <= 254
+    if op.count_clamped:
+        assert counts.cpu().tolist() == _torch_counts(x, H, wl.clamp)
+    # sampled rows against the oracle
+    gen = np.random.default_rng(wl.seed)
+    idx = np.unique(np.concatenate([np.arange(64), np.arange(T - 64, T),
+                                    gen.choice(T, size=min(T, 768), replace=False)]))
+    it = torch.from_numpy(idx).cuda()
+    xs = x.index_select(0, it).cpu()
+    ws = None if w is None else w.index_select(0, it).cpu()
+    ref = _oracle(wl, xs, ws)
+    rep = compare(q.index_select(0, it).cpu().numpy(), s.index_select(0, it).cpu().numpy(), ref,
+                  wl.group, wl.scale_fmt, wl.out_fmt)
+    rep.check(name + " full")
+    print(name, "full: %d sampled rows, identical %.6f" % (len(idx), rep.identical_frac))
+
+
+# ------------------------------------------------------------- edge cases
+
+GEOMS = [  # (H, group) incl. the CTA-reduction path (one scale per row, wide or odd rows)
+    (16, 16), (16, 0), (48, 16), (48, 0), (80, 16), (512, 0), (512, 512), (1040, 16),
+    (2048, 64), (2048, 256), (4096, 0), (7168, 128), (7168, 0), (16384, 512), (16384, 0),
+]
+
+
+@pytest.mark.parametrize("H,group", GEOMS)
+@pytest.mark.parametrize("scale_fmt,out_fmt", [("fp32", "e4m3"), ("ue8m0", "e4m3"),
+                                               ("ue8m0", "e2m1"), ("fp32", "e2m1")])
+def test_geometry_sweep(H, group, scale_fmt, out_fmt):
+    rng = np.random.default_rng(H * 7 + group)
+    T = 29
+    x = torch.from_numpy(rng.standard_normal((T, 2 * H)).astype(np.float32) * 2).to(torch.bfloat16)
+    w = torch.from_numpy(rng.uniform(0.0, 1.0, T).astype(np.float32))
+    op = tk.SwigluQuant(H, group, scale_fmt, out_fmt, True, 3.0, True)
+    counts = torch.zeros(2, dtype=torch.int64, device="cuda")
+    q, s = _run(op, x.cuda(), w.cuda(), counts)
+    ref = oracle.swiglu_quant(wls.bf16_bits(x), w.numpy(), group, scale_fmt, out_fmt, clamp=3.0,
+                              want_y=True)
+    compare(q.cpu().numpy(), s.cpu().numpy(), ref, group, scale_fmt, out_fmt).check((H, group))
+    assert counts.cpu().tolist() == ref["counts"].tolist()
+
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
+
+
+def test_special_rows():
+    H, g = 256, 128
+    rows = []
+    rows.append(np.zeros(2 * H))                                            # all zero
+    rows.append(np.concatenate([np.full(H, -95.0), np.full(H, 3.0)]))      # silu underflows to subnormals
+    rows.append(np.concatenate([np.full(H, 1e-20), np.full(H, 1e-20)]))    # y ~ 1e-40: subnormal amax
+    rows.append(np.concatenate([np.full(H, 2.0), np.full(H, -2.0)]))       # equal magnitudes
+    one_hot = np.zeros(2 * H)
+    one_hot[5], one_hot[H + 5] = 3.0, 1.0
+    rows.append(one_hot)
+    big = np.concatenate([np.full(H, 1e18), np.linspace(-1e18, 1e18, H)])
+    rows.append(big)
+    rng = np.random.default_rng(0)
+    rows.append(rng.standard_normal(2 * H) * 1e-3)
+    x = _bf16(np.stack(rows))
+    for scale_fmt in ("fp32", "ue8m0"):
+        for out_fmt in ("e4m3", "e2m1"):
+            op = tk.SwigluQuant(H, g, scale_fmt, out_fmt, False)
+            q, s = _run(op, x.cuda(), None)
+            ref = oracle.swiglu_quant(wls.bf16_bits(x), None, g, scale_fmt, out_fmt, want_y=True)
+            compare(q.cpu().numpy(), s.cpu().numpy(), ref, g, scale_fmt, out_fmt).check(
+                "special %s %s" % (scale_fmt, out_fmt))
+
+
+def test_zero_rows_is_noop_and_tails():
+    H = 512
+    op = tk.SwigluQuant(H, 128, "fp32", "e4m3", True)
+    x = torch.zeros(0, 2 * H, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(0, dtype=torch.float32, device="cuda")
+    q, s = _run(op, x, w)
+    assert q.shape == (0, H) and s.shape == (0, 4)
+    for T in (1, 2, 3, 5, 17):
+        xr = _bf16(np.random.default_rng(T).standard_normal((T, 2 * H)))
+        wr = torch.rand(T)
+        q, s = _run(op, xr.cuda(), wr.cuda())
+        ref = oracle.swiglu_quant(wls.bf16_bits(xr), wr.numpy(), 128, "fp32", "e4m3", want_y=True)
+        compare(q.cpu().numpy(), s.cpu().numpy(), ref, 128, "fp32", "e4m3").check("T=%d" % T)
+
+
+def test_guard_bands_untouched():
+    """Outputs live inside larger buffers filled with a sentinel; only the
+    output bytes may change."""
+    H, T, g = 1024, 301, 32
+    for scale_fmt, out_fmt in (("fp32", "e4m3"), ("ue8m0", "e2m1")):
+        op = tk.SwigluQuant(H, g, scale_fmt, out_fmt, True, 7.0, False)
+        q_shape, s_shape, s_dtype = op.output_shapes(T)
+        pad = 256
+        qn = q_shape[0] * q_shape[1]
+        qbuf = torch.full((qn + 2 * pad,), 0xA5, dtype=torch.uint8, device="cuda")
+        q = qbuf[pad:pad + qn].view(q_shape)
+        sn = s_shape[0] * s_shape[1]
+        sbuf = torch.full((sn + 2 * pad,), -7.0 if s_dtype == torch.float32 else 0x5A,
+                          dtype=s_dtype, device="cuda")
+        s = sbuf[pad:pad + sn].view(s_shape)
+        x = _bf16(np.random.default_rng(1).standard_normal((T, 2 * H)) * 4).cuda()
+        w = torch.rand(T, device="cuda")
+        op(x, w, q=q, scales=s)
+        torch.cuda.synchronize()
+        assert bool((qbuf[:pad] == 0xA5).all()) and bool((qbuf[pad + qn:] == 0xA5).all())
+        fill = -7.0 if s_dtype == torch.float32 else 0x5A
+        assert bool((sbuf[:pad] == fill).all()) and bool((sbuf[pad + sn:] == fill).all())
+
+
+def test_clamp_counter_accumulates_and_streams():
+    wl = wls.WORKLOADS["moe_T32768_H2048_g128_ue8m0_clamp7"].with_rows(4096)
+    x, w = wls.make_inputs(wl, "cuda")
+    op = _op(wl, count=True)
+    counts = torch.zeros(2, dtype=torch.int64, device="cuda")
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for st in streams:
+        with torch.cuda.stream(st):
+            outs.append(op(x, w, clamped_count=counts, stream=st))
+    torch.cuda.synchronize()
+    one = _torch_counts(x, wl.H, wl.clamp)
+    assert counts.cpu().tolist() == [2 * one[0], 2 * one[1]]
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_host_side_errors():
+    H = 256
+    op = tk.SwigluQuant(H, 128, "fp32", "e4m3", True, 7.0, True)
+    x = torch.zeros(8, 2 * H + 16, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(8, device="cuda")
+    q = torch.empty(8, H, dtype=torch.uint8, device="cuda")
+    s = torch.empty(8, 2, device="cuda")
+    c = torch.zeros(2, dtype=torch.int64, device="cuda")
+    base = x.data_ptr()
+    with pytest.raises(tk.TkError) as e:   # x not 32-byte aligned
+        tk.tk_swiglu_quant_run(op.plan, 8, base + 2, w, q, s, c, None)
+    assert e.value.status == 3
+    with pytest.raises(tk.TkError) as e:   # q not 16-byte aligned
+        tk.tk_swiglu_quant_run(op.plan, 8, base, w, q.data_ptr() + 1, s, c, None)
+    assert e.value.status == 3
+    with pytest.raises(tk.TkError) as e:   # weights expected
+        tk.tk_swiglu_quant_run(op.plan, 8, base, None, q, s, c, None)
+    assert e.value.status == 1
+    with pytest.raises(tk.TkError) as e:   # counter expected
+        tk.tk_swiglu_quant_run(op.plan, 8, base, w, q, s, None, None)
+    assert e.value.status == 1
+    with pytest.raises(tk.TkError) as e:
+        tk.tk_swiglu_quant_run(op.plan, -1, base, w, q, s, c, None)
+    assert e.value.status == 1
+    with pytest.raises(tk.TkError) as e:
+        tk.tk_swiglu_quant_plan(tk.SwigluQuantDesc(H, 128, 0, 0, 1, 0, 0.0, 0, 0), 4096)
+    assert e.value.status == 1
+    torch.cuda.synchronize()
+
+
+# ----------------------------------------------------- standalone cast
+
+@pytest.mark.parametrize("in_dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("H,group", [(2048, 128), (512, 0), (7168, 0), (1024, 32), (48, 16)])
+@pytest.mark.parametrize("scale_fmt,out_fmt", [("fp32", "e4m3"), ("ue8m0", "e4m3"),
+                                               ("ue8m0", "e2m1"), ("fp32", "e2m1")])
+def test_cast_bit_exact(in_dtype, H, group, scale_fmt, out_fmt):
+    """With the activation given as input there is nothing approximate left:
+    scales and codes must equal the oracle's bit for bit."""
+    rng = np.random.default_rng(H + group)
+    T = 211
+    v = rng.standard_normal((T, H)) * np.exp2(rng.integers(-40, 40, (T, 1)))
+    v[3] = 0.0
+    v[4, : H // 2] = 2.0 ** -140                    # fp32 subnormals
+    v[5] = np.where(np.arange(H) % 3 == 0, 448.0, -0.0)
+    v[6] = rng.standard_normal(H) * 1e-30
+    y = torch.from_numpy(v.astype(np.float32))
+    if in_dtype == "bf16":
+        y = y.to(torch.bfloat16)
+    op = tk.QuantCast(H, group, scale_fmt, out_fmt, in_dtype)
+    q, s = op(y.cuda())
+    torch.cuda.synchronize()
+    yf = y.float().numpy()
+    rq, rs = oracle.quant_rows_f32(yf, group, scale_fmt, out_fmt)
+    gq, gs = q.cpu().numpy(), s.cpu().numpy()
+    if scale_fmt == "fp32":
+        assert np.array_equal(gs.view(np.uint32), rs.view(np.uint32)), "scales differ"
+    else:
+        assert np.array_equal(gs, rs), "scale bytes differ"
+    bad = np.argwhere(unpack(gq, out_fmt) != unpack(rq, out_fmt))
+    assert bad.size == 0, "codes differ at %s" % (bad[:5].tolist(),)
