@@ -18,18 +18,22 @@ import threading
 
 from . import _abi
 from ._abi import (IN_DTYPES, OUT_FMTS, SCALE_FMTS, QuantCastDesc, SwigluQuantDesc, TkError,
-                   tk_last_error_message, tk_quant_cast_plan, tk_quant_cast_plan_destroy,
+                   tk_fault_word, tk_last_error_message, tk_quant_cast_plan, tk_quant_cast_plan_destroy,
                    tk_quant_cast_run, tk_quant_cast_validate, tk_status_string,
-                   tk_swiglu_quant_launch_info, tk_swiglu_quant_output_sizes, tk_swiglu_quant_plan,
-                   tk_swiglu_quant_plan_destroy, tk_swiglu_quant_run, tk_swiglu_quant_validate)
+                   tk_swiglu_quant_host_pipe_create, tk_swiglu_quant_host_pipe_destroy,
+                   tk_swiglu_quant_host_workspace_size, tk_swiglu_quant_launch_info,
+                   tk_swiglu_quant_output_sizes, tk_swiglu_quant_plan, tk_swiglu_quant_plan_destroy,
+                   tk_swiglu_quant_run, tk_swiglu_quant_run_host, tk_swiglu_quant_validate)
 
 __all__ = [
-    "SwigluQuant", "QuantCast", "swiglu_quant", "quant_cast", "TkError",
+    "SwigluQuant", "HostPipe", "QuantCast", "swiglu_quant", "quant_cast", "TkError",
+    "tk_swiglu_quant_host_pipe_create", "tk_swiglu_quant_host_pipe_destroy",
+    "tk_swiglu_quant_host_workspace_size", "tk_swiglu_quant_run_host",
     "SwigluQuantDesc", "QuantCastDesc", "tk_swiglu_quant_validate", "tk_swiglu_quant_plan",
     "tk_swiglu_quant_plan_destroy", "tk_swiglu_quant_output_sizes", "tk_swiglu_quant_run",
     "tk_swiglu_quant_launch_info", "tk_quant_cast_validate", "tk_quant_cast_plan",
     "tk_quant_cast_plan_destroy", "tk_quant_cast_run", "tk_status_string",
-    "tk_last_error_message",
+    "tk_last_error_message", "tk_fault_word",
 ]
 
 
@@ -121,6 +125,57 @@ class SwigluQuant:
         with torch.cuda.device(x.device):
             tk_swiglu_quant_run(self.plan, T, x, topk_weights, q, scales, clamped_count,
                                 stream.cuda_stream)
+        return q, scales
+
+
+class HostPipe:
+    """Host-buffer form of a SwigluQuant (tk_swiglu_quant_run_host): inputs
+    and outputs are CPU tensors (pinned for overlap); a device workspace of
+    three chunk slots is allocated once, here, through torch."""
+
+    def __init__(self, op: SwigluQuant, chunk_rows: int = 1024):
+        torch = _torch()
+        self.op = op
+        self.chunk_rows = int(chunk_rows)
+        self.pipe = tk_swiglu_quant_host_pipe_create(op.plan, self.chunk_rows)
+        self.ws_bytes = tk_swiglu_quant_host_workspace_size(self.pipe)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device="cuda:%d" % op.device)
+
+    def __del__(self):
+        pipe = getattr(self, "pipe", None)
+        if pipe:
+            try:
+                tk_swiglu_quant_host_pipe_destroy(pipe)
+            except Exception:
+                pass
+            self.pipe = None
+
+    def __call__(self, x, topk_weights=None, *, q=None, scales=None, clamped_count=None,
+                 stream=None):
+        """Enqueue; returns (q, scales) host tensors, complete once `stream`
+        (default: torch's current stream) has passed this call."""
+        torch = _torch()
+        op = self.op
+        T = x.shape[0]
+        for t, name in ((x, "x"), (topk_weights, "topk_weights"), (q, "q"), (scales, "scales"),
+                        (clamped_count, "clamped_count")):
+            if t is not None and (t.is_cuda or not t.is_contiguous()):
+                raise ValueError("%s must be a contiguous CPU tensor" % name)
+        if x.dtype != torch.bfloat16 or tuple(x.shape) != (T, 2 * op.hidden):
+            raise ValueError("x must be bf16 [T, %d]" % (2 * op.hidden))
+        q_shape, s_shape, s_dtype = op.output_shapes(T)
+        if q is None:
+            q = torch.empty(q_shape, dtype=torch.uint8, pin_memory=True)
+        if scales is None:
+            scales = torch.empty(s_shape, dtype=s_dtype, pin_memory=True)
+        if tuple(q.shape) != q_shape or tuple(scales.shape) != s_shape or scales.dtype != s_dtype:
+            raise ValueError("q / scales have the wrong shape or dtype")
+        if stream is None:
+            stream = torch.cuda.current_stream(op.device)
+        with torch.cuda.device(op.device):
+            tk_swiglu_quant_run_host(self.pipe, T, x, topk_weights if op.has_w else None, q, scales,
+                                     clamped_count if op.count_clamped else None, self.workspace,
+                                     self.ws_bytes, stream.cuda_stream)
         return q, scales
 
 

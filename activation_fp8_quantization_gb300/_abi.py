@@ -53,11 +53,17 @@ SIGNATURES = {
                                                     _PSZ, _PSZ]),
     "tk_swiglu_quant_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP]),
     "tk_swiglu_quant_launch_info": (ctypes.c_int, [_VP, ctypes.c_int64, _PINT, _PINT, _PINT, _PINT]),
+    "tk_swiglu_quant_host_pipe_create": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.POINTER(_VP)]),
+    "tk_swiglu_quant_host_pipe_destroy": (ctypes.c_int, [_VP]),
+    "tk_swiglu_quant_host_workspace_size": (ctypes.c_int, [_VP, _PSZ]),
+    "tk_swiglu_quant_run_host": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP,
+                                                ctypes.c_size_t, _VP]),
     "tk_quant_cast_validate": (ctypes.c_int, [ctypes.POINTER(QuantCastDesc)]),
     "tk_quant_cast_plan": (ctypes.c_int, [ctypes.POINTER(QuantCastDesc), ctypes.c_int,
                                           ctypes.POINTER(_VP)]),
     "tk_quant_cast_plan_destroy": (ctypes.c_int, [_VP]),
     "tk_quant_cast_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP]),
+    "tk_fault_word": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tk_last_error_message": (ctypes.c_char_p, []),
 }
@@ -135,6 +141,30 @@ def tk_swiglu_quant_launch_info(plan: int, num_tokens: int) -> dict:
     return {"grid": g.value, "block": b.value, "rows_per_cta": r.value, "num_sms": n.value}
 
 
+def tk_swiglu_quant_host_pipe_create(plan: int, chunk_rows: int) -> int:
+    h = _VP()
+    check(lib().tk_swiglu_quant_host_pipe_create(plan, chunk_rows, ctypes.byref(h)))
+    return h.value
+
+
+def tk_swiglu_quant_host_pipe_destroy(pipe: int) -> None:
+    check(lib().tk_swiglu_quant_host_pipe_destroy(pipe))
+
+
+def tk_swiglu_quant_host_workspace_size(pipe: int) -> int:
+    b = ctypes.c_size_t()
+    check(lib().tk_swiglu_quant_host_workspace_size(pipe, ctypes.byref(b)))
+    return b.value
+
+
+def tk_swiglu_quant_run_host(pipe: int, num_tokens: int, x_host, topk_weights_host, q_host,
+                             scales_host, clamped_count_host, workspace, workspace_bytes: int,
+                             stream: int | None) -> None:
+    check(lib().tk_swiglu_quant_run_host(pipe, num_tokens, _ptr(x_host), _ptr(topk_weights_host),
+                                         _ptr(q_host), _ptr(scales_host), _ptr(clamped_count_host),
+                                         _ptr(workspace), workspace_bytes, stream))
+
+
 def tk_quant_cast_validate(desc: QuantCastDesc) -> int:
     return lib().tk_quant_cast_validate(ctypes.byref(desc))
 
@@ -151,6 +181,12 @@ def tk_quant_cast_plan_destroy(plan: int) -> None:
 
 def tk_quant_cast_run(plan: int, num_tokens: int, x, q, scales, stream: int | None) -> None:
     check(lib().tk_quant_cast_run(plan, num_tokens, _ptr(x), _ptr(q), _ptr(scales), stream))
+
+
+def tk_fault_word(device: int, clear: bool = False) -> int:
+    v = ctypes.c_uint32()
+    check(lib().tk_fault_word(device, ctypes.byref(v), int(clear)))
+    return v.value
 
 
 def tk_status_string(status: int) -> str:

@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -97,8 +98,101 @@ Geometry geometry(int64_t hidden, int32_t group)
     return g;
 }
 
-// Device facts a plan records once.
-tk_status query_device(int device, const void *fn, int block, int *num_sms, int *max_grid)
+// Guard that makes `device` current and restores the previous device.
+struct DeviceScope {
+    int prev = -1;
+    bool switched = false;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceScope(int device)
+    {
+        err = cudaGetDevice(&prev);
+        if (err == cudaSuccess && prev != device) {
+            err = cudaSetDevice(device);
+            switched = err == cudaSuccess;
+        }
+    }
+    ~DeviceScope()
+    {
+        if (switched)
+            cudaSetDevice(prev);
+    }
+};
+
+// Everything a launch needs, fixed when the plan is made.
+struct Launch {
+    const void *fn;
+    bool stream;       // warp_stream_kernel (else row_quant_kernel)
+    int block;         // threads per CTA
+    int rpc;           // row kernel: rows per CTA per iteration
+    int tpr, tpg_log2, groups;
+    int wpr, stages;   // stream kernel: warps per row, ring slots per warp
+    size_t smem;       // dynamic shared memory per CTA
+    int max_grid;      // resident CTAs on all SMs
+    int num_sms;
+    unsigned *fault;   // device address of the fault word
+};
+
+int grid_for(const Launch &L, int64_t T)
+{
+    const int64_t units = L.stream ? (T * L.wpr + (L.block / 32) - 1) / (L.block / 32) : (T + L.rpc - 1) / L.rpc;
+    return (int)(units < L.max_grid ? units : L.max_grid);
+}
+
+tk::RowShape shape_for(const Launch &L, int64_t T, int64_t hidden)
+{
+    return tk::RowShape{T, (int32_t)hidden, L.tpr, L.tpg_log2, L.rpc, L.groups, L.stages, L.wpr, L.fault};
+}
+
+int env_int(const char *name, int dflt)
+{
+    const char *v = getenv(name);
+    return v ? atoi(v) : dflt;
+}
+
+// Ring depth of the stream kernel: the most bytes in flight per SM with at
+// least 24 resident warps per SM (ties: the shallower ring).
+// TK_PIPELINE_STAGES=<n> (2..8) overrides the choice.
+tk_status choose_stream_ring(Launch *L, int slot_bytes, int optin)
+{
+    const int warps = L->block / 32;
+    const int forced = env_int("TK_PIPELINE_STAGES", 0);
+    long best = -1;
+    for (int S = 2; S <= 8; ++S) {
+        const size_t smem = (size_t)warps * S * (slot_bytes + 8);
+        if (smem > (size_t)optin)
+            break;
+        int occ = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, L->fn, L->block, smem);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (occ < 1)
+            continue;
+        const long inflight = (long)occ * warps * S * slot_bytes;
+        const bool pick = forced ? S == forced : ((long)occ * warps >= 24 || best < 0) && inflight > best;
+        if (pick) {
+            best = inflight;
+            L->stages = S;
+            L->smem = smem;
+            L->max_grid = occ;
+        }
+    }
+    if (best < 0)
+        return fail(TK_ERR_UNSUPPORTED, "no warp ring fits in shared memory");
+    return TK_OK;
+}
+
+}  // namespace
+
+// Set by a stream kernel that gave up waiting on one of its own copies.
+__device__ unsigned int g_tk_fault_word;
+
+namespace {
+
+// Validate the device, pick the kernel (the stream kernel when the width is a
+// multiple of 512 and a scale group fits in a warp's slice; TK_KERNEL=rows
+// forces the row kernel) and size its launch.
+tk_status make_launch(int device, int64_t hidden, int32_t group, const void *row_fn, const void *stream_fn,
+                      int slot_bytes, Launch *L)
 {
     int count = 0;
     cudaError_t e = cudaGetDeviceCount(&count);
@@ -106,24 +200,58 @@ tk_status query_device(int device, const void *fn, int block, int *num_sms, int 
         return cuda_fail(e, "cudaGetDeviceCount");
     if (device < 0 || device >= count)
         return fail(TK_ERR_INVALID_ARG, "device %d out of range (%d devices)", device, count);
-    e = cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, device);
+    DeviceScope scope(device);
+    if (scope.err != cudaSuccess)
+        return cuda_fail(scope.err, "cudaSetDevice");
+    *L = Launch{};
+    e = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, device);
+    int optin = 0;
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    void *fault = nullptr;
+    if (e == cudaSuccess)
+        e = cudaGetSymbolAddress(&fault, g_tk_fault_word);
     if (e != cudaSuccess)
-        return cuda_fail(e, "cudaDeviceGetAttribute(MultiProcessorCount)");
-    int prev = -1;
-    e = cudaGetDevice(&prev);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "cudaGetDevice");
-    if (prev != device && (e = cudaSetDevice(device)) != cudaSuccess)
-        return cuda_fail(e, "cudaSetDevice");
-    int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, block, 0);
-    if (prev != device)
-        cudaSetDevice(prev);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-    if (occ < 1)
-        return fail(TK_ERR_UNSUPPORTED, "kernel cannot be resident with %d threads per CTA", block);
-    *max_grid = *num_sms * occ;
+        return cuda_fail(e, "querying the device");
+    L->fault = static_cast<unsigned *>(fault);
+
+    const Geometry geo = geometry(hidden, group);
+    L->tpr = geo.tpr;
+    L->tpg_log2 = geo.tpg_log2;
+    L->groups = geo.groups;
+    const char *force = getenv("TK_KERNEL");
+    const bool want_rows = force && strcmp(force, "rows") == 0;
+    L->stream = stream_fn && hidden % 512 == 0 && !geo.cta_reduce && !want_rows;
+    if (L->stream) {
+        L->fn = stream_fn;
+        L->block = tk::kStreamThreads;
+        L->rpc = 1;
+        L->wpr = (int)(hidden / 512);
+        e = cudaFuncSetAttribute(L->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(L->fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "configuring the stream kernel's shared memory");
+        tk_status st = choose_stream_ring(L, slot_bytes, optin);
+        if (st != TK_OK)
+            return st;
+    } else {
+        L->fn = row_fn;
+        L->block = geo.block;
+        L->rpc = geo.rpc;
+        L->stages = 0;
+        L->wpr = 0;
+        L->smem = 0;
+        int occ = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, L->fn, L->block, 0);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (occ < 1)
+            return fail(TK_ERR_UNSUPPORTED, "kernel cannot be resident with %d threads per CTA", L->block);
+        L->max_grid = occ;
+    }
+    L->max_grid *= L->num_sms;
     return TK_OK;
 }
 
@@ -138,30 +266,19 @@ tk_status check_current_device(int device)
     return TK_OK;
 }
 
-int grid_for(int64_t T, int rpc, int max_grid)
-{
-    const int64_t nrb = (T + rpc - 1) / rpc;
-    return (int)(nrb < max_grid ? nrb : max_grid);
-}
 
 }  // namespace
 
 struct tk_swiglu_quant_plan_s {
     tk_swiglu_quant_desc desc;
     int device;
-    int num_sms;
-    int max_grid;
-    Geometry geo;
-    const void *fn;
+    Launch L;
 };
 
 struct tk_quant_cast_plan_s {
     tk_quant_cast_desc desc;
     int device;
-    int num_sms;
-    int max_grid;
-    Geometry geo;
-    const void *fn;
+    Launch L;
 };
 
 // ------------------------------------------------------------------ fused op
@@ -193,14 +310,16 @@ TK_API tk_status tk_swiglu_quant_plan(const tk_swiglu_quant_desc *d, int device,
     if (st != TK_OK)
         return st;
     const Geometry geo = geometry(d->hidden, d->group_size);
-    const void *fn = tk::swiglu_kernel_fn(d->out_fmt, d->scale_fmt, d->use_clamp != 0, geo.cta_reduce);
-    if (!fn)
+    const bool clamp = d->use_clamp != 0;
+    const void *row_fn = tk::swiglu_kernel_fn(d->out_fmt, d->scale_fmt, clamp, geo.cta_reduce);
+    const void *stream_fn = tk::swiglu_stream_fn(d->out_fmt, d->scale_fmt, clamp);
+    if (!row_fn)
         return fail(TK_ERR_UNSUPPORTED, "no kernel for this combination");
-    int num_sms = 0, max_grid = 0;
-    st = query_device(device, fn, geo.block, &num_sms, &max_grid);
+    Launch L{};
+    st = make_launch(device, d->hidden, d->group_size, row_fn, stream_fn, tk::kSwigluSlotBytes, &L);
     if (st != TK_OK)
         return st;
-    auto *p = new (std::nothrow) tk_swiglu_quant_plan_s{*d, device, num_sms, max_grid, geo, fn};
+    auto *p = new (std::nothrow) tk_swiglu_quant_plan_s{*d, device, L};
     if (!p)
         return fail(TK_ERR_INVALID_ARG, "out of host memory");
     *plan = p;
@@ -265,10 +384,9 @@ TK_API tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t T, con
     a.limit = d.use_clamp ? d.clamp_limit : 0.0f;
     a.H = (int32_t)d.hidden;
     tk::OutArgs o{static_cast<uint8_t *>(q), scales};
-    const Geometry &g = plan->geo;
-    tk::RowShape sh{T, (int32_t)d.hidden, g.tpr, g.tpg_log2, g.rpc, g.groups};
-    const int grid = grid_for(T, g.rpc, plan->max_grid);
-    cudaError_t e = tk::launch_swiglu(plan->fn, grid, g.block, a, o, sh, static_cast<cudaStream_t>(stream));
+    const Launch &L = plan->L;
+    cudaError_t e = tk::launch_swiglu(L.fn, grid_for(L, T), L.block, L.smem, a, o, shape_for(L, T, d.hidden),
+                                      static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the fused kernel");
     return ok();
@@ -280,13 +398,222 @@ TK_API tk_status tk_swiglu_quant_launch_info(tk_swiglu_quant_plan_t plan, int64_
     if (!plan || T < 0)
         return fail(TK_ERR_INVALID_ARG, "plan is NULL or num_tokens < 0");
     if (grid)
-        *grid = T == 0 ? 0 : grid_for(T, plan->geo.rpc, plan->max_grid);
+        *grid = T == 0 ? 0 : grid_for(plan->L, T);
     if (block)
-        *block = plan->geo.block;
+        *block = plan->L.block;
     if (rows_per_cta)
-        *rows_per_cta = plan->geo.rpc;
+        *rows_per_cta = plan->L.stream ? 0 : plan->L.rpc;
     if (num_sms)
-        *num_sms = plan->num_sms;
+        *num_sms = plan->L.num_sms;
+    return ok();
+}
+
+// -------------------------------------------------------- host-buffer pipe
+
+namespace {
+constexpr int kSlots = 3;
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+}  // namespace
+
+struct tk_swiglu_quant_host_pipe_s {
+    tk_swiglu_quant_plan_t plan;
+    int64_t chunk_rows;
+    cudaStream_t s_in, s_k, s_out;
+    cudaEvent_t ev_entry, ev_exit;
+    cudaEvent_t ev_in[kSlots], ev_k[kSlots], ev_out[kSlots];
+    size_t x_bytes, w_bytes, q_bytes, s_bytes;  // per slot, unaligned
+    size_t slot_bytes, total_bytes;
+    size_t q_row, s_row;                        // output bytes per row
+};
+
+namespace {
+void destroy_pipe_objects(tk_swiglu_quant_host_pipe_s *p)
+{
+    cudaStream_t ss[3] = {p->s_in, p->s_k, p->s_out};
+    for (cudaStream_t st : ss)
+        if (st) {
+            cudaStreamSynchronize(st);
+            cudaStreamDestroy(st);
+        }
+    cudaEvent_t es[2] = {p->ev_entry, p->ev_exit};
+    for (cudaEvent_t e : es)
+        if (e)
+            cudaEventDestroy(e);
+    for (int i = 0; i < kSlots; ++i) {
+        if (p->ev_in[i])
+            cudaEventDestroy(p->ev_in[i]);
+        if (p->ev_k[i])
+            cudaEventDestroy(p->ev_k[i]);
+        if (p->ev_out[i])
+            cudaEventDestroy(p->ev_out[i]);
+    }
+}
+}  // namespace
+
+TK_API tk_status tk_swiglu_quant_host_pipe_create(tk_swiglu_quant_plan_t plan, int64_t chunk_rows,
+                                                  tk_swiglu_quant_host_pipe_t *out)
+{
+    if (!out)
+        return fail(TK_ERR_INVALID_ARG, "pipe output pointer is NULL");
+    *out = nullptr;
+    if (!plan || chunk_rows < 1)
+        return fail(TK_ERR_INVALID_ARG, "plan is NULL or chunk_rows < 1");
+    const tk_swiglu_quant_desc &d = plan->desc;
+    auto *p = new (std::nothrow) tk_swiglu_quant_host_pipe_s{};
+    if (!p)
+        return fail(TK_ERR_INVALID_ARG, "out of host memory");
+    p->plan = plan;
+    p->chunk_rows = chunk_rows;
+    const size_t groups = d.group_size ? (size_t)(d.hidden / d.group_size) : 1;
+    p->q_row = (size_t)(d.out_fmt == TK_OUT_E4M3 ? d.hidden : d.hidden / 2);
+    p->s_row = groups * (d.scale_fmt == TK_SCALE_FP32 ? 4u : 1u);
+    p->x_bytes = (size_t)chunk_rows * (size_t)d.hidden * 4u;
+    p->w_bytes = d.has_topk_weights ? (size_t)chunk_rows * 4u : 0;
+    p->q_bytes = (size_t)chunk_rows * p->q_row;
+    p->s_bytes = (size_t)chunk_rows * p->s_row;
+    p->slot_bytes = align256(p->x_bytes) + align256(p->w_bytes) + align256(p->q_bytes) + align256(p->s_bytes);
+    p->total_bytes = kSlots * p->slot_bytes + 256;  // + the clamp counter
+
+    DeviceScope scope(plan->device);
+    cudaError_t e = scope.err;
+    cudaStream_t *ss[3] = {&p->s_in, &p->s_k, &p->s_out};
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+        e = cudaStreamCreateWithFlags(ss[i], cudaStreamNonBlocking);
+    cudaEvent_t *es[2 + 3 * kSlots] = {&p->ev_entry, &p->ev_exit};
+    for (int i = 0; i < kSlots; ++i) {
+        es[2 + i] = &p->ev_in[i];
+        es[2 + kSlots + i] = &p->ev_k[i];
+        es[2 + 2 * kSlots + i] = &p->ev_out[i];
+    }
+    for (int i = 0; i < 2 + 3 * kSlots && e == cudaSuccess; ++i)
+        e = cudaEventCreateWithFlags(es[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        destroy_pipe_objects(p);
+        delete p;
+        return cuda_fail(e, "creating the host pipe's streams and events");
+    }
+    *out = p;
+    return ok();
+}
+
+TK_API tk_status tk_swiglu_quant_host_pipe_destroy(tk_swiglu_quant_host_pipe_t pipe)
+{
+    if (!pipe)
+        return ok();
+    {
+        DeviceScope scope(pipe->plan->device);
+        destroy_pipe_objects(pipe);
+    }
+    delete pipe;
+    return ok();
+}
+
+TK_API tk_status tk_swiglu_quant_host_workspace_size(tk_swiglu_quant_host_pipe_t pipe, size_t *bytes)
+{
+    if (!pipe || !bytes)
+        return fail(TK_ERR_INVALID_ARG, "pipe or bytes is NULL");
+    *bytes = pipe->total_bytes;
+    return ok();
+}
+
+TK_API tk_status tk_swiglu_quant_run_host(tk_swiglu_quant_host_pipe_t pipe, int64_t T, const void *x_host,
+                                          const float *w_host, void *q_host, void *scales_host,
+                                          int64_t *count_host, void *workspace, size_t workspace_bytes,
+                                          void *stream)
+{
+    if (!pipe)
+        return fail(TK_ERR_INVALID_ARG, "pipe is NULL");
+    if (T < 0)
+        return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)T);
+    if (T == 0)
+        return ok();
+    tk_swiglu_quant_plan_t plan = pipe->plan;
+    const tk_swiglu_quant_desc &d = plan->desc;
+    if (!x_host || !q_host || !scales_host)
+        return fail(TK_ERR_INVALID_ARG, "x_host, q_host and scales_host must be non-NULL");
+    if (d.has_topk_weights && !w_host)
+        return fail(TK_ERR_INVALID_ARG, "the plan expects topk_weights_host");
+    if (d.count_clamped && !count_host)
+        return fail(TK_ERR_INVALID_ARG, "the plan expects clamped_count_host");
+    if (!workspace || workspace_bytes < pipe->total_bytes)
+        return fail(TK_ERR_INVALID_ARG, "workspace must hold %zu bytes (got %zu)", pipe->total_bytes,
+                    workspace_bytes);
+    if (!aligned(workspace, 256))
+        return fail(TK_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    tk_status st = check_current_device(plan->device);
+    if (st != TK_OK)
+        return st;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int64_t *dcount = reinterpret_cast<int64_t *>(ws + kSlots * pipe->slot_bytes);
+    cudaStream_t user = static_cast<cudaStream_t>(stream);
+    const size_t x_row = (size_t)d.hidden * 4u;
+    cudaError_t e = cudaEventRecord(pipe->ev_entry, user);
+    cudaStream_t ss[3] = {pipe->s_in, pipe->s_k, pipe->s_out};
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+        e = cudaStreamWaitEvent(ss[i], pipe->ev_entry, 0);
+    if (e == cudaSuccess && d.count_clamped)
+        e = cudaMemcpyAsync(dcount, count_host, 2 * sizeof(int64_t), cudaMemcpyHostToDevice, pipe->s_in);
+
+    const int64_t nchunks = (T + pipe->chunk_rows - 1) / pipe->chunk_rows;
+    for (int64_t c = 0; c < nchunks && e == cudaSuccess; ++c) {
+        const int slot = (int)(c % kSlots);
+        const int64_t r0 = c * pipe->chunk_rows;
+        const int64_t rows = (T - r0) < pipe->chunk_rows ? (T - r0) : pipe->chunk_rows;
+        uint8_t *sx = ws + slot * pipe->slot_bytes;
+        uint8_t *sw = sx + align256(pipe->x_bytes);
+        uint8_t *sq = sw + align256(pipe->w_bytes);
+        uint8_t *ssc = sq + align256(pipe->q_bytes);
+        // copy in, once the slot's previous chunk has been copied out
+        if (c >= kSlots)
+            e = cudaStreamWaitEvent(pipe->s_in, pipe->ev_out[slot], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(sx, static_cast<const uint8_t *>(x_host) + (size_t)r0 * x_row,
+                                (size_t)rows * x_row, cudaMemcpyHostToDevice, pipe->s_in);
+        if (e == cudaSuccess && d.has_topk_weights)
+            e = cudaMemcpyAsync(sw, w_host + r0, (size_t)rows * 4u, cudaMemcpyHostToDevice, pipe->s_in);
+        if (e == cudaSuccess)
+            e = cudaEventRecord(pipe->ev_in[slot], pipe->s_in);
+        // compute
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(pipe->s_k, pipe->ev_in[slot], 0);
+        if (e == cudaSuccess) {
+            tk::SwigluArgs a{};
+            a.x = reinterpret_cast<const uint16_t *>(sx);
+            a.w = d.has_topk_weights ? reinterpret_cast<const float *>(sw) : nullptr;
+            a.counts = d.count_clamped ? reinterpret_cast<unsigned long long *>(dcount) : nullptr;
+            a.limit = d.use_clamp ? d.clamp_limit : 0.0f;
+            a.H = (int32_t)d.hidden;
+            tk::OutArgs o{sq, ssc};
+            const Launch &L = plan->L;
+            e = tk::launch_swiglu(L.fn, grid_for(L, rows), L.block, L.smem, a, o, shape_for(L, rows, d.hidden),
+                                  pipe->s_k);
+        }
+        if (e == cudaSuccess)
+            e = cudaEventRecord(pipe->ev_k[slot], pipe->s_k);
+        // copy out
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(pipe->s_out, pipe->ev_k[slot], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<uint8_t *>(q_host) + (size_t)r0 * pipe->q_row, sq,
+                                (size_t)rows * pipe->q_row, cudaMemcpyDeviceToHost, pipe->s_out);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<uint8_t *>(scales_host) + (size_t)r0 * pipe->s_row, ssc,
+                                (size_t)rows * pipe->s_row, cudaMemcpyDeviceToHost, pipe->s_out);
+        if (e == cudaSuccess)
+            e = cudaEventRecord(pipe->ev_out[slot], pipe->s_out);
+    }
+    // the last copy-out waited for the last kernel, and kernels run in order
+    if (e == cudaSuccess && d.count_clamped)
+        e = cudaMemcpyAsync(count_host, dcount, 2 * sizeof(int64_t), cudaMemcpyDeviceToHost, pipe->s_out);
+    if (e == cudaSuccess)
+        e = cudaEventRecord(pipe->ev_exit, pipe->s_out);
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(user, pipe->ev_exit, 0);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "enqueueing the host-buffer pipeline");
     return ok();
 }
 
@@ -313,14 +640,16 @@ TK_API tk_status tk_quant_cast_plan(const tk_quant_cast_desc *d, int device, tk_
     if (st != TK_OK)
         return st;
     const Geometry geo = geometry(d->hidden, d->group_size);
-    const void *fn = tk::cast_kernel_fn(d->in_dtype, d->out_fmt, d->scale_fmt, geo.cta_reduce);
-    if (!fn)
+    const void *row_fn = tk::cast_kernel_fn(d->in_dtype, d->out_fmt, d->scale_fmt, geo.cta_reduce);
+    const void *stream_fn = tk::cast_stream_fn(d->in_dtype, d->out_fmt, d->scale_fmt);
+    if (!row_fn)
         return fail(TK_ERR_UNSUPPORTED, "no kernel for this combination");
-    int num_sms = 0, max_grid = 0;
-    st = query_device(device, fn, geo.block, &num_sms, &max_grid);
+    Launch L{};
+    st = make_launch(device, d->hidden, d->group_size, row_fn, stream_fn,
+                     d->in_dtype == TK_IN_BF16 ? tk::kCastBf16SlotBytes : tk::kCastF32SlotBytes, &L);
     if (st != TK_OK)
         return st;
-    auto *p = new (std::nothrow) tk_quant_cast_plan_s{*d, device, num_sms, max_grid, geo, fn};
+    auto *p = new (std::nothrow) tk_quant_cast_plan_s{*d, device, L};
     if (!p)
         return fail(TK_ERR_INVALID_ARG, "out of host memory");
     *plan = p;
@@ -356,16 +685,35 @@ TK_API tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t T, const v
         return st;
     tk::CastArgs a{x, (int32_t)d.hidden};
     tk::OutArgs o{static_cast<uint8_t *>(q), scales};
-    const Geometry &g = plan->geo;
-    tk::RowShape sh{T, (int32_t)d.hidden, g.tpr, g.tpg_log2, g.rpc, g.groups};
-    const int grid = grid_for(T, g.rpc, plan->max_grid);
-    cudaError_t e = tk::launch_cast(plan->fn, grid, g.block, a, o, sh, static_cast<cudaStream_t>(stream));
+    const Launch &L = plan->L;
+    cudaError_t e = tk::launch_cast(L.fn, grid_for(L, T), L.block, L.smem, a, o, shape_for(L, T, d.hidden),
+                                    static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the cast kernel");
     return ok();
 }
 
 // ---------------------------------------------------------------- diagnostics
+
+TK_API tk_status tk_fault_word(int device, uint32_t *value, int clear)
+{
+    if (!value)
+        return fail(TK_ERR_INVALID_ARG, "value is NULL");
+    DeviceScope scope(device);
+    if (scope.err != cudaSuccess)
+        return cuda_fail(scope.err, "cudaSetDevice");
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_tk_fault_word, sizeof v);
+    if (e == cudaSuccess && clear) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_tk_fault_word, &zero, sizeof zero);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading the fault word");
+    *value = v;
+    return ok();
+}
+
 
 TK_API const char *tk_status_string(tk_status s)
 {

@@ -27,7 +27,27 @@ const void *pick_out(int out_fmt, int scale_fmt, bool cta)
         return pick<Src, kOutE2M1>(scale_fmt, cta);
     return nullptr;
 }
+template <class Src>
+const void *stream_pick(int out_fmt, int scale_fmt)
+{
+    if (out_fmt == kOutE4M3)
+        return scale_fmt == kScaleF32 ? reinterpret_cast<const void *>(&warp_stream_kernel<Src, kOutE4M3, kScaleF32>)
+                                      : reinterpret_cast<const void *>(&warp_stream_kernel<Src, kOutE4M3, kScaleUE8M0>);
+    if (out_fmt == kOutE2M1)
+        return scale_fmt == kScaleF32 ? reinterpret_cast<const void *>(&warp_stream_kernel<Src, kOutE2M1, kScaleF32>)
+                                      : reinterpret_cast<const void *>(&warp_stream_kernel<Src, kOutE2M1, kScaleUE8M0>);
+    return nullptr;
+}
 }  // namespace
+
+const void *cast_stream_fn(int in_dtype, int out_fmt, int scale_fmt)
+{
+    if (in_dtype == 0)
+        return stream_pick<CastBf16Src>(out_fmt, scale_fmt);
+    if (in_dtype == 1)
+        return stream_pick<CastF32Src>(out_fmt, scale_fmt);
+    return nullptr;
+}
 
 const void *cast_kernel_fn(int in_dtype, int out_fmt, int scale_fmt, bool cta_reduce)
 {
@@ -38,14 +58,14 @@ const void *cast_kernel_fn(int in_dtype, int out_fmt, int scale_fmt, bool cta_re
     return nullptr;
 }
 
-cudaError_t launch_cast(const void *kfn, int grid, int block, const CastArgs &a,
+cudaError_t launch_cast(const void *kfn, int grid, int block, size_t smem, const CastArgs &a,
                         const OutArgs &o, const RowShape &sh, cudaStream_t stream)
 {
     CastArgs a_ = a;
     OutArgs o_ = o;
     RowShape sh_ = sh;
     void *args[] = {&a_, &o_, &sh_};
-    return cudaLaunchKernel(kfn, dim3(grid), dim3(block), args, 0, stream);
+    return cudaLaunchKernel(kfn, dim3(grid), dim3(block), args, smem, stream);
 }
 
 }  // namespace tk

@@ -8,15 +8,23 @@
 
 namespace tk {
 
-// Kernel entry for a (format, scale, clamp, reduction) combination of the
-// fused op, or nullptr if there is none.
+// Entry of the fused op's row-block kernel (any width) or of its warp-stream
+// kernel (width a multiple of 512) for a format / scale / clamp combination;
+// nullptr if there is none.
 const void *swiglu_kernel_fn(int out_fmt, int scale_fmt, bool clamp, bool cta_reduce);
-cudaError_t launch_swiglu(const void *fn, int grid, int block, const SwigluArgs &a,
+const void *swiglu_stream_fn(int out_fmt, int scale_fmt, bool clamp);
+cudaError_t launch_swiglu(const void *fn, int grid, int block, size_t smem, const SwigluArgs &a,
                           const OutArgs &o, const RowShape &sh, cudaStream_t stream);
 
 // Same for the standalone cast (in_dtype: 0 bf16, 1 fp32).
 const void *cast_kernel_fn(int in_dtype, int out_fmt, int scale_fmt, bool cta_reduce);
-cudaError_t launch_cast(const void *fn, int grid, int block, const CastArgs &a,
+const void *cast_stream_fn(int in_dtype, int out_fmt, int scale_fmt);
+cudaError_t launch_cast(const void *fn, int grid, int block, size_t smem, const CastArgs &a,
                         const OutArgs &o, const RowShape &sh, cudaStream_t stream);
+
+// Bytes of one warp-ring slot of the stream kernels.
+constexpr int kSwigluSlotBytes = SwigluSrc<false>::kSpans * SwigluSrc<false>::kSpanBytes;
+constexpr int kCastBf16SlotBytes = CastBf16Src::kSpans * CastBf16Src::kSpanBytes;
+constexpr int kCastF32SlotBytes = CastF32Src::kSpans * CastF32Src::kSpanBytes;
 
 }  // namespace tk

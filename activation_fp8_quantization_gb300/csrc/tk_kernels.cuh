@@ -1,30 +1,44 @@
 // Device side of the fused SwiGLU + top-k weight + FP8/FP4 cast, sm_103a.
 //
-// One persistent, grid-strided kernel template serves both entry points. A
-// thread owns 16 consecutive columns of one row: for the fused op that is one
-// 32-byte vector of the gate half and one of the up half ("TileKernels from
-// Beginner to Master", zhichai.net/en/topic/177618752, chapter 1: 32-byte
-// vectors on SM100-class parts; chapter 2: both halves of a row reached by a
-// `hidden` offset). The activation stays in registers from load to code store
+// Two persistent, grid-strided kernel templates serve both entry points. A
+// thread owns 16 consecutive columns of one row: for the fused op that is 32
+// bytes of the gate half and 32 of the up half ("TileKernels from Beginner to
+// Master", zhichai.net/en/topic/177618752, chapter 1: 32-byte vectors on
+// SM100-class parts; chapter 2: both halves of a row reached by a `hidden`
+// offset). The activation stays in registers from load to code store
 // (chapter 2, "operator fusion, three stages"); group absmax is a butterfly of
 // warp shuffles over the threads of one group, or a CTA reduction through
 // shared memory for one-scale-per-row at widths a warp cannot cover.
 //
 // The schedule is persistent (chapter 2, "Persistent Kernel": a fixed grid
 // that stays resident while rows stream through): the host sizes the grid to
-// the CTAs that fit on all SMs at once, each CTA walks row blocks with a grid
-// stride, and the next row block's loads are issued before the current one is
-// computed so that every thread keeps 64 bytes of HBM reads in flight.
+// the CTAs that fit on all SMs at once.
+//
+//  - warp_stream_kernel (rows whose width is a multiple of 512): every warp
+//    streams 512-column slices of rows through its own ring of shared-memory
+//    slots filled by TMA bulk copies (one lane issues them, an mbarrier per
+//    slot counts the bytes in), so the bytes in flight are set by the ring
+//    depth, not by registers, and no CTA-wide barrier is needed.
+//  - row_quant_kernel (any width that is a multiple of 16): CTAs walk row
+//    blocks with a grid stride; each thread keeps the next row block's loads
+//    (64 bytes) in flight while it computes the current one.
 //
 // Numerics (IEEE, no fast-math, no FMA contraction: the library is built with
-// -fmad=false and every fused multiply-add below is written out):
-//   silu(g) = g * sigmoid(g) with e^{-|g|} from ex2.approx and the reciprocal
-//   from rcp.approx; y = (silu(g') * u') * w in fp32. The scale and the
-//   quotient y / s are the IEEE fp32 results: s = amax / Qmax by correctly
-//   rounded division; y / s either by an exact power-of-two multiply (UE8M0)
-//   or by a reciprocal with one Markstein correction step, which returns the
-//   correctly rounded quotient. Codes come from the hardware's
-//   round-to-nearest-even, saturating e4m3x2 / e2m1x2 conversions.
+// -fmad=false and every fused multiply-add below is written out). Two columns
+// travel together through Blackwell's packed fp32x2 multiply / add / FMA, so
+// each instruction does two IEEE operations:
+//   silu(g) = max(g * t, g) / (1 + t), t = e^{-|g|} = h * h with
+//   h = 2^{-|g| log2(e) / 2} from ex2.approx.ftz (h is a normal number for
+//   |g| <= 174, and the multiply rounds a subnormal t correctly, so no
+//   subnormal is lost), and the reciprocal of 1 + t in [1, 2] from
+//   rcp.approx.ftz; y = (silu(g') * u') * w in fp32. The kernel carries -y
+//   (the weight enters as -w, an exact negation), which lets the quotient
+//   keep the sign of zero without a fix-up. The scale and the quotient y / s
+//   are the IEEE fp32 results: s = amax / Qmax by correctly rounded division;
+//   y / s either by an exact power-of-two multiply (UE8M0) or by a reciprocal
+//   with one Markstein correction step, which returns the correctly rounded
+//   quotient. Codes come from the hardware's round-to-nearest-even,
+//   saturating e4m3x2 / e2m1x2 conversions.
 #pragma once
 
 #include <cstdint>
@@ -47,6 +61,9 @@ struct RowShape {
     int32_t tpg_log2;   // log2(threads per group); unused by the CTA-reduction variant
     int32_t rpc;        // rows per CTA per iteration
     int32_t groups;     // scales per row
+    int32_t stages;     // warp_stream_kernel: slots per warp ring (>= 2)
+    int32_t wpr;        // warp_stream_kernel: warps (512-column slices) per row
+    unsigned *fault;    // warp_stream_kernel: device word, bit 0 set if a wait gave up
 };
 
 struct OutArgs {
@@ -80,61 +97,179 @@ __device__ __forceinline__ void st_stream_64(void *p, uint32_t a, uint32_t b)
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// ------------------------------------------------------ TMA and mbarriers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// make barrier initialisation visible to the async (TMA) proxy
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// order this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA) writes to the same memory
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// one arrival that also announces `bytes` of incoming transactions
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+// bulk copy global -> this CTA's shared memory, completion counted on `bar`;
+// both addresses 16-byte aligned, bytes a multiple of 16
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// Each try_wait suspends for a hardware-chosen interval; this many tries is
+// far beyond any legitimate copy (well over a second), after which the
+// kernel gives up on the barrier instead of spinning forever.
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kSpinLimit; ++i)
+        if (mbar_try_wait(bar, parity))
+            return true;
+    return false;
+}
+
 // ---------------------------------------------------------------- arithmetic
 
-__device__ __forceinline__ float ex2_approx(float x)
+// A pair of fp32 values in one 64-bit register pair, for the f32x2 forms.
+__device__ __forceinline__ uint64_t pk(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float plo(uint64_t v)
+{
+    float lo;
+    asm("{\n\t.reg .f32 hi;\n\tmov.b64 {%0, hi}, %1;\n\t}" : "=f"(lo) : "l"(v));
+    return lo;
+}
+__device__ __forceinline__ float phi(uint64_t v)
+{
+    float hi;
+    asm("{\n\t.reg .f32 lo;\n\tmov.b64 {lo, %0}, %1;\n\t}" : "=f"(hi) : "l"(v));
+    return hi;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t splat(float v) { return pk(v, v); }
+
+__device__ __forceinline__ float ex2_ftz(float x)
 {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
-__device__ __forceinline__ float rcp_approx(float x)
+__device__ __forceinline__ float rcp_ftz(float x)
 {
     float y;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
-// silu(g) = g / (1 + e^{-g}). With t = e^{-|g|} in (0, 1] nothing overflows:
-// for g >= 0 it is g / (1 + t); for g < 0 it is g * t / (1 + t).
-__device__ __forceinline__ float silu(float g)
+// -(silu(g) * u * w) for the two columns of a pair; w2n = (-w, -w).
+// silu(g) = g / (1 + e^{-g}) = max(g * t, g) / (1 + t) with t = e^{-|g|}:
+// for g >= 0, g * t <= g; for g < 0, g * t >= g and g * t is the numerator.
+__device__ __forceinline__ uint64_t neg_swiglu2(float g0, float g1, float u0, float u1, uint64_t w2n)
 {
-    const float t = ex2_approx(__fmul_rn(fabsf(g), -1.4426950408889634f));
-    const float num = g < 0.0f ? __fmul_rn(g, t) : g;
-    return __fmul_rn(num, rcp_approx(__fadd_rn(1.0f, t)));
+    constexpr float kNegHalfLog2e = -0.72134752044448170368f;  // -log2(e) / 2
+    const uint64_t h = pk(ex2_ftz(__fmul_rn(fabsf(g0), kNegHalfLog2e)),
+                          ex2_ftz(__fmul_rn(fabsf(g1), kNegHalfLog2e)));
+    const uint64_t t = mul2(h, h);
+    const uint64_t gt = mul2(pk(g0, g1), t);
+    const uint64_t num = pk(fmaxf(plo(gt), g0), fmaxf(phi(gt), g1));
+    const uint64_t den = add2(t, splat(1.0f));
+    const uint64_t silu = mul2(num, pk(rcp_ftz(plo(den)), rcp_ftz(phi(den))));
+    return mul2(mul2(silu, pk(u0, u1)), w2n);
 }
 
-// Correctly rounded a / b from rb = RN(1/b): q0 = RN(a * rb) is within one
-// ulp of a / b, the FMA returns the exact remainder a - b * q0, and one
-// correction step RN(q0 + r * rb) is RN(a / b) (P. Markstein, "Computation of
-// elementary functions on the IBM RISC System/6000 processor", 1990; see also
-// Muller et al., "Handbook of Floating-Point Arithmetic", the chapter on
-// division with an FMA). Valid while the remainder does not underflow; the
-// caller keeps b >= 2^-80 so that is true whenever |a / b| >= 2^-11, and
-// smaller quotients encode to a signed zero whatever their last bits.
-// For a = -0 the correction adds +0 and -0, which rounds to +0; b > 0 here,
-// so the quotient's sign is a's and is copied back.
-__device__ __forceinline__ float div_markstein(float a, float b, float rb)
+// Correctly rounded quotients y / b of a pair, from ny = -y, b and
+// nrb = -RN(1/b): q0 = RN(y * rb) is within one ulp of y / b, the FMA gives
+// the exact q0 * b - y, and one correction step RN(q0 + (y - q0 b) rb) is
+// RN(y / b) (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", 1990; Muller et al., "Handbook of
+// Floating-Point Arithmetic", division with an FMA). Valid while the
+// remainder does not underflow: the caller keeps b >= 2^-73, which covers
+// every |y / b| >= 2^-11, and smaller quotients encode to a signed zero
+// whatever their last bits. With -y as the addend both zeros keep their sign
+// (y = -0: q0 = -0, r = +0, q = -0 + -0 = -0; y = +0: +0).
+__device__ __forceinline__ uint64_t div_markstein2(uint64_t ny, uint64_t b2, uint64_t nrb2)
 {
-    const float q0 = __fmul_rn(a, rb);
-    const float r = __fmaf_rn(-q0, b, a);
-    return copysignf(__fmaf_rn(r, rb, q0), a);
+    const uint64_t q0 = mul2(ny, nrb2);
+    const uint64_t r = fma2(q0, b2, ny);
+    return fma2(r, nrb2, q0);
 }
 
 template <int OUT> struct Fmt;
 template <> struct Fmt<kOutE4M3> {
     // 448 = 1.75 * 2^8: exponent 8, fraction bits of 1.75
     static constexpr float kQmax = 448.0f;
+    static constexpr float kRcpQmax = 0x1.24924ap-9f;   // RN(1 / 448)
     static constexpr int kQE = 8;
     static constexpr uint32_t kQM = 0x600000u;
 };
 template <> struct Fmt<kOutE2M1> {
     // 6 = 1.5 * 2^2
     static constexpr float kQmax = 6.0f;
+    static constexpr float kRcpQmax = 0x1.555556p-3f;   // RN(1 / 6)
     static constexpr int kQE = 2;
     static constexpr uint32_t kQM = 0x400000u;
 };
+
+// Correctly rounded a / b for one value (the pair form's scalar twin).
+__device__ __forceinline__ float div_markstein1(float a, float b, float rb)
+{
+    const float q0 = __fmul_rn(a, rb);
+    const float r = __fmaf_rn(-q0, b, a);
+    return __fmaf_rn(r, rb, q0);
+}
 
 // Smallest k with Qmax * 2^k >= amax, read off amax's bits: with
 // amax = m * 2^e (1 <= m < 2) and Qmax = q * 2^QE, k = e - QE when m <= q and
@@ -180,35 +315,44 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi)
 
 // ------------------------------------------------------- quantize and store
 
-// Scale the thread's 16 values by 1/s (s from the group's amax), encode and
-// store them; the group's first thread also stores the scale.
+// Scale the thread's 16 values (held negated, as 8 pairs) by 1/s, with s
+// from the group's amax, encode and store them; the group's first thread
+// also stores the scale.
 template <int OUT, int SCALE>
-__device__ __forceinline__ void quantize_store(const float (&y)[kEPT], float amax, int64_t row,
+__device__ __forceinline__ void quantize_store(const uint64_t (&ny)[kEPT / 2], float amax, int64_t row,
                                                int col0, int group_idx, bool write_scale,
                                                const RowShape &sh, const OutArgs &o)
 {
-    float v[kEPT];
+    uint64_t v[kEPT / 2];
     if (SCALE == kScaleUE8M0) {
         const int k = ue8m0_exponent<OUT>(amax);
-        const float inv = __uint_as_float((uint32_t)(127 - k) << 23);  // 2^-k, k <= 126 here
+        // -2^-k (k <= 126 here): the product is the exact power-of-two scaling
+        const uint64_t ninv = splat(-__uint_as_float((uint32_t)(127 - k) << 23));
 #pragma unroll
-        for (int i = 0; i < kEPT; ++i)
-            v[i] = __fmul_rn(y[i], inv);  // exact: a power-of-two scaling, rounded once at most
+        for (int i = 0; i < kEPT / 2; ++i)
+            v[i] = mul2(ny[i], ninv);
         if (write_scale)
             static_cast<uint8_t *>(o.scales)[row * sh.groups + group_idx] = (uint8_t)(k + 127);
     } else {
-        float s = __fdiv_rn(amax, Fmt<OUT>::kQmax);
-        if (s == 0.0f)
-            s = 1.0f;
-        if (s >= 0x1p-80f) {
-            const float rs = __frcp_rn(s);
+        // amax >= 2^-64 keeps s >= 2^-73 and every remainder above the
+        // subnormal range, so both divisions can take the Markstein step;
+        // smaller groups (a uniform branch, never taken by ordinary data) use
+        // the IEEE division directly.
+        float s;
+        if (amax >= 0x1p-64f) {
+            s = div_markstein1(amax, Fmt<OUT>::kQmax, Fmt<OUT>::kRcpQmax);
+            const uint64_t s2 = splat(s);
+            const uint64_t nrs2 = splat(-__frcp_rn(s));
 #pragma unroll
-            for (int i = 0; i < kEPT; ++i)
-                v[i] = div_markstein(y[i], s, rs);
+            for (int i = 0; i < kEPT / 2; ++i)
+                v[i] = div_markstein2(ny[i], s2, nrs2);
         } else {
+            s = __fdiv_rn(amax, Fmt<OUT>::kQmax);
+            if (s == 0.0f)
+                s = 1.0f;
 #pragma unroll
-            for (int i = 0; i < kEPT; ++i)
-                v[i] = __fdiv_rn(y[i], s);
+            for (int i = 0; i < kEPT / 2; ++i)
+                v[i] = pk(__fdiv_rn(-plo(ny[i]), s), __fdiv_rn(-phi(ny[i]), s));
         }
         if (write_scale)
             static_cast<float *>(o.scales)[row * sh.groups + group_idx] = s;
@@ -217,24 +361,31 @@ __device__ __forceinline__ void quantize_store(const float (&y)[kEPT], float ama
         uint32_t w[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            w[j] = cvt_e4m3x2(v[4 * j], v[4 * j + 1]) | (cvt_e4m3x2(v[4 * j + 2], v[4 * j + 3]) << 16);
+            w[j] = cvt_e4m3x2(plo(v[2 * j]), phi(v[2 * j])) |
+                   (cvt_e4m3x2(plo(v[2 * j + 1]), phi(v[2 * j + 1])) << 16);
         st_stream_128(o.q + row * (int64_t)sh.H + col0, w[0], w[1], w[2], w[3]);
     } else {
         uint32_t w[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j)
-            w[j] = cvt_e2m1x2(v[8 * j], v[8 * j + 1]) | (cvt_e2m1x2(v[8 * j + 2], v[8 * j + 3]) << 8) |
-                   (cvt_e2m1x2(v[8 * j + 4], v[8 * j + 5]) << 16) |
-                   (cvt_e2m1x2(v[8 * j + 6], v[8 * j + 7]) << 24);
+            w[j] = cvt_e2m1x2(plo(v[4 * j]), phi(v[4 * j])) |
+                   (cvt_e2m1x2(plo(v[4 * j + 1]), phi(v[4 * j + 1])) << 8) |
+                   (cvt_e2m1x2(plo(v[4 * j + 2]), phi(v[4 * j + 2])) << 16) |
+                   (cvt_e2m1x2(plo(v[4 * j + 3]), phi(v[4 * j + 3])) << 24);
         st_stream_64(o.q + row * (int64_t)(sh.H / 2) + col0 / 2, w[0], w[1]);
     }
 }
 
 // ------------------------------------------------------------ the kernel
 
-// Src supplies: Args (kernel argument), Regs (raw loaded data for one row
-// slice), load(args, row, col0, regs), produce(args, regs, row, y) -> fills
-// y[16] and returns nothing, and finish(args) at kernel exit.
+// Src supplies: Args (kernel argument); Regs and load(args, row, col0, regs),
+// which issues the thread's loads for one row slice; zero(regs);
+// produce(args, regs, ok, ny, amax) -> the 16 activations negated as 8 pairs
+// and their absmax; finish(args) at kernel exit.
+//
+// General form: any H that is a multiple of 16, any group size, and one scale
+// per row with a CTA-wide reduction. Each thread keeps the next row block's
+// loads (64 bytes) in flight while it computes the current one.
 template <class Src, int OUT, int SCALE, bool CTA_REDUCE>
 __global__ void __launch_bounds__(kMaxThreads)
 row_quant_kernel(typename Src::Args a, OutArgs o, RowShape sh)
@@ -242,39 +393,28 @@ row_quant_kernel(typename Src::Args a, OutArgs o, RowShape sh)
     __shared__ float red[2][32];
     Src src;
     const int tid = threadIdx.x;
-    const int slot = tid / sh.tpr;               // row slot in this CTA
-    const int lr = tid - slot * sh.tpr;          // thread index within the row
+    const int nthr = blockDim.x;
+    const int slot = tid / sh.tpr;
+    const int lr = tid - slot * sh.tpr;
     const bool slot_ok = slot < sh.rpc;
     const int col0 = lr * kEPT;
     const int64_t nrb = (sh.T + sh.rpc - 1) / sh.rpc;
     const int tpg_mask = (1 << sh.tpg_log2) - 1;
     const int group_idx = CTA_REDUCE ? 0 : (lr >> sh.tpg_log2);
     const bool first_of_group = CTA_REDUCE ? (tid == 0) : ((lr & tpg_mask) == 0);
-
     typename Src::Regs cur, nxt;
     int64_t rb = blockIdx.x;
     int64_t row = rb * sh.rpc + slot;
     bool ok = slot_ok && rb < nrb && row < sh.T;
-    if (ok)
-        Src::load(a, row, col0, cur);
-    else
-        Src::zero(cur);
-
+    if (ok) Src::load(a, row, col0, cur); else Src::zero(cur);
     int it = 0;
     for (; rb < nrb; rb += gridDim.x, ++it) {
         const int64_t nrow = (rb + gridDim.x) * sh.rpc + slot;
         const bool nok = slot_ok && (rb + gridDim.x) < nrb && nrow < sh.T;
-        if (nok)
-            Src::load(a, nrow, col0, nxt);
-        else
-            Src::zero(nxt);
-
-        float y[kEPT];
-        src.produce(a, cur, row, ok, y);
+        if (nok) Src::load(a, nrow, col0, nxt); else Src::zero(nxt);
+        uint64_t ny[kEPT / 2];
         float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kEPT; ++i)
-            amax = fmaxf(amax, fabsf(y[i]));
+        src.produce(a, cur, ok, ny, amax);
 
         if (CTA_REDUCE) {
 #pragma unroll
@@ -284,20 +424,152 @@ row_quant_kernel(typename Src::Args a, OutArgs o, RowShape sh)
             if ((tid & 31) == 0)
                 buf[tid >> 5] = amax;
             __syncthreads();
-            const int nwarps = (blockDim.x + 31) >> 5;
+            const int nwarps = (nthr + 31) >> 5;
             amax = 0.0f;
             for (int w = 0; w < nwarps; ++w)
                 amax = fmaxf(amax, buf[w]);
         } else {
-            for (int off = 1; off <= tpg_mask; off <<= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+            // five shuffles always; offsets past the group mask to 0 (no-op)
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off & tpg_mask));
         }
         if (ok)
-            quantize_store<OUT, SCALE>(y, amax, row, col0, group_idx, first_of_group, sh, o);
+            quantize_store<OUT, SCALE>(ny, amax, row, col0, group_idx, first_of_group, sh, o);
+        cur = nxt; row = nrow; ok = nok;
+    }
+    src.finish(a);
+}
 
-        cur = nxt;
-        row = nrow;
-        ok = nok;
+// ----------------------------------------------------- warp_stream_kernel
+
+constexpr int kStreamThreads = 256;   // 8 warps per CTA
+
+// Src additionally supplies: kSpans spans of kSpanBytes per warp slice (the
+// warp's 512 columns of the gate half and of the up half, or of the cast
+// input), span(args, row, col_base, s) -> their global addresses,
+// fetch_span(slot, lane, regs) -> the lane's bytes from a filled slot, and
+// scalar(args, row) -> the optional per-row fp32 (nullptr if none).
+//
+// Shared memory: warp w owns `stages` slots of kSpans * kSpanBytes bytes at
+// w * stages * slot_bytes, and `stages` mbarriers after all rings.
+// Task k of a warp (its k-th slice) uses slot k % stages with parity
+// (k / stages) & 1; the slot is refilled with task k + stages as soon as the
+// warp has read it, before the arithmetic, so `stages` copies stay in flight.
+template <class Src, int OUT, int SCALE>
+__global__ void __launch_bounds__(kStreamThreads)
+warp_stream_kernel(typename Src::Args a, OutArgs o, RowShape sh)
+{
+    constexpr uint32_t kSlot = Src::kSpans * Src::kSpanBytes;
+    extern __shared__ __align__(128) uint8_t smem[];
+    Src src;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = sh.stages;
+    const int nwarps = blockDim.x >> 5;
+    uint8_t *ring = smem + (size_t)warp * S * kSlot;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)nwarps * S * kSlot) + warp * S;
+    const int tpg_mask = (1 << sh.tpg_log2) - 1;
+
+    // Task t of the grid is slice t % wpr of row t / wpr; a warp takes tasks
+    // first, first + stride, ... Cursors hold (row, slice) and advance by the
+    // stride's quotient and remainder, so no division runs per task.
+    const int stride = (int)gridDim.x * nwarps;          // < 2^31: grid <= SMs * CTAs per SM
+    const int d_row = stride / sh.wpr;
+    const int d_sl = stride - d_row * sh.wpr;
+    struct Cursor {
+        int64_t row;
+        int sl;
+    };
+    auto advance = [&](Cursor &c) {
+        c.row += d_row;
+        c.sl += d_sl;
+        if (c.sl >= sh.wpr) {
+            c.sl -= sh.wpr;
+            ++c.row;
+        }
+    };
+    const int first = (int)blockIdx.x * nwarps + warp;
+    Cursor cur{first / sh.wpr, first % sh.wpr};
+
+    auto issue = [&](const Cursor &c, int slot) {   // lane 0 only
+        uint8_t *dst = ring + (size_t)slot * kSlot;
+        mbar_arrive_expect_tx(bars + slot, kSlot);
+#pragma unroll
+        for (int sp = 0; sp < Src::kSpans; ++sp)
+            bulk_g2s(dst + sp * Src::kSpanBytes, Src::span(a, c.row, c.sl * 512, sp), Src::kSpanBytes,
+                     bars + slot);
+    };
+
+    Cursor fill = cur;   // the next task to copy in
+    if (lane == 0) {
+        for (int i = 0; i < S; ++i)
+            mbar_init(bars + i, 1);
+        fence_mbar_init();
+    }
+    for (int i = 0; i < S; ++i) {
+        if (lane == 0 && fill.row < sh.T)
+            issue(fill, i);
+        advance(fill);
+    }
+    __syncwarp();
+
+    const float *wp = cur.row < sh.T ? Src::scalar(a, cur.row) : nullptr;
+    float w_next = wp ? __ldg(wp) : 1.0f;
+    int slot = 0;
+    uint32_t parity = 0;
+    while (cur.row < sh.T) {
+        const int64_t row = cur.row;
+        const int cbase = cur.sl * 512;
+        const float w_cur = w_next;
+        advance(cur);
+        if (cur.row < sh.T) {
+            const float *np = Src::scalar(a, cur.row);
+            w_next = np ? __ldg(np) : 1.0f;
+        }
+        if (!mbar_wait_bounded(bars + slot, parity)) {
+            // give up: flag it, let the copies already issued land, leave
+            if (lane == 0)
+                atomicOr(sh.fault, 1u);
+            int sl = slot;
+            uint32_t par = parity;
+            Cursor c = cur;
+            for (int i = 1; i < S; ++i) {
+                if (++sl == S) {
+                    sl = 0;
+                    par ^= 1u;
+                }
+                if (c.row < sh.T)
+                    mbar_wait_bounded(bars + sl, par);
+                advance(c);
+            }
+            return;
+        }
+        typename Src::Regs regs;
+        Src::fetch_span(ring + (size_t)slot * kSlot, lane, regs);
+        Src::set_scalar(regs, w_cur);
+        __syncwarp();
+        if (fill.row < sh.T) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(fill, slot);
+            }
+        }
+        advance(fill);
+
+        uint64_t ny[kEPT / 2];
+        float amax = 0.0f;
+        src.produce(a, regs, true, ny, amax);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off & tpg_mask));
+        const int lr = (cbase >> 4) + lane;
+        quantize_store<OUT, SCALE>(ny, amax, row, cbase + lane * kEPT, lr >> sh.tpg_log2,
+                                   (lr & tpg_mask) == 0, sh, o);
+        if (++slot == S) {
+            slot = 0;
+            parity ^= 1u;
+        }
     }
     src.finish(a);
 }
@@ -331,6 +603,7 @@ struct SwigluSrc {
         ld_stream_256(p + a.H, r.u);
         r.w = a.w ? __ldg(a.w + row) : 1.0f;
     }
+
     __device__ __forceinline__ static void zero(Regs &r)
     {
 #pragma unroll
@@ -340,24 +613,50 @@ struct SwigluSrc {
         }
         r.w = 0.0f;
     }
-    __device__ __forceinline__ void produce(const Args &a, const Regs &r, int64_t, bool ok,
-                                            float (&y)[kEPT])
+
+    static constexpr int kSpans = 2;          // the gate half, the up half
+    static constexpr int kSpanBytes = 1024;   // 512 bf16 columns
+
+    __device__ __forceinline__ static const void *span(const Args &a, int64_t row, int cbase, int sp)
+    {
+        return a.x + row * (2 * (int64_t)a.H) + sp * a.H + cbase;
+    }
+    __device__ __forceinline__ static const float *scalar(const Args &a, int64_t row)
+    {
+        return a.w ? a.w + row : nullptr;
+    }
+    __device__ __forceinline__ static void fetch_span(const uint8_t *slot, int lane, Regs &r)
+    {
+        const uint4 *g = reinterpret_cast<const uint4 *>(slot + lane * 32);
+        const uint4 *u = reinterpret_cast<const uint4 *>(slot + 1024 + lane * 32);
+        const uint4 g0 = g[0], g1 = g[1], u0 = u[0], u1 = u[1];
+        r.g[0] = g0.x; r.g[1] = g0.y; r.g[2] = g0.z; r.g[3] = g0.w;
+        r.g[4] = g1.x; r.g[5] = g1.y; r.g[6] = g1.z; r.g[7] = g1.w;
+        r.u[0] = u0.x; r.u[1] = u0.y; r.u[2] = u0.z; r.u[3] = u0.w;
+        r.u[4] = u1.x; r.u[5] = u1.y; r.u[6] = u1.z; r.u[7] = u1.w;
+    }
+    __device__ __forceinline__ static void set_scalar(Regs &r, float w) { r.w = w; }
+    __device__ __forceinline__ void produce(const Args &a, const Regs &r, bool ok,
+                                            uint64_t (&ny)[kEPT / 2], float &amax)
     {
         const float L = a.limit;
+        const uint64_t w2n = splat(-r.w);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float g[2] = {bf16_lo(r.g[i]), bf16_hi(r.g[i])};
-            float u[2] = {bf16_lo(r.u[i]), bf16_hi(r.u[i])};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (CLAMP) {
-                    cnt_g += (ok && g[h] > L) ? 1u : 0u;
-                    cnt_u += (ok && fabsf(u[h]) > L) ? 1u : 0u;
-                    g[h] = fminf(g[h], L);
-                    u[h] = fminf(fmaxf(u[h], -L), L);
-                }
-                y[2 * i + h] = __fmul_rn(__fmul_rn(silu(g[h]), u[h]), r.w);
+            float g0 = bf16_lo(r.g[i]), g1 = bf16_hi(r.g[i]);
+            float u0 = bf16_lo(r.u[i]), u1 = bf16_hi(r.u[i]);
+            if (CLAMP) {
+                cnt_g += (ok && g0 > L) ? 1u : 0u;
+                cnt_g += (ok && g1 > L) ? 1u : 0u;
+                cnt_u += (ok && fabsf(u0) > L) ? 1u : 0u;
+                cnt_u += (ok && fabsf(u1) > L) ? 1u : 0u;
+                g0 = fminf(g0, L);
+                g1 = fminf(g1, L);
+                u0 = fminf(fmaxf(u0, -L), L);
+                u1 = fminf(fmaxf(u1, -L), L);
             }
+            ny[i] = neg_swiglu2(g0, g1, u0, u1, w2n);
+            amax = fmaxf(amax, fmaxf(fabsf(plo(ny[i])), fabsf(phi(ny[i]))));
         }
     }
     __device__ __forceinline__ void finish(const Args &a)
@@ -387,18 +686,38 @@ struct CastBf16Src {
     {
         ld_stream_256(static_cast<const uint16_t *>(a.x) + row * (int64_t)a.H + col0, r.v);
     }
+
     __device__ __forceinline__ static void zero(Regs &r)
     {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             r.v[i] = 0u;
     }
-    __device__ __forceinline__ void produce(const Args &, const Regs &r, int64_t, bool, float (&y)[kEPT])
+
+    static constexpr int kSpans = 1;
+    static constexpr int kSpanBytes = 1024;   // 512 bf16 columns
+
+    __device__ __forceinline__ static const void *span(const Args &a, int64_t row, int cbase, int)
+    {
+        return static_cast<const uint16_t *>(a.x) + row * (int64_t)a.H + cbase;
+    }
+    __device__ __forceinline__ static const float *scalar(const Args &, int64_t) { return nullptr; }
+    __device__ __forceinline__ static void fetch_span(const uint8_t *slot, int lane, Regs &r)
+    {
+        const uint4 *p = reinterpret_cast<const uint4 *>(slot + lane * 32);
+        const uint4 c0 = p[0], c1 = p[1];
+        r.v[0] = c0.x; r.v[1] = c0.y; r.v[2] = c0.z; r.v[3] = c0.w;
+        r.v[4] = c1.x; r.v[5] = c1.y; r.v[6] = c1.z; r.v[7] = c1.w;
+    }
+    __device__ __forceinline__ static void set_scalar(Regs &, float) {}
+    __device__ __forceinline__ void produce(const Args &, const Regs &r, bool, uint64_t (&ny)[kEPT / 2],
+                                            float &amax)
     {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            y[2 * i] = bf16_lo(r.v[i]);
-            y[2 * i + 1] = bf16_hi(r.v[i]);
+            const float y0 = bf16_lo(r.v[i]), y1 = bf16_hi(r.v[i]);
+            ny[i] = pk(-y0, -y1);
+            amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
         }
     }
     __device__ __forceinline__ void finish(const Args &) {}
@@ -415,17 +734,44 @@ struct CastF32Src {
         ld_stream_256(p, lo);
         ld_stream_256(p + 8, hi);
     }
+
     __device__ __forceinline__ static void zero(Regs &r)
     {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
             r.v[i] = 0u;
     }
-    __device__ __forceinline__ void produce(const Args &, const Regs &r, int64_t, bool, float (&y)[kEPT])
+
+    static constexpr int kSpans = 1;
+    static constexpr int kSpanBytes = 2048;   // 512 fp32 columns
+
+    __device__ __forceinline__ static const void *span(const Args &a, int64_t row, int cbase, int)
+    {
+        return static_cast<const float *>(a.x) + row * (int64_t)a.H + cbase;
+    }
+    __device__ __forceinline__ static const float *scalar(const Args &, int64_t) { return nullptr; }
+    __device__ __forceinline__ static void fetch_span(const uint8_t *slot, int lane, Regs &r)
+    {
+        const uint4 *p = reinterpret_cast<const uint4 *>(slot + lane * 64);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint4 c = p[k];
+            r.v[4 * k] = c.x;
+            r.v[4 * k + 1] = c.y;
+            r.v[4 * k + 2] = c.z;
+            r.v[4 * k + 3] = c.w;
+        }
+    }
+    __device__ __forceinline__ static void set_scalar(Regs &, float) {}
+    __device__ __forceinline__ void produce(const Args &, const Regs &r, bool, uint64_t (&ny)[kEPT / 2],
+                                            float &amax)
     {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            y[i] = __uint_as_float(r.v[i]);
+        for (int i = 0; i < 8; ++i) {
+            const float y0 = __uint_as_float(r.v[2 * i]), y1 = __uint_as_float(r.v[2 * i + 1]);
+            ny[i] = pk(-y0, -y1);
+            amax = fmaxf(amax, fmaxf(fabsf(y0), fabsf(y1)));
+        }
     }
     __device__ __forceinline__ void finish(const Args &) {}
 };

@@ -17,7 +17,22 @@ const void *pick(bool clamp, bool cta)
         return cta ? fn<OUT, SCALE, true, true>() : fn<OUT, SCALE, true, false>();
     return cta ? fn<OUT, SCALE, false, true>() : fn<OUT, SCALE, false, false>();
 }
+template <int OUT, int SCALE>
+const void *stream_fn(bool clamp)
+{
+    return clamp ? reinterpret_cast<const void *>(&warp_stream_kernel<SwigluSrc<true>, OUT, SCALE>)
+                 : reinterpret_cast<const void *>(&warp_stream_kernel<SwigluSrc<false>, OUT, SCALE>);
+}
 }  // namespace
+
+const void *swiglu_stream_fn(int out_fmt, int scale_fmt, bool clamp)
+{
+    if (out_fmt == kOutE4M3)
+        return scale_fmt == kScaleF32 ? stream_fn<kOutE4M3, kScaleF32>(clamp) : stream_fn<kOutE4M3, kScaleUE8M0>(clamp);
+    if (out_fmt == kOutE2M1)
+        return scale_fmt == kScaleF32 ? stream_fn<kOutE2M1, kScaleF32>(clamp) : stream_fn<kOutE2M1, kScaleUE8M0>(clamp);
+    return nullptr;
+}
 
 const void *swiglu_kernel_fn(int out_fmt, int scale_fmt, bool clamp, bool cta_reduce)
 {
@@ -30,14 +45,14 @@ const void *swiglu_kernel_fn(int out_fmt, int scale_fmt, bool clamp, bool cta_re
     return nullptr;
 }
 
-cudaError_t launch_swiglu(const void *kfn, int grid, int block, const SwigluArgs &a,
+cudaError_t launch_swiglu(const void *kfn, int grid, int block, size_t smem, const SwigluArgs &a,
                           const OutArgs &o, const RowShape &sh, cudaStream_t stream)
 {
     SwigluArgs a_ = a;
     OutArgs o_ = o;
     RowShape sh_ = sh;
     void *args[] = {&a_, &o_, &sh_};
-    return cudaLaunchKernel(kfn, dim3(grid), dim3(block), args, 0, stream);
+    return cudaLaunchKernel(kfn, dim3(grid), dim3(block), args, smem, stream);
 }
 
 }  // namespace tk

@@ -13,8 +13,9 @@ weights; synthetic inputs from workloads.py). Prints ONE JSON line on rank 0.
             launch's dirty outputs (steady state).
   roofline  algorithmic bytes per launch / average launch time vs the
             measured HBM copy bandwidth.
-  e2e       the same metric through the C ABI with pinned host buffers: every
-            step copies its inputs host->device and its codes and scales back.
+  e2e       the same metric through the host-buffer C-ABI call with pinned
+            host buffers: every step copies its inputs host->device and its
+            codes and scales back, chunked so the copies overlap the kernel.
   cpu_baseline  the CPU oracle on a bounded sample of rows (rank 0, N=1).
 
 --impl reference times the CPU oracle itself (the only reference this method
@@ -54,6 +55,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle sample for cpu_baseline")
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--e2e-chunk-rows", type=int, default=1024)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--jsonl", default=None, help="also append the JSON line to this file")
@@ -383,21 +385,48 @@ def run_ours(args, dist: Dist):
     return 0
 
 
+def kernel_source_hash() -> str:
+    """sha256 over the CUDA sources, to tell whether a committed ncu summary
+    still describes the kernel that runs."""
+    import hashlib
+    csrc = os.path.join(ROOT, "activation_fp8_quantization_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
 def load_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary for this workload
-    and the current kernel, if one exists (profiles/<workload>.traffic.json)."""
-    path = os.path.join(ROOT, "profiles", "swiglu_quant_%s.traffic.json" % workload)
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    from the committed ncu summary profiles/swiglu_quant_<workload>.md, or
+    None if there is none or it was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "swiglu_quant_%s.md" % workload)
+    fields = {}
     try:
         with open(path) as f:
-            return json.load(f).get("dram_bytes_per_launch")
-    except (OSError, ValueError):
+            for line in f:
+                if line.startswith("- ") and ": " in line:
+                    k, v = line[2:].strip().split(": ", 1)
+                    fields[k.strip("`")] = v.strip().strip("`")
+    except OSError:
+        return None
+    if fields.get("source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
         return None
 
 
 def measure_e2e(op, wl, x0, w0, dev, args, dist: Dist):
-    """The same metric through the public call with pinned host buffers: per
-    step, copy x (and w) host->device, run, copy codes and scales back."""
+    """The same metric through the host-buffer C-ABI call
+    (tk_swiglu_quant_run_host): inputs start and outputs end in page-locked
+    host memory; each step's rows are cut into chunks whose copy-in, kernel
+    and copy-out overlap on the pipe's three streams."""
     import torch
+    import activation_fp8_quantization_gb300 as tk
 
     T = wl.T
     x_h = x0.cpu().pin_memory()
@@ -405,44 +434,35 @@ def measure_e2e(op, wl, x0, w0, dev, args, dist: Dist):
     q_shape, s_shape, s_dtype = op.output_shapes(T)
     q_h = torch.empty(q_shape, dtype=torch.uint8).pin_memory()
     s_h = torch.empty(s_shape, dtype=s_dtype).pin_memory()
-    x_d = torch.empty_like(x0)
-    w_d = None if w0 is None else torch.empty_like(w0)
-    q_d = torch.empty(q_shape, dtype=torch.uint8, device=dev)
-    s_d = torch.empty(s_shape, dtype=s_dtype, device=dev)
-    counts = torch.zeros(2, dtype=torch.int64, device=dev) if op.count_clamped else None
+    c_h = torch.zeros(2, dtype=torch.int64).pin_memory() if op.count_clamped else None
+    pipe = tk.HostPipe(op, args.e2e_chunk_rows)
     stream = torch.cuda.Stream(device=dev)
 
     def step():
-        x_d.copy_(x_h, non_blocking=True)
-        if w_d is not None:
-            w_d.copy_(w_h, non_blocking=True)
-        op(x_d, w_d, q=q_d, scales=s_d, clamped_count=counts, stream=stream)
-        q_h.copy_(q_d, non_blocking=True)
-        s_h.copy_(s_d, non_blocking=True)
+        pipe(x_h, w_h, q=q_h, scales=s_h, clamped_count=c_h, stream=stream)
 
     n = max(1, args.e2e_steps)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
+    for _ in range(3):
+        step()
     stream.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     dist.barrier()
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(n):
-            step()
-        ev1.record(stream)
+    ev0.record(stream)
+    for _ in range(n):
+        step()
+    ev1.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
     ms = dist.max(ev0.elapsed_time(ev1), device=dev)
     rows_total = dist.sum(float(T * n), device=dev)
-    h2d = x_h.numel() * x_h.element_size() + (0 if w_h is None else w_h.numel() * 4)
-    d2h = q_h.numel() + s_h.numel() * s_h.element_size()
+    h2d = x_h.numel() * x_h.element_size() + (0 if w_h is None else w_h.numel() * 4) + (
+        0 if c_h is None else 16)
+    d2h = q_h.numel() + s_h.numel() * s_h.element_size() + (0 if c_h is None else 16)
     return {"value": rows_total / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
-            "path": "SwigluQuant call on pinned host buffers, copies on the launch stream"}
+            "path": "tk_swiglu_quant_run_host on pinned host buffers, %d-row chunks" % args.e2e_chunk_rows}
 
 
 def main(argv=None):

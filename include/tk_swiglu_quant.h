@@ -127,6 +127,56 @@ tk_status tk_swiglu_quant_launch_info(tk_swiglu_quant_plan_t plan, int64_t num_t
                                       int *grid, int *block, int *rows_per_cta, int *num_sms);
 
 /* ------------------------------------------------------------------------
+ * Host-buffer variant of the fused call
+ *
+ * For callers whose activations live in host memory: the rows are cut into
+ * chunks of `chunk_rows`; chunk c is copied host->device, processed and its
+ * codes and scales copied back, while the copy-in of the next chunk and the
+ * copy-out of the previous one proceed on two further streams (three ring
+ * slots of device workspace). A host pipe owns those internal streams and
+ * events (host-side objects; no device memory) and serves one call at a time:
+ * concurrent calls need one pipe each. The device workspace is the caller's.
+ * ---------------------------------------------------------------------- */
+
+typedef struct tk_swiglu_quant_host_pipe_s *tk_swiglu_quant_host_pipe_t;
+
+/* Make a pipe for `plan` moving `chunk_rows` rows per chunk (>= 1). The
+ * plan must outlive the pipe. Creates three streams and eleven events on the
+ * plan's device (TK_ERR_CUDA if that fails). */
+tk_status tk_swiglu_quant_host_pipe_create(tk_swiglu_quant_plan_t plan, int64_t chunk_rows,
+                                           tk_swiglu_quant_host_pipe_t *pipe);
+
+/* Release a pipe (NULL is accepted): waits for its streams, then destroys
+ * them and its events. */
+tk_status tk_swiglu_quant_host_pipe_destroy(tk_swiglu_quant_host_pipe_t pipe);
+
+/* Bytes of device workspace run_host needs (three chunk slots of input,
+ * weights, codes and scales, plus the clamp counter), at 256-byte alignment. */
+tk_status tk_swiglu_quant_host_workspace_size(tk_swiglu_quant_host_pipe_t pipe, size_t *bytes);
+
+/* Enqueue the fused op on host buffers, ordered after prior work on `stream`;
+ * later work on `stream` is ordered after the last copy back. Returns without
+ * synchronising: the host outputs are complete once `stream` has reached
+ * this point (e.g. cudaStreamSynchronize).
+ *   x_host, topk_weights_host    host inputs as in tk_swiglu_quant_run
+ *   q_host, scales_host          host outputs as in tk_swiglu_quant_run
+ *   clamped_count_host           host int64[2], ADDED to like the device
+ *                                counter (copied in, added to, copied back);
+ *                                required iff count_clamped
+ *   workspace                    device memory of at least
+ *                                tk_swiglu_quant_host_workspace_size bytes,
+ *                                256-byte aligned, not used by anything else
+ *                                until `stream` passes this call
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to run asynchronously and overlap; pageable memory works but
+ * the copies then serialise. The host buffers must stay valid and untouched
+ * until `stream` passes this call. */
+tk_status tk_swiglu_quant_run_host(tk_swiglu_quant_host_pipe_t pipe, int64_t num_tokens,
+                                   const void *x_host, const float *topk_weights_host,
+                                   void *q_host, void *scales_host, int64_t *clamped_count_host,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * Standalone per-token / per-block cast: x [T, H] (bf16 or fp32) -> codes + scales,
  * with the same grouping, scale and code rules as the fused call.
  * ---------------------------------------------------------------------- */
@@ -153,6 +203,14 @@ tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t num_tokens, const
 /* ------------------------------------------------------------------------
  * Diagnostics
  * ---------------------------------------------------------------------- */
+
+/* Read, and if `clear` is non-zero reset, the fault word of `device`. Bit 0
+ * is set by a kernel that gave up waiting for one of its own asynchronous
+ * copies (a wait over a second long, which no correct run reaches) and
+ * returned early, leaving that launch's outputs incomplete. The word is
+ * shared by every call on the device; the read is ordered after all work
+ * already submitted to the device (it synchronises with it). */
+tk_status tk_fault_word(int device, uint32_t *value, int clear);
 
 /* Static name of a status ("TK_OK", ...). Never NULL. */
 const char *tk_status_string(tk_status status);

@@ -265,3 +265,102 @@ def test_cast_bit_exact(in_dtype, H, group, scale_fmt, out_fmt):
         assert np.array_equal(gs, rs), "scale bytes differ"
     bad = np.argwhere(unpack(gq, out_fmt) != unpack(rq, out_fmt))
     assert bad.size == 0, "codes differ at %s" % (bad[:5].tolist(),)
+
+
+# ------------------------------------------------------ host-buffer pipe
+
+@pytest.mark.parametrize("chunk_rows", [1, 7, 1000, 4096, 100000])
+def test_host_pipe_matches_device_call(chunk_rows):
+    wl = wls.WORKLOADS["moe_T32768_H2048_g128_ue8m0_clamp7"].with_rows(3001)
+    x, w = wls.make_inputs(wl, "cpu")
+    op = _op(wl, count=True)
+    counts_d = torch.zeros(2, dtype=torch.int64, device="cuda")
+    qd, sd = _run(op, x.cuda(), w.cuda(), counts_d)
+    pipe = tk.HostPipe(op, chunk_rows)
+    xh, wh = x.pin_memory(), w.pin_memory()
+    counts_h = torch.tensor([5, 7], dtype=torch.int64).pin_memory()
+    for _ in range(2):   # the pipe and its workspace are reusable
+        qh, sh = pipe(xh, wh, clamped_count=counts_h)
+        torch.cuda.synchronize()
+        assert torch.equal(qh, qd.cpu()) and torch.equal(sh, sd.cpu())
+    c = counts_d.cpu()
+    assert counts_h.tolist() == [5 + 2 * int(c[0]), 7 + 2 * int(c[1])]
+
+
+def test_host_pipe_pageable_and_fp32_scales():
+    wl = wls.WORKLOADS["ragged_T100003_H3072_g128"].with_rows(777)
+    x, w = wls.make_inputs(wl, "cpu")
+    op = _op(wl)
+    qd, sd = _run(op, x.cuda(), w.cuda())
+    pipe = tk.HostPipe(op, 100)
+    q = torch.empty(op.output_shapes(777)[0], dtype=torch.uint8)          # pageable
+    s = torch.empty(op.output_shapes(777)[1], dtype=torch.float32)
+    pipe(x, w, q=q, scales=s)
+    torch.cuda.synchronize()
+    assert torch.equal(q, qd.cpu()) and torch.equal(s, sd.cpu())
+
+
+def test_host_pipe_errors():
+    op = tk.SwigluQuant(256, 128, "fp32", "e4m3", True)
+    pipe = tk.HostPipe(op, 64)
+    x = torch.zeros(8, 512, dtype=torch.bfloat16)
+    w = torch.ones(8)
+    q = torch.empty(8, 256, dtype=torch.uint8)
+    s = torch.empty(8, 2)
+    with pytest.raises(tk.TkError) as e:   # workspace too small
+        tk.tk_swiglu_quant_run_host(pipe.pipe, 8, x, w, q, s, None, pipe.workspace, 16, None)
+    assert e.value.status == 1
+    with pytest.raises(tk.TkError) as e:   # misaligned workspace
+        tk.tk_swiglu_quant_run_host(pipe.pipe, 8, x, w, q, s, None, pipe.workspace.data_ptr() + 8,
+                                    pipe.ws_bytes, None)
+    assert e.value.status == 3
+    with pytest.raises(tk.TkError) as e:   # weights expected
+        tk.tk_swiglu_quant_run_host(pipe.pipe, 8, x, None, q, s, None, pipe.workspace, pipe.ws_bytes, None)
+    assert e.value.status == 1
+
+
+# ------------------------------------------- both kernels on the same shapes
+
+def test_plan_picks_the_stream_kernel_where_it_applies():
+    # rows_per_cta == 0 marks the warp-stream kernel (widths a multiple of 512
+    # whose scale groups fit in a warp's 512 columns)
+    assert tk.SwigluQuant(2048, 128).launch_info(8192)["rows_per_cta"] == 0
+    assert tk.SwigluQuant(512, 0).launch_info(256)["rows_per_cta"] == 0
+    assert tk.SwigluQuant(4096, 0).launch_info(256)["rows_per_cta"] == 1     # CTA reduction
+    assert tk.SwigluQuant(1040, 16).launch_info(256)["rows_per_cta"] > 0
+
+
+@pytest.mark.parametrize("name", wls.ORDER)
+def test_row_kernel_forced_parity(name, monkeypatch):
+    """TK_KERNEL=rows makes the plan take the row-block kernel even where the
+    stream kernel applies; both must agree with the oracle."""
+    monkeypatch.setenv("TK_KERNEL", "rows")
+    wl = wls.WORKLOADS[name]
+    op = _op(wl, count=True)
+    assert op.launch_info(1000)["rows_per_cta"] > 0
+    rows = 2 * op.launch_info(1 << 30)["grid"] * op.launch_info(1 << 30)["rows_per_cta"] + 19
+    x, w = wls.make_inputs(wl.with_rows(rows), "cpu")
+    counts = torch.zeros(2, dtype=torch.int64, device="cuda")
+    q, s = _run(op, x.cuda(), None if w is None else w.cuda(), counts if op.count_clamped else None)
+    ref = _oracle(wl, x, w)
+    compare(q.cpu().numpy(), s.cpu().numpy(), ref, wl.group, wl.scale_fmt, wl.out_fmt).check(name)
+    if op.count_clamped:
+        assert counts.cpu().tolist() == ref["counts"].tolist()
+
+
+@pytest.mark.parametrize("stages", [2, 3, 5, 8])
+def test_stream_ring_depths(stages, monkeypatch):
+    monkeypatch.setenv("TK_PIPELINE_STAGES", str(stages))
+    wl = wls.WORKLOADS["moe_T32768_H2048_g128_ue8m0_clamp7"].with_rows(5000)
+    op = _op(wl, count=True)
+    x, w = wls.make_inputs(wl, "cpu")
+    counts = torch.zeros(2, dtype=torch.int64, device="cuda")
+    q, s = _run(op, x.cuda(), w.cuda(), counts)
+    ref = _oracle(wl, x, w)
+    compare(q.cpu().numpy(), s.cpu().numpy(), ref, wl.group, wl.scale_fmt, wl.out_fmt).check(str(stages))
+    assert counts.cpu().tolist() == ref["counts"].tolist()
+
+
+def test_fault_word_clear_after_runs():
+    torch.cuda.synchronize()
+    assert tk.tk_fault_word(torch.cuda.current_device()) == 0
