@@ -23,12 +23,14 @@ from ._abi import (IN_DTYPES, OUT_FMTS, SCALE_FMTS, QuantCastDesc, SwigluQuantDe
                    tk_swiglu_quant_host_pipe_create, tk_swiglu_quant_host_pipe_destroy,
                    tk_swiglu_quant_host_workspace_size, tk_swiglu_quant_launch_info,
                    tk_swiglu_quant_output_sizes, tk_swiglu_quant_plan, tk_swiglu_quant_plan_destroy,
-                   tk_swiglu_quant_run, tk_swiglu_quant_run_host, tk_swiglu_quant_validate)
+                   tk_swiglu_quant_run, tk_swiglu_quant_run_host, tk_swiglu_quant_run_host_static,
+                   tk_swiglu_quant_validate)
 
 __all__ = [
     "SwigluQuant", "HostPipe", "QuantCast", "swiglu_quant", "quant_cast", "TkError",
     "tk_swiglu_quant_host_pipe_create", "tk_swiglu_quant_host_pipe_destroy",
     "tk_swiglu_quant_host_workspace_size", "tk_swiglu_quant_run_host",
+    "tk_swiglu_quant_run_host_static",
     "SwigluQuantDesc", "QuantCastDesc", "tk_swiglu_quant_validate", "tk_swiglu_quant_plan",
     "tk_swiglu_quant_plan_destroy", "tk_swiglu_quant_output_sizes", "tk_swiglu_quant_run",
     "tk_swiglu_quant_launch_info", "tk_quant_cast_validate", "tk_quant_cast_plan",

@@ -58,6 +58,8 @@ SIGNATURES = {
     "tk_swiglu_quant_host_workspace_size": (ctypes.c_int, [_VP, _PSZ]),
     "tk_swiglu_quant_run_host": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP,
                                                 ctypes.c_size_t, _VP]),
+    "tk_swiglu_quant_run_host_static": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP,
+                                                       _VP]),
     "tk_quant_cast_validate": (ctypes.c_int, [ctypes.POINTER(QuantCastDesc)]),
     "tk_quant_cast_plan": (ctypes.c_int, [ctypes.POINTER(QuantCastDesc), ctypes.c_int,
                                           ctypes.POINTER(_VP)]),
@@ -163,6 +165,17 @@ def tk_swiglu_quant_run_host(pipe: int, num_tokens: int, x_host, topk_weights_ho
     check(lib().tk_swiglu_quant_run_host(pipe, num_tokens, _ptr(x_host), _ptr(topk_weights_host),
                                          _ptr(q_host), _ptr(scales_host), _ptr(clamped_count_host),
                                          _ptr(workspace), workspace_bytes, stream))
+
+
+def tk_swiglu_quant_run_host_static(pipe: int, num_tokens: int, x_host, topk_weights_host, q_host,
+                                    scales_host, clamped_count_host, stream: int | None) -> None:
+    check(lib().tk_swiglu_quant_run_host_static(pipe, num_tokens, _ptr(x_host), _ptr(topk_weights_host),
+                                                _ptr(q_host), _ptr(scales_host),
+                                                _ptr(clamped_count_host), stream))
+
+
+# TK_STATIC_SCRATCH_BYTES of the header
+STATIC_SCRATCH_BYTES = 32 << 20
 
 
 def tk_quant_cast_validate(desc: QuantCastDesc) -> int:

@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -615,6 +616,54 @@ TK_API tk_status tk_swiglu_quant_run_host(tk_swiglu_quant_host_pipe_t pipe, int6
     if (e != cudaSuccess)
         return cuda_fail(e, "enqueueing the host-buffer pipeline");
     return ok();
+}
+
+// ------------------------------------------- host-buffer call without allocation
+
+// The workspace of tk_swiglu_quant_run_host_static: one array per device,
+// reserved when the library's module loads, shared by every such call.
+static __device__ __align__(256) unsigned char g_tk_static_scratch[TK_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 256;
+std::mutex g_static_mu;
+void *g_static_addr[kMaxDevices] = {};   // device address of the array, looked up once per device
+}  // namespace
+
+TK_API tk_status tk_swiglu_quant_run_host_static(tk_swiglu_quant_host_pipe_t pipe, int64_t T, const void *x_host,
+                                                 const float *w_host, void *q_host, void *scales_host,
+                                                 int64_t *count_host, void *stream)
+{
+    if (!pipe)
+        return fail(TK_ERR_INVALID_ARG, "pipe is NULL");
+    if (pipe->total_bytes > TK_STATIC_SCRATCH_BYTES)
+        return fail(TK_ERR_UNSUPPORTED,
+                    "the pipe needs %zu bytes of workspace but the built-in array holds %zu: "
+                    "make the pipe with fewer chunk_rows",
+                    pipe->total_bytes, (size_t)TK_STATIC_SCRATCH_BYTES);
+    const int device = pipe->plan->device;
+    if (device < 0 || device >= kMaxDevices)
+        return fail(TK_ERR_UNSUPPORTED, "device %d is beyond the %d devices this call supports", device,
+                    kMaxDevices);
+    tk_status st = check_current_device(device);
+    if (st != TK_OK)
+        return st;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        if (!g_static_addr[device]) {
+            // the symbol's host name is only a stand-in; the device address
+            // comes from the runtime, with this device current
+            cudaError_t e = cudaGetSymbolAddress(&g_static_addr[device], g_tk_static_scratch);
+            if (e != cudaSuccess) {
+                g_static_addr[device] = nullptr;
+                return cuda_fail(e, "cudaGetSymbolAddress of the built-in workspace");
+            }
+        }
+        scratch = g_static_addr[device];
+    }
+    return tk_swiglu_quant_run_host(pipe, T, x_host, w_host, q_host, scales_host, count_host, scratch,
+                                    TK_STATIC_SCRATCH_BYTES, stream);
 }
 
 // ------------------------------------------------------------ standalone cast

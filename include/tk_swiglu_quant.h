@@ -176,6 +176,44 @@ tk_status tk_swiglu_quant_run_host(tk_swiglu_quant_host_pipe_t pipe, int64_t num
                                    void *q_host, void *scales_host, int64_t *clamped_count_host,
                                    void *workspace, size_t workspace_bytes, void *stream);
 
+/* Size of the device array that tk_swiglu_quant_run_host_static uses as its
+ * workspace: 32 MiB, held on every GPU that loads this library until the
+ * process exits. */
+#define TK_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* The host-buffer call for callers that cannot allocate device memory.
+ *
+ * The pages describe no such entry point; it exists for integration. Some
+ * callers are not allowed to call cudaMalloc or any allocating routine: a
+ * plug-in running inside a host application whose allocator owns all device
+ * memory (a serving runtime that has carved the whole HBM into its own pool),
+ * code with a fixed memory budget that must not grow at run time, or a
+ * process whose policy forbids new device allocations after start-up. Such a
+ * caller still has its activations in host memory and wants the codes and
+ * scales back in host memory.
+ *
+ * This call does exactly what tk_swiglu_quant_run_host does, with the same
+ * arguments except the workspace: the three chunk slots and the clamp
+ * counter live in one static device array of TK_STATIC_SCRATCH_BYTES inside
+ * this library. The call allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine); it only enqueues copies and kernels.
+ *   - The pipe's workspace (tk_swiglu_quant_host_workspace_size) must fit in
+ *     TK_STATIC_SCRATCH_BYTES; otherwise the call returns TK_ERR_UNSUPPORTED
+ *     and enqueues nothing: make the pipe with fewer chunk_rows (1024 rows
+ *     fit for hidden 2048; about 300 for hidden 7168).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current, once; make that first
+ *     call before any stream capture.
+ *   - Every call on a device shares the one array, and it keeps the last
+ *     call's contents; nothing in it needs clearing, since each call writes
+ *     every byte before reading it. Calls whose work overlaps on the GPU race
+ *     on the array: issue them on one stream, or order them with events.
+ * Statuses as tk_swiglu_quant_run_host. */
+tk_status tk_swiglu_quant_run_host_static(tk_swiglu_quant_host_pipe_t pipe, int64_t num_tokens,
+                                          const void *x_host, const float *topk_weights_host,
+                                          void *q_host, void *scales_host,
+                                          int64_t *clamped_count_host, void *stream);
+
 /* ------------------------------------------------------------------------
  * Standalone per-token / per-block cast: x [T, H] (bf16 or fp32) -> codes + scales,
  * with the same grouping, scale and code rules as the fused call.
