@@ -189,11 +189,34 @@ __device__ unsigned int g_tk_fault_word;
 
 namespace {
 
-// Validate the device, pick the kernel (the stream kernel when the width is a
-// multiple of 512 and a scale group fits in a warp's slice; TK_KERNEL=rows
-// forces the row kernel) and size its launch.
+// Both kernels of a plan: the row kernel always, the stream kernel where it
+// applies. TK_KERNEL=rows or =stream (read when the plan is made) forces one.
+struct Launches {
+    Launch rows;
+    Launch stream;
+    bool has_stream;
+    int forced;   // 0: by size, 1: rows, 2: stream
+};
+
+// The stream kernel pays off once every resident warp has several slices to
+// stream (its ring stays full); smaller batches go to the row kernel, whose
+// register prefetch starts up faster.
+constexpr int64_t kStreamMinTasksPerWarp = 16;
+
+const Launch &pick(const Launches &Ls, int64_t T)
+{
+    if (!Ls.has_stream || Ls.forced == 1)
+        return Ls.rows;
+    if (Ls.forced == 2)
+        return Ls.stream;
+    const int64_t warps = (int64_t)Ls.stream.max_grid * (Ls.stream.block / 32);
+    return T * Ls.stream.wpr >= kStreamMinTasksPerWarp * warps ? Ls.stream : Ls.rows;
+}
+
+// Validate the device and size one kernel's launch: the stream kernel when
+// `want_stream` (the caller checked that it applies), else the row kernel.
 tk_status make_launch(int device, int64_t hidden, int32_t group, const void *row_fn, const void *stream_fn,
-                      int slot_bytes, Launch *L)
+                      int slot_bytes, bool want_stream, Launch *L)
 {
     int count = 0;
     cudaError_t e = cudaGetDeviceCount(&count);
@@ -220,9 +243,7 @@ tk_status make_launch(int device, int64_t hidden, int32_t group, const void *row
     L->tpr = geo.tpr;
     L->tpg_log2 = geo.tpg_log2;
     L->groups = geo.groups;
-    const char *force = getenv("TK_KERNEL");
-    const bool want_rows = force && strcmp(force, "rows") == 0;
-    L->stream = stream_fn && hidden % 512 == 0 && !geo.cta_reduce && !want_rows;
+    L->stream = want_stream;
     if (L->stream) {
         L->fn = stream_fn;
         L->block = tk::kStreamThreads;
@@ -256,6 +277,22 @@ tk_status make_launch(int device, int64_t hidden, int32_t group, const void *row
     return TK_OK;
 }
 
+tk_status make_launches(int device, int64_t hidden, int32_t group, const void *row_fn, const void *stream_fn,
+                        int slot_bytes, Launches *Ls)
+{
+    *Ls = Launches{};
+    const char *force = getenv("TK_KERNEL");
+    Ls->forced = !force ? 0 : (strcmp(force, "rows") == 0 ? 1 : (strcmp(force, "stream") == 0 ? 2 : 0));
+    tk_status st = make_launch(device, hidden, group, row_fn, stream_fn, slot_bytes, false, &Ls->rows);
+    if (st != TK_OK)
+        return st;
+    const Geometry geo = geometry(hidden, group);
+    Ls->has_stream = stream_fn && hidden % 512 == 0 && !geo.cta_reduce;
+    if (Ls->has_stream)
+        st = make_launch(device, hidden, group, row_fn, stream_fn, slot_bytes, true, &Ls->stream);
+    return st;
+}
+
 tk_status check_current_device(int device)
 {
     int cur = -1;
@@ -273,13 +310,13 @@ tk_status check_current_device(int device)
 struct tk_swiglu_quant_plan_s {
     tk_swiglu_quant_desc desc;
     int device;
-    Launch L;
+    Launches Ls;
 };
 
 struct tk_quant_cast_plan_s {
     tk_quant_cast_desc desc;
     int device;
-    Launch L;
+    Launches Ls;
 };
 
 // ------------------------------------------------------------------ fused op
@@ -316,11 +353,11 @@ TK_API tk_status tk_swiglu_quant_plan(const tk_swiglu_quant_desc *d, int device,
     const void *stream_fn = tk::swiglu_stream_fn(d->out_fmt, d->scale_fmt, clamp);
     if (!row_fn)
         return fail(TK_ERR_UNSUPPORTED, "no kernel for this combination");
-    Launch L{};
-    st = make_launch(device, d->hidden, d->group_size, row_fn, stream_fn, tk::kSwigluSlotBytes, &L);
+    Launches Ls{};
+    st = make_launches(device, d->hidden, d->group_size, row_fn, stream_fn, tk::kSwigluSlotBytes, &Ls);
     if (st != TK_OK)
         return st;
-    auto *p = new (std::nothrow) tk_swiglu_quant_plan_s{*d, device, L};
+    auto *p = new (std::nothrow) tk_swiglu_quant_plan_s{*d, device, Ls};
     if (!p)
         return fail(TK_ERR_INVALID_ARG, "out of host memory");
     *plan = p;
@@ -385,7 +422,7 @@ TK_API tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t T, con
     a.limit = d.use_clamp ? d.clamp_limit : 0.0f;
     a.H = (int32_t)d.hidden;
     tk::OutArgs o{static_cast<uint8_t *>(q), scales};
-    const Launch &L = plan->L;
+    const Launch &L = pick(plan->Ls, T);
     cudaError_t e = tk::launch_swiglu(L.fn, grid_for(L, T), L.block, L.smem, a, o, shape_for(L, T, d.hidden),
                                       static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
@@ -398,14 +435,15 @@ TK_API tk_status tk_swiglu_quant_launch_info(tk_swiglu_quant_plan_t plan, int64_
 {
     if (!plan || T < 0)
         return fail(TK_ERR_INVALID_ARG, "plan is NULL or num_tokens < 0");
+    const Launch &L = pick(plan->Ls, T);
     if (grid)
-        *grid = T == 0 ? 0 : grid_for(plan->L, T);
+        *grid = T == 0 ? 0 : grid_for(L, T);
     if (block)
-        *block = plan->L.block;
+        *block = L.block;
     if (rows_per_cta)
-        *rows_per_cta = plan->L.stream ? 0 : plan->L.rpc;
+        *rows_per_cta = L.stream ? 0 : L.rpc;
     if (num_sms)
-        *num_sms = plan->L.num_sms;
+        *num_sms = L.num_sms;
     return ok();
 }
 
@@ -588,7 +626,7 @@ TK_API tk_status tk_swiglu_quant_run_host(tk_swiglu_quant_host_pipe_t pipe, int6
             a.limit = d.use_clamp ? d.clamp_limit : 0.0f;
             a.H = (int32_t)d.hidden;
             tk::OutArgs o{sq, ssc};
-            const Launch &L = plan->L;
+            const Launch &L = pick(plan->Ls, rows);
             e = tk::launch_swiglu(L.fn, grid_for(L, rows), L.block, L.smem, a, o, shape_for(L, rows, d.hidden),
                                   pipe->s_k);
         }
@@ -693,12 +731,12 @@ TK_API tk_status tk_quant_cast_plan(const tk_quant_cast_desc *d, int device, tk_
     const void *stream_fn = tk::cast_stream_fn(d->in_dtype, d->out_fmt, d->scale_fmt);
     if (!row_fn)
         return fail(TK_ERR_UNSUPPORTED, "no kernel for this combination");
-    Launch L{};
-    st = make_launch(device, d->hidden, d->group_size, row_fn, stream_fn,
-                     d->in_dtype == TK_IN_BF16 ? tk::kCastBf16SlotBytes : tk::kCastF32SlotBytes, &L);
+    Launches Ls{};
+    st = make_launches(device, d->hidden, d->group_size, row_fn, stream_fn,
+                       d->in_dtype == TK_IN_BF16 ? tk::kCastBf16SlotBytes : tk::kCastF32SlotBytes, &Ls);
     if (st != TK_OK)
         return st;
-    auto *p = new (std::nothrow) tk_quant_cast_plan_s{*d, device, L};
+    auto *p = new (std::nothrow) tk_quant_cast_plan_s{*d, device, Ls};
     if (!p)
         return fail(TK_ERR_INVALID_ARG, "out of host memory");
     *plan = p;
@@ -734,7 +772,7 @@ TK_API tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t T, const v
         return st;
     tk::CastArgs a{x, (int32_t)d.hidden};
     tk::OutArgs o{static_cast<uint8_t *>(q), scales};
-    const Launch &L = plan->L;
+    const Launch &L = pick(plan->Ls, T);
     cudaError_t e = tk::launch_cast(L.fn, grid_for(L, T), L.block, L.smem, a, o, shape_for(L, T, d.hidden),
                                     static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)

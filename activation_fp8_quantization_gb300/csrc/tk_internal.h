@@ -22,6 +22,24 @@ const void *cast_stream_fn(int in_dtype, int out_fmt, int scale_fmt);
 cudaError_t launch_cast(const void *fn, int grid, int block, size_t smem, const CastArgs &a,
                         const OutArgs &o, const RowShape &sh, cudaStream_t stream);
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel of the stream drains; it waits for that kernel
+// itself (griddepcontrol.wait) before touching global memory.
+inline cudaError_t launch_pdl(const void *fn, int grid, int block, size_t smem, void **args, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 // Bytes of one warp-ring slot of the stream kernels.
 constexpr int kSwigluSlotBytes = SwigluSrc<false>::kSpans * SwigluSrc<false>::kSpanBytes;
 constexpr int kCastBf16SlotBytes = CastBf16Src::kSpans * CastBf16Src::kSpanBytes;

@@ -97,6 +97,18 @@ __device__ __forceinline__ void st_stream_64(void *p, uint32_t a, uint32_t b)
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Wait until the grid this launch depends on (the previous kernel in the
+// stream, if it was launched as a programmatic dependency) has completed and
+// its memory is visible; a no-op otherwise. Called before the first global
+// access, so results never depend on what ran before.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel in the stream to be scheduled now: its CTAs take SMs
+// as this grid's CTAs retire and then wait in pdl_wait() for this grid.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ------------------------------------------------------ TMA and mbarriers
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
@@ -402,6 +414,8 @@ row_quant_kernel(typename Src::Args a, OutArgs o, RowShape sh)
     const int tpg_mask = (1 << sh.tpg_log2) - 1;
     const int group_idx = CTA_REDUCE ? 0 : (lr >> sh.tpg_log2);
     const bool first_of_group = CTA_REDUCE ? (tid == 0) : ((lr & tpg_mask) == 0);
+    pdl_wait();
+    pdl_launch_dependents();
     typename Src::Regs cur, nxt;
     int64_t rb = blockIdx.x;
     int64_t row = rb * sh.rpc + slot;
@@ -501,6 +515,8 @@ warp_stream_kernel(typename Src::Args a, OutArgs o, RowShape sh)
                      bars + slot);
     };
 
+    pdl_wait();
+    pdl_launch_dependents();
     Cursor fill = cur;   // the next task to copy in
     if (lane == 0) {
         for (int i = 0; i < S; ++i)

@@ -52,7 +52,7 @@ cudaError_t launch_swiglu(const void *kfn, int grid, int block, size_t smem, con
     OutArgs o_ = o;
     RowShape sh_ = sh;
     void *args[] = {&a_, &o_, &sh_};
-    return cudaLaunchKernel(kfn, dim3(grid), dim3(block), args, smem, stream);
+    return launch_pdl(kfn, grid, block, smem, args, stream);
 }
 
 }  // namespace tk

@@ -121,8 +121,11 @@ tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t num_tokens,
                               const void *x, const float *topk_weights, void *q,
                               void *scales, int64_t *clamped_count, void *stream);
 
-/* Launch shape the plan chose (host only): CTAs in the persistent grid, threads
- * per CTA, rows one CTA processes per iteration, and the SM count used. */
+/* Launch shape a run of num_tokens rows would use (host only): CTAs in the
+ * persistent grid, threads per CTA, rows one CTA processes per iteration (0
+ * when the warp-stream kernel runs: each warp then streams 512-column
+ * slices), and the SM count. A plan holds two kernels where the width is a
+ * multiple of 512 and picks one per run by num_tokens. */
 tk_status tk_swiglu_quant_launch_info(tk_swiglu_quant_plan_t plan, int64_t num_tokens,
                                       int *grid, int *block, int *rows_per_cta, int *num_sms);
 

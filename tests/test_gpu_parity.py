@@ -35,12 +35,23 @@ def _oracle(wl, x_cpu, w_cpu):
                                wl.group, wl.scale_fmt, wl.out_fmt, clamp=wl.clamp, want_y=True)
 
 
+def _rows_for_two_passes(op):
+    """Rows that make every CTA (row kernel) or every warp (stream kernel) of
+    the full grid take two steps, plus a ragged tail."""
+    info = op.launch_info(1 << 30)
+    if info["rows_per_cta"]:
+        return 2 * info["grid"] * info["rows_per_cta"] + 37
+    wpr = op.hidden // 512
+    return 2 * info["grid"] * (info["block"] // 32) // wpr + 37
+
+
+@pytest.mark.parametrize("kernel", ["rows", "stream"])
 @pytest.mark.parametrize("name", wls.ORDER)
-def test_workload_small_parity(name):
+def test_workload_small_parity(name, kernel, monkeypatch):
+    monkeypatch.setenv("TK_KERNEL", kernel)
     wl = wls.WORKLOADS[name]
     op = _op(wl, count=True)
-    info = op.launch_info(1 << 30)
-    rows = 2 * info["grid"] * info["rows_per_cta"] + 37
+    rows = _rows_for_two_passes(op)
     wl_s = wl.with_rows(rows)
     x, w = wls.make_inputs(wl_s, "cpu")
     counts = torch.zeros(2, dtype=torch.int64, device="cuda")
@@ -50,7 +61,7 @@ def test_workload_small_parity(name):
     rep.check(name)
     if op.count_clamped:
         assert counts.cpu().tolist() == ref["counts"].tolist()
-    print(name, rows, "rows: identical %.6f, boundary groups %d, flips %d" % (
+    print(name, kernel, rows, "rows: identical %.6f, boundary groups %d, flips %d" % (
         rep.identical_frac, rep.n_boundary_groups, rep.n_boundary_flips))
 
 
@@ -104,10 +115,14 @@ GEOMS = [  # (H, group) incl. the CTA-reduction path (one scale per row, wide or
 ]
 
 
+@pytest.mark.parametrize("kernel", ["rows", "stream"])
 @pytest.mark.parametrize("H,group", GEOMS)
 @pytest.mark.parametrize("scale_fmt,out_fmt", [("fp32", "e4m3"), ("ue8m0", "e4m3"),
                                                ("ue8m0", "e2m1"), ("fp32", "e2m1")])
-def test_geometry_sweep(H, group, scale_fmt, out_fmt):
+def test_geometry_sweep(H, group, scale_fmt, out_fmt, kernel, monkeypatch):
+    """Forcing the stream kernel on a shape it does not apply to leaves the
+    row kernel in place, so those cases run the row kernel twice."""
+    monkeypatch.setenv("TK_KERNEL", kernel)
     rng = np.random.default_rng(H * 7 + group)
     T = 29
     x = torch.from_numpy(rng.standard_normal((T, 2 * H)).astype(np.float32) * 2).to(torch.bfloat16)
@@ -125,8 +140,10 @@ def _bf16(a):
     return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
 
 
-def test_special_rows():
-    H, g = 256, 128
+@pytest.mark.parametrize("kernel", ["rows", "stream"])
+def test_special_rows(kernel, monkeypatch):
+    monkeypatch.setenv("TK_KERNEL", kernel)
+    H, g = 512, 128
     rows = []
     rows.append(np.zeros(2 * H))                                            # all zero
     rows.append(np.concatenate([np.full(H, -95.0), np.full(H, 3.0)]))      # silu underflows to subnormals
@@ -236,11 +253,13 @@ def test_host_side_errors():
 
 # ----------------------------------------------------- standalone cast
 
+@pytest.mark.parametrize("kernel", ["rows", "stream"])
 @pytest.mark.parametrize("in_dtype", ["fp32", "bf16"])
 @pytest.mark.parametrize("H,group", [(2048, 128), (512, 0), (7168, 0), (1024, 32), (48, 16)])
 @pytest.mark.parametrize("scale_fmt,out_fmt", [("fp32", "e4m3"), ("ue8m0", "e4m3"),
                                                ("ue8m0", "e2m1"), ("fp32", "e2m1")])
-def test_cast_bit_exact(in_dtype, H, group, scale_fmt, out_fmt):
+def test_cast_bit_exact(in_dtype, H, group, scale_fmt, out_fmt, kernel, monkeypatch):
+    monkeypatch.setenv("TK_KERNEL", kernel)
     """With the activation given as input there is nothing approximate left:
     scales and codes must equal the oracle's bit for bit."""
     rng = np.random.default_rng(H + group)
@@ -321,36 +340,49 @@ def test_host_pipe_errors():
 
 # ------------------------------------------- both kernels on the same shapes
 
-def test_plan_picks_the_stream_kernel_where_it_applies():
-    # rows_per_cta == 0 marks the warp-stream kernel (widths a multiple of 512
-    # whose scale groups fit in a warp's 512 columns)
-    assert tk.SwigluQuant(2048, 128).launch_info(8192)["rows_per_cta"] == 0
-    assert tk.SwigluQuant(512, 0).launch_info(256)["rows_per_cta"] == 0
-    assert tk.SwigluQuant(4096, 0).launch_info(256)["rows_per_cta"] == 1     # CTA reduction
-    assert tk.SwigluQuant(1040, 16).launch_info(256)["rows_per_cta"] > 0
+def test_plan_picks_the_kernel_by_batch_size():
+    # rows_per_cta == 0 marks the warp-stream kernel. It applies to widths
+    # that are multiples of 512 whose scale groups fit in a warp's 512
+    # columns, and runs once every resident warp has >= 16 slices to stream.
+    op = tk.SwigluQuant(2048, 128)
+    assert op.launch_info(1024)["rows_per_cta"] > 0
+    assert op.launch_info(65536)["rows_per_cta"] == 0
+    assert tk.SwigluQuant(512, 0).launch_info(1 << 20)["rows_per_cta"] == 0
+    assert tk.SwigluQuant(4096, 0).launch_info(1 << 20)["rows_per_cta"] == 1    # CTA reduction
+    assert tk.SwigluQuant(1040, 16).launch_info(1 << 20)["rows_per_cta"] > 0
 
 
-@pytest.mark.parametrize("name", wls.ORDER)
-def test_row_kernel_forced_parity(name, monkeypatch):
-    """TK_KERNEL=rows makes the plan take the row-block kernel even where the
-    stream kernel applies; both must agree with the oracle."""
-    monkeypatch.setenv("TK_KERNEL", "rows")
-    wl = wls.WORKLOADS[name]
-    op = _op(wl, count=True)
-    assert op.launch_info(1000)["rows_per_cta"] > 0
-    rows = 2 * op.launch_info(1 << 30)["grid"] * op.launch_info(1 << 30)["rows_per_cta"] + 19
-    x, w = wls.make_inputs(wl.with_rows(rows), "cpu")
-    counts = torch.zeros(2, dtype=torch.int64, device="cuda")
-    q, s = _run(op, x.cuda(), None if w is None else w.cuda(), counts if op.count_clamped else None)
-    ref = _oracle(wl, x, w)
-    compare(q.cpu().numpy(), s.cpu().numpy(), ref, wl.group, wl.scale_fmt, wl.out_fmt).check(name)
-    if op.count_clamped:
-        assert counts.cpu().tolist() == ref["counts"].tolist()
+def test_back_to_back_launches_see_the_previous_output():
+    """Launches may be scheduled while the previous kernel of the stream
+    drains; each waits for it before reading. Chain the fused kernel into a
+    cast that reads the fused kernel's fp32 scales as its input, on one stream
+    with no synchronisation in between, and compare with a synchronised run."""
+    wl = wls.WORKLOADS["moe_T8192_H2048_g128"]
+    x, w = wls.make_inputs(wl, "cuda")
+    op = _op(wl)
+    cast = tk.QuantCast(16, 16, "fp32", "e4m3", "fp32")
+    ref_s = None
+    for chained in (False, True):
+        s = torch.full((wl.T, 16), -1.0, device="cuda")
+        q = torch.empty((wl.T, wl.H), dtype=torch.uint8, device="cuda")
+        for _ in range(3):
+            s.fill_(-1.0)
+            op(x, w, q=q, scales=s)
+            if not chained:
+                torch.cuda.synchronize()
+            q2, s2 = cast(s)
+        torch.cuda.synchronize()
+        if ref_s is None:
+            ref_s = (s.clone(), q2.clone(), s2.clone())
+        else:
+            assert torch.equal(s, ref_s[0]) and torch.equal(q2, ref_s[1]) and torch.equal(s2, ref_s[2])
+    assert bool((ref_s[0] > 0).all())
 
 
 @pytest.mark.parametrize("stages", [2, 3, 5, 8])
 def test_stream_ring_depths(stages, monkeypatch):
     monkeypatch.setenv("TK_PIPELINE_STAGES", str(stages))
+    monkeypatch.setenv("TK_KERNEL", "stream")
     wl = wls.WORKLOADS["moe_T32768_H2048_g128_ue8m0_clamp7"].with_rows(5000)
     op = _op(wl, count=True)
     x, w = wls.make_inputs(wl, "cpu")
