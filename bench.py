@@ -55,7 +55,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle sample for cpu_baseline")
     p.add_argument("--e2e-steps", type=int, default=200)
-    p.add_argument("--e2e-chunk-rows", type=int, default=1024)
+    p.add_argument("--e2e-chunk-rows", type=int, default=2048)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--jsonl", default=None, help="also append the JSON line to this file")
