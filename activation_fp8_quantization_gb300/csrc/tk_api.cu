@@ -144,6 +144,16 @@ tk::RowShape shape_for(const Launch &L, int64_t T, int64_t hidden)
     return tk::RowShape{T, (int32_t)hidden, L.tpr, L.tpg_log2, L.rpc, L.groups, L.stages, L.wpr, L.fault};
 }
 
+// A clamp limit whose fp32 bits end in 16 zeros is a bf16 value: the kernels
+// then clamp the bf16 inputs directly, two lanes per instruction.
+void set_packed_limit(tk::SwigluArgs &a)
+{
+    uint32_t bits;
+    memcpy(&bits, &a.limit, sizeof bits);
+    a.packed_clamp = (bits & 0xffffu) == 0;
+    a.limit2 = (bits >> 16) * 0x00010001u;
+}
+
 int env_int(const char *name, int dflt)
 {
     const char *v = getenv(name);
@@ -421,6 +431,7 @@ TK_API tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t T, con
     a.counts = d.count_clamped ? reinterpret_cast<unsigned long long *>(clamped_count) : nullptr;
     a.limit = d.use_clamp ? d.clamp_limit : 0.0f;
     a.H = (int32_t)d.hidden;
+    set_packed_limit(a);
     tk::OutArgs o{static_cast<uint8_t *>(q), scales};
     const Launch &L = pick(plan->Ls, T);
     cudaError_t e = tk::launch_swiglu(L.fn, grid_for(L, T), L.block, L.smem, a, o, shape_for(L, T, d.hidden),
@@ -625,6 +636,7 @@ TK_API tk_status tk_swiglu_quant_run_host(tk_swiglu_quant_host_pipe_t pipe, int6
             a.counts = d.count_clamped ? reinterpret_cast<unsigned long long *>(dcount) : nullptr;
             a.limit = d.use_clamp ? d.clamp_limit : 0.0f;
             a.H = (int32_t)d.hidden;
+            set_packed_limit(a);
             tk::OutArgs o{sq, ssc};
             const Launch &L = pick(plan->Ls, rows);
             e = tk::launch_swiglu(L.fn, grid_for(L, rows), L.block, L.smem, a, o, shape_for(L, rows, d.hidden),

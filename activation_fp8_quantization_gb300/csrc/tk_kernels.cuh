@@ -598,7 +598,35 @@ struct SwigluArgs {
     unsigned long long *counts;   // [2] or null
     float limit;
     int32_t H;
+    uint32_t limit2;              // the limit as bf16 in both halves (when packed_clamp)
+    int32_t packed_clamp;         // the limit is exact in bf16: clamp and count on packed bf16 pairs
 };
+
+// bf16x2 lane-wise min, max and comparisons (all-ones or zero per 16-bit lane)
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_gt_mask(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("set.gt.u32.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_ne_mask(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("set.ne.u32.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
 
 struct Regs32x2 {
     uint32_t g[8];
@@ -657,6 +685,28 @@ struct SwigluSrc {
     {
         const float L = a.limit;
         const uint64_t w2n = splat(-r.w);
+        if (CLAMP && a.packed_clamp) {
+            // The limit is a bf16 value, so clamping the bf16 inputs is exact
+            // and two lanes go per instruction. A lane's clamp is recorded as
+            // one bit (bit i of its half for pair i); popc counts them.
+            const uint32_t L2 = a.limit2, nL2 = a.limit2 ^ 0x80008000u;
+            uint32_t mg = 0, mu = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t bit = 0x00010001u << i;
+                mg |= bf16x2_gt_mask(r.g[i], L2) & bit;
+                const uint32_t gc = bf16x2_min(r.g[i], L2);
+                const uint32_t uc = bf16x2_max(bf16x2_min(r.u[i], L2), nL2);
+                mu |= bf16x2_ne_mask(uc, r.u[i]) & bit;
+                ny[i] = neg_swiglu2(bf16_lo(gc), bf16_hi(gc), bf16_lo(uc), bf16_hi(uc), w2n);
+                amax = fmaxf(amax, fmaxf(fabsf(plo(ny[i])), fabsf(phi(ny[i]))));
+            }
+            if (ok) {
+                cnt_g += __popc(mg);
+                cnt_u += __popc(mu);
+            }
+            return;
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             float g0 = bf16_lo(r.g[i]), g1 = bf16_hi(r.g[i]);

@@ -28,18 +28,25 @@ class Workload:
     w_dist: str | None = None   # None | "topk8_norm" | "uniform"
     clamp: float | None = None
     seed: int = 0
+    op: str = "swiglu"          # "swiglu": x is [T, 2H] bf16; "cast": x is [T, H]
+    in_dtype: str = "bf16"      # cast input: "bf16" | "fp32"
 
     @property
     def groups_per_row(self) -> int:
         return 1 if self.group == 0 else self.H // self.group
 
+    @property
+    def x_cols(self) -> int:
+        return 2 * self.H if self.op == "swiglu" else self.H
+
     def algo_bytes(self, rows: int | None = None) -> int:
-        """Minimum HBM bytes one pass moves: bf16 input, codes, scales, weights."""
+        """Minimum HBM bytes one pass moves: input, codes, scales, weights."""
         T = self.T if rows is None else rows
+        x = T * self.x_cols * (4 if self.in_dtype == "fp32" else 2)
         q = T * self.H if self.out_fmt == "e4m3" else T * self.H // 2
         s = T * self.groups_per_row * (4 if self.scale_fmt == "fp32" else 1)
         w = 4 * T if self.w_dist else 0
-        return 4 * T * self.H + q + s + w
+        return x + q + s + w
 
     def with_rows(self, T: int) -> "Workload":
         return Workload(**{**self.__dict__, "T": T})
@@ -68,32 +75,46 @@ WORKLOADS = {
 
 ORDER = list(WORKLOADS)
 
+# Inputs of the standalone per-token / per-block cast (no SwiGLU): an
+# activation that is already computed, [T, H].
+CAST_WORKLOADS = {
+    "cast_T8192_H4096_g128_bf16": Workload("cast_T8192_H4096_g128_bf16", 8192, 4096, 128, "fp32",
+                                           "e4m3", "row_lognormal", seed=2001, op="cast"),
+    "cast_T16384_H7168_g128_ue8m0_bf16": Workload("cast_T16384_H7168_g128_ue8m0_bf16", 16384, 7168, 128,
+                                                  "ue8m0", "e4m3", "normal", seed=2002, op="cast"),
+    "cast_T8192_H4096_token_fp32": Workload("cast_T8192_H4096_token_fp32", 8192, 4096, 0, "fp32", "e4m3",
+                                            "row_lognormal", seed=2003, op="cast", in_dtype="fp32"),
+}
+ALL_WORKLOADS = {**WORKLOADS, **CAST_WORKLOADS}
+
 _CHUNK_ROWS = 4096
 
 
 def make_inputs(wl: Workload, device: str | torch.device = "cpu"):
-    """Return (x bf16 [T, 2H], w fp32 [T] or None) for a workload, drawn from
+    """Return (x [T, 2H] bf16, or [T, H] for a cast workload; w fp32 [T] or
+    None) for a workload, drawn from
     one torch.Generator seeded with wl.seed on ``device``. Rows are drawn in
     chunks of 4096 so that peak memory stays bounded at large T."""
     device = torch.device(device)
     gen = torch.Generator(device=device)
     gen.manual_seed(wl.seed)
-    T, H = wl.T, wl.H
-    x = torch.empty((T, 2 * H), dtype=torch.bfloat16, device=device)
+    T, C = wl.T, wl.x_cols
+    xdt = torch.float32 if wl.in_dtype == "fp32" else torch.bfloat16
+    x = torch.empty((T, C), dtype=xdt, device=device)
     for r0 in range(0, T, _CHUNK_ROWS):
         r1 = min(T, r0 + _CHUNK_ROWS)
         n = r1 - r0
-        v = torch.randn((n, 2 * H), generator=gen, device=device, dtype=torch.float32)
+        v = torch.randn((n, C), generator=gen, device=device, dtype=torch.float32)
         if wl.x_sigma != 1.0:
             v.mul_(wl.x_sigma)
         if wl.x_dist == "row_lognormal":
             v.mul_(torch.randn((n, 1), generator=gen, device=device).exp_())
         elif wl.x_dist == "outliers":
-            hit = torch.rand((n, 2 * H), generator=gen, device=device) < 1e-3
+            hit = torch.rand((n, C), generator=gen, device=device) < 1e-3
             v = torch.where(hit, v * 50.0, v)
         elif wl.x_dist != "normal":
             raise ValueError(wl.x_dist)
-        x[r0:r1] = v.to(torch.bfloat16)
+        x[r0:r1] = v.to(xdt)
     w = None
     if wl.w_dist is not None:
         w = torch.rand((T,), generator=gen, device=device, dtype=torch.float32)

@@ -189,23 +189,30 @@ def time_oracle(wl, seconds: float, seed_rows: int = 8) -> dict:
 
     lib = oracle.load()
     small = wl.with_rows(max(8, seed_rows))
-    x, w = wls.make_inputs(small, "cpu")
-    xb = wls.bf16_bits(x)
-    wn = None if w is None else w.numpy()
     t = time.perf_counter()
-    oracle.swiglu_quant(xb, wn, wl.group, wl.scale_fmt, wl.out_fmt, clamp=wl.clamp, lib=lib)
+    oracle_step(wl, *wls.make_inputs(small, "cpu"), lib)()
     per_row = (time.perf_counter() - t) / small.T
     rows = int(max(8, min(wl.T, seconds / max(per_row, 1e-9))))
     rows = max(8, (rows // 8) * 8)
-    sample = wl.with_rows(rows)
-    x, w = wls.make_inputs(sample, "cpu")
-    xb = wls.bf16_bits(x)
-    wn = None if w is None else w.numpy()
+    step = oracle_step(wl, *wls.make_inputs(wl.with_rows(rows), "cpu"), lib)
     t = time.perf_counter()
-    oracle.swiglu_quant(xb, wn, wl.group, wl.scale_fmt, wl.out_fmt, clamp=wl.clamp, lib=lib)
+    step()
     dt = time.perf_counter() - t
     return {"rows": rows, "seconds": dt, "tokens_per_s": rows / dt,
             "gbs": wl.algo_bytes(rows) / dt / 1e9}
+
+
+def oracle_step(wl, x, w, lib):
+    """A closure running the CPU oracle once on these rows (inputs prepared)."""
+    import oracle
+    from activation_fp8_quantization_gb300 import workloads as wls
+
+    if wl.op == "cast":
+        y = x.float().numpy()
+        return lambda: oracle.quant_rows_f32(y, wl.group, wl.scale_fmt, wl.out_fmt, lib=lib)
+    xb = wls.bf16_bits(x)
+    wn = None if w is None else w.numpy()
+    return lambda: oracle.swiglu_quant(xb, wn, wl.group, wl.scale_fmt, wl.out_fmt, clamp=wl.clamp, lib=lib)
 
 
 def run_reference(args, dist):
@@ -216,20 +223,14 @@ def run_reference(args, dist):
 
     if dist.rank != 0:
         return 0
-    wl = wls.WORKLOADS[args.workload]
+    wl = wls.ALL_WORKLOADS[args.workload]
     lib = oracle.load()
     # one step = a bounded sample of the workload; size it so K + W steps fit in ~2 minutes
     calib = time_oracle(wl, 0.5)
     per_row = calib["seconds"] / calib["rows"]
     budget = 120.0 / max(1, args.steps + args.warmup)
     rows = int(max(8, min(wl.T, budget / per_row)))
-    sample = wl.with_rows(rows)
-    x, w = wls.make_inputs(sample, "cpu")
-    xb = wls.bf16_bits(x)
-    wn = None if w is None else w.numpy()
-
-    def step():
-        oracle.swiglu_quant(xb, wn, wl.group, wl.scale_fmt, wl.out_fmt, clamp=wl.clamp, lib=lib)
+    step = oracle_step(wl, *wls.make_inputs(wl.with_rows(rows), "cpu"), lib)
 
     for _ in range(args.warmup):
         step()
@@ -239,7 +240,7 @@ def run_reference(args, dist):
     dt = time.perf_counter() - t
     value = rows * args.steps / dt
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "impl": "reference", "metric": metric_of(wl), "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64/f32", "data": "synthetic",
@@ -255,9 +256,18 @@ def run_reference(args, dist):
 
 
 def config_of(wl, n: int) -> dict:
-    return {"workload": wl.name, "T": wl.T, "H": wl.H, "group": wl.group, "scale_fmt": wl.scale_fmt,
-            "out_fmt": wl.out_fmt, "topk_weights": wl.w_dist is not None, "clamp": wl.clamp,
-            "parallelism": "replicas x%d" % n}
+    c = {"workload": wl.name, "T": wl.T, "H": wl.H, "group": wl.group, "scale_fmt": wl.scale_fmt,
+         "out_fmt": wl.out_fmt, "topk_weights": wl.w_dist is not None, "clamp": wl.clamp,
+         "parallelism": "replicas x%d" % n}
+    if wl.op != "swiglu":
+        c.update({"op": wl.op, "in_dtype": wl.in_dtype})
+    return c
+
+
+def metric_of(wl) -> str:
+    if wl.op == "cast":
+        return "tokens/s and achieved HBM GB/s (fraction of GB300 peak) for the standalone FP8 cast"
+    return METRIC
 
 
 def emit(line: dict, args):
@@ -280,10 +290,14 @@ def run_ours(args, dist: Dist):
         raise SystemExit("bench.py needs a CUDA GPU")
     dev = dist.local_rank
     torch.cuda.set_device(dev)
-    wl = wls.WORKLOADS[args.workload]
+    wl = wls.ALL_WORKLOADS[args.workload]
     T, H = wl.T, wl.H
-    op = tk.SwigluQuant(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.w_dist is not None, wl.clamp,
-                        wl.clamp is not None, dev)
+    if wl.op == "cast":
+        op = tk.QuantCast(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.in_dtype, dev)
+        op.count_clamped = False
+    else:
+        op = tk.SwigluQuant(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.w_dist is not None, wl.clamp,
+                            wl.clamp is not None, dev)
     algo = wl.algo_bytes()
     per_set = algo
     n_sets = max(2, -(-3 * L2_BYTES // per_set) + 1)   # sets beyond the current one hold > 3x L2
@@ -298,7 +312,6 @@ def run_ours(args, dist: Dist):
         ss.append(torch.empty(s_shape, dtype=s_dtype, device=dev))
     counts = torch.zeros(2, dtype=torch.int64, device=dev) if op.count_clamped else None
     lib = _abi.lib()
-    run = lib.tk_swiglu_quant_run
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
     cp = None if counts is None else counts.data_ptr()
@@ -307,7 +320,10 @@ def run_ours(args, dist: Dist):
 
     def launch(i):
         xp, wp, qp, spp = ptrs[i % n_sets]
-        st = run(op.plan, T, xp, wp, qp, spp, cp, sh)
+        if wl.op == "cast":
+            st = lib.tk_quant_cast_run(op.plan, T, xp, qp, spp, sh)
+        else:
+            st = lib.tk_swiglu_quant_run(op.plan, T, xp, wp, qp, spp, cp, sh)
         if st != 0:
             raise tk.TkError(st, _abi.tk_last_error_message())
 
@@ -352,7 +368,7 @@ def run_ours(args, dist: Dist):
     peaks = measured_peaks()
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and wl.op == "swiglu":
         e2e = measure_e2e(op, wl, x0, w0, dev, args, dist)
 
     cpu = None
@@ -365,7 +381,7 @@ def run_ours(args, dist: Dist):
         return 0
     traffic = load_traffic(wl.name)
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "metric": metric_of(wl), "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",

@@ -286,6 +286,29 @@ def test_cast_bit_exact(in_dtype, H, group, scale_fmt, out_fmt, kernel, monkeypa
     assert bad.size == 0, "codes differ at %s" % (bad[:5].tolist(),)
 
 
+@pytest.mark.parametrize("name", list(wls.CAST_WORKLOADS))
+def test_cast_workload_full_size(name):
+    """The standalone cast on its benchmark workloads, full size, in the
+    benchmark's launch configuration; sampled rows bit for bit."""
+    wl = wls.CAST_WORKLOADS[name]
+    x, _ = wls.make_inputs(wl, "cuda")
+    op = tk.QuantCast(wl.H, wl.group, wl.scale_fmt, wl.out_fmt, wl.in_dtype)
+    q, s = op(x)
+    torch.cuda.synchronize()
+    gen = np.random.default_rng(wl.seed)
+    idx = np.unique(np.concatenate([np.arange(32), np.arange(wl.T - 32, wl.T),
+                                    gen.choice(wl.T, size=256, replace=False)]))
+    it = torch.from_numpy(idx).cuda()
+    y = x.index_select(0, it).float().cpu().numpy()
+    rq, rs = oracle.quant_rows_f32(y, wl.group, wl.scale_fmt, wl.out_fmt)
+    gq, gs = q.index_select(0, it).cpu().numpy(), s.index_select(0, it).cpu().numpy()
+    assert np.array_equal(gq, rq)
+    if wl.scale_fmt == "fp32":
+        assert np.array_equal(gs.view(np.uint32), rs.view(np.uint32))
+    else:
+        assert np.array_equal(gs, rs)
+
+
 # ------------------------------------------------------ host-buffer pipe
 
 @pytest.mark.parametrize("chunk_rows", [1, 7, 1000, 4096, 100000])
