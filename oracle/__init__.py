@@ -25,6 +25,7 @@ CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast
 
 SCALE_FMTS = {"fp32": 0, "ue8m0": 1}
 OUT_FMTS = {"e4m3": 0, "e2m1": 1}
+SCALE_LAYOUTS = {"row": 0, "col": 1, "col_packed": 2}
 
 _lock = threading.Lock()
 _lib = None
@@ -73,6 +74,13 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
                                      c.c_int64, c.c_int, c.c_int, c.c_int, c.c_float,
                                      c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p]
     lib.tko_swiglu_quant.restype = c.c_int
+    lib.tko_scale_ld.argtypes = [c.c_int, c.c_int, c.c_int64]
+    lib.tko_scale_ld.restype = c.c_int64
+    lib.tko_scales_to_layout.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_int, c.c_int, c.c_void_p]
+    lib.tko_scales_to_layout.restype = c.c_int
+    lib.tko_moe_reduce.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_int64, c.c_int64,
+                                   c.c_void_p, c.c_void_p, c.c_int64, c.c_int64, c.c_float, c.c_void_p]
+    lib.tko_moe_reduce.restype = c.c_int
     return lib
 
 
@@ -148,3 +156,49 @@ def unpack_e2m1(packed: np.ndarray) -> np.ndarray:
     lo = packed & 0xF
     hi = packed >> 4
     return np.stack([lo, hi], axis=-1).reshape(*packed.shape[:-1], packed.shape[-1] * 2)
+
+
+def scales_to_layout(scales: np.ndarray, scale_fmt: str, layout: str, fill=0,
+                     lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Row-major scales [rows, G] -> a flat byte buffer in `layout`, padding
+    left at `fill` (bytes)."""
+    lib = lib or load()
+    scales = np.ascontiguousarray(scales)
+    rows, groups = scales.shape
+    code = SCALE_LAYOUTS[layout]
+    ld = lib.tko_scale_ld(code, SCALE_FMTS[scale_fmt], rows)
+    esz = 4 if scale_fmt == "fp32" else 1
+    if layout == "row":
+        nbytes = rows * groups * esz
+    elif layout == "col":
+        nbytes = groups * ld * esz
+    else:
+        nbytes = (groups // 4) * ld * 4
+    out = np.full(nbytes, fill, np.uint8)
+    rc = lib.tko_scales_to_layout(_ptr(scales), rows, groups, SCALE_FMTS[scale_fmt], code, _ptr(out))
+    if rc != 0:
+        raise ValueError("no such scale layout for these scales")
+    return out
+
+
+def moe_reduce(y: np.ndarray, pos: np.ndarray, w: np.ndarray, gs: float, y_scale=None,
+               lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """The weighted top-k combine. y: bf16 bits [R, H] (uint16) or E4M3 codes
+    [R, H] (uint8, with y_scale fp32 [R, H/128]); pos int32 [T, K] (-1 empty);
+    w fp32 [T, K]. Returns bf16 bits [T, H] (uint16)."""
+    lib = lib or load()
+    pos = np.ascontiguousarray(pos, np.int32)
+    w = np.ascontiguousarray(w, np.float32)
+    T, K = pos.shape
+    R, H = y.shape
+    out = np.zeros((T, H), np.uint16)
+    if y.dtype == np.uint16:
+        yb, yf, ys = np.ascontiguousarray(y), None, None
+    else:
+        yb, yf = None, np.ascontiguousarray(y, np.uint8)
+        ys = np.ascontiguousarray(y_scale, np.float32)
+    rc = lib.tko_moe_reduce(_ptr(yb), _ptr(yf), _ptr(ys), R, H, _ptr(pos), _ptr(w), T, K, float(gs),
+                            _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out

@@ -304,3 +304,133 @@ int tko_swiglu_quant(const uint16_t *x, int64_t rows, int64_t hidden, const floa
     }
     return 0;
 }
+
+/* ------------------------------------------------------------ scale layouts */
+
+#define TKO_LAYOUT_ROW 0
+#define TKO_LAYOUT_COL 1
+#define TKO_LAYOUT_COL_PACKED 2
+
+/* Padded rows per column of a column-major scale layout: 16 bytes worth of
+ * scale elements (4 fp32, 16 UE8M0 bytes), or rows rounded up to 4 for the
+ * packed words. */
+int64_t tko_scale_ld(int layout, int scale_fmt, int64_t rows)
+{
+    if (layout == TKO_LAYOUT_COL) {
+        int64_t per16 = (scale_fmt == TKO_SCALE_FP32) ? 4 : 16;
+        return (rows + per16 - 1) / per16 * per16;
+    }
+    if (layout == TKO_LAYOUT_COL_PACKED)
+        return (rows + 3) / 4 * 4;
+    return 0;
+}
+
+/* Copy row-major scales [rows, groups] into `layout` (the layouts a
+ * following FP8 GEMM reads: "TMA-aligned column-major scale factors" and
+ * "packed" UE8M0 in the quantization section of "TileLang + TileKernels",
+ * zhichai.net/topic/177618740; the exact placement is this library's
+ * reading):
+ *   column-major: element (t, j) at j * ld + t;
+ *   packed (UE8M0): byte k of 32-bit word m * ld + t is the exponent of group
+ *   4m + k of row t (little-endian words: byte address 4 (m ld + t) + k).
+ * Padding is not written. Returns 0, or -1 for a combination that has no
+ * layout. */
+int tko_scales_to_layout(const void *row_major, int64_t rows, int64_t groups, int scale_fmt,
+                         int layout, void *out)
+{
+    int64_t ld = tko_scale_ld(layout, scale_fmt, rows);
+    for (int64_t t = 0; t < rows; ++t) {
+        for (int64_t j = 0; j < groups; ++j) {
+            if (scale_fmt == TKO_SCALE_FP32) {
+                float v = ((const float *)row_major)[t * groups + j];
+                if (layout == TKO_LAYOUT_ROW)
+                    ((float *)out)[t * groups + j] = v;
+                else if (layout == TKO_LAYOUT_COL)
+                    ((float *)out)[j * ld + t] = v;
+                else
+                    return -1;
+            } else {
+                uint8_t v = ((const uint8_t *)row_major)[t * groups + j];
+                if (layout == TKO_LAYOUT_ROW)
+                    ((uint8_t *)out)[t * groups + j] = v;
+                else if (layout == TKO_LAYOUT_COL)
+                    ((uint8_t *)out)[j * ld + t] = v;
+                else if (groups % 4 == 0)
+                    ((uint8_t *)out)[4 * ((j / 4) * ld + t) + (j % 4)] = v;
+                else
+                    return -1;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------ top-k combine (reduce) */
+
+/* RNE of a double to bf16 (the upper half of an fp32), through fp32: a double
+ * rounds to fp32 first only if the fp32 rounding cannot create a bf16 tie, so
+ * here the bf16 value is found directly: the nearest bf16 by exhaustive
+ * comparison of the two bf16 neighbours of v, ties to the even mantissa. NaN
+ * and infinities are outside the contract. */
+static uint16_t bf16_rne_from_double(double v)
+{
+    float f = (float)v;                       /* the bf16 neighbours bracket f's */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint32_t lo_bits = u & 0xffff0000u;        /* toward zero in magnitude */
+    uint32_t hi_bits = lo_bits + 0x10000u;     /* next bf16 away from zero */
+    float lo, hi;
+    memcpy(&lo, &lo_bits, sizeof lo);
+    memcpy(&hi, &hi_bits, sizeof hi);
+    double dlo = fabs(v - (double)lo), dhi = fabs(v - (double)hi);
+    uint32_t pick;
+    if (dlo < dhi)
+        pick = lo_bits;
+    else if (dhi < dlo)
+        pick = hi_bits;
+    else
+        pick = ((lo_bits >> 16) & 1) ? hi_bits : lo_bits;
+    return (uint16_t)(pick >> 16);
+}
+
+/* The weighted top-k combine after the expert GEMMs ("TileKernels从入门到精通",
+ * zhichai.net/topic/177618752, ch.3 "结算中心的减法工程" and "动态寻址": routing
+ * weights, quantization factors and a global scale applied while gathering the
+ * expert rows through token_topk_to_pos, one read and one write):
+ *   out[t, i] = gs * sum_{k < K, pos[t,k] >= 0} w[t,k] * deq(y[pos[t,k], i]),
+ * with deq(y) = y for bf16 expert rows (y_fp8 == NULL) or, for E4M3 codes,
+ * decode(code) * y_scale[row, i / 128]. The sum is taken in double and
+ * rounded once to bf16 (round to nearest even).
+ *   y_bf16   [R, hidden] bf16 bits, or NULL when y_fp8 is given
+ *   y_fp8    [R, hidden] E4M3 codes, y_scale [R, hidden / 128] fp32
+ *   pos      [T, K] int32 row indices into y (-1: empty slot)
+ *   w        [T, K] fp32
+ *   out      [T, hidden] bf16 bits
+ * Returns 0, or -1 on a bad argument (a position outside [0, R)). */
+int tko_moe_reduce(const uint16_t *y_bf16, const uint8_t *y_fp8, const float *y_scale, int64_t R,
+                   int64_t hidden, const int32_t *pos, const float *w, int64_t T, int64_t K, float gs,
+                   uint16_t *out)
+{
+    if (hidden % 128 != 0 && y_fp8)
+        return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t i = 0; i < hidden; ++i) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                int32_t r = pos[t * K + k];
+                if (r < 0)
+                    continue;
+                if (r >= R)
+                    return -1;
+                double v;
+                if (y_fp8)
+                    v = tko_e4m3_decode(y_fp8[r * hidden + i]) * (double)y_scale[r * (hidden / 128) + i / 128];
+                else
+                    v = bf16_to_double(y_bf16[r * hidden + i]);
+                acc += (double)w[t * K + k] * v;
+            }
+            out[t * hidden + i] = bf16_rne_from_double((double)gs * acc);
+        }
+    }
+    return 0;
+}

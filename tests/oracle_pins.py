@@ -338,6 +338,91 @@ def pin_quant_rows_indexing(lib):
             assert tops == [c], (out_fmt, r, j, tops)
 
 
+def pin_scale_layouts(lib):
+    # column-major = numpy's transpose into a padded [G, ld] array; packed =
+    # little-endian words of four consecutive group exponents (hand example)
+    rng = np.random.default_rng(9)
+    for rows in (1, 3, 17):
+        f = rng.standard_normal((rows, 8)).astype(np.float32)
+        got = oracle.scales_to_layout(f, "fp32", "col", lib=lib).view(np.float32)
+        ld = -(-rows // 4) * 4
+        want = np.zeros((8, ld), np.float32)
+        want[:, :rows] = f.T
+        assert np.array_equal(got.reshape(8, ld), want), rows
+        b = rng.integers(0, 255, (rows, 8)).astype(np.uint8)
+        got = oracle.scales_to_layout(b, "ue8m0", "col", lib=lib)
+        ld = -(-rows // 16) * 16
+        want = np.zeros((8, ld), np.uint8)
+        want[:, :rows] = b.T
+        assert np.array_equal(got.reshape(8, ld), want), rows
+    b = np.array([[1, 2, 3, 4, 5, 6, 7, 8], [9, 10, 11, 12, 13, 14, 15, 16]], np.uint8)
+    words = oracle.scales_to_layout(b, "ue8m0", "col_packed", lib=lib).view("<u4").reshape(2, 4)
+    assert words[0, 0] == 0x04030201 and words[0, 1] == 0x0C0B0A09
+    assert words[1, 0] == 0x08070605 and words[1, 1] == 0x100F0E0D
+    assert words[0, 2] == 0 and words[1, 3] == 0     # padding rows 2, 3 not written
+
+
+def _bf16_to_f64(bits):
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def pin_moe_reduce(lib):
+    # hand-worked: y rows [1, 2] and [3, -1]; token 0 takes both with weights
+    # 0.5 and 0.25 -> [1.25, 0.75]; token 1 takes row 1 with weight 2 and an
+    # empty slot -> [6, -2] (bf16 0x3FA0 0x3F40 0x40C0 0xC000)
+    y = np.array([[0x3F80, 0x4000], [0x4040, 0xBF80]], np.uint16)
+    pos = np.array([[0, 1], [1, -1]], np.int32)
+    w = np.array([[0.5, 0.25], [2.0, 9.0]], np.float32)
+    assert oracle.moe_reduce(y, pos, w, 1.0, lib=lib).reshape(-1).tolist() == [0x3FA0, 0x3F40, 0x40C0, 0xC000]
+    # global scale multiplies the sum
+    assert oracle.moe_reduce(y, pos, w, 2.0, lib=lib).reshape(-1).tolist() == [0x4020, 0x3FC0, 0x4140, 0xC080]
+    # exact bf16 midpoints round to the even mantissa: 1 + 2^-8 lies between
+    # 1.0 (0x3F80) and 1 + 2^-7 (0x3F81) -> 0x3F80; 1 + 3 * 2^-8 lies between
+    # 0x3F81 and 0x3F82 -> 0x3F82
+    one = np.array([[0x3F80]], np.uint16)
+    for wt, want in ((1 + 2.0 ** -8, 0x3F80), (1 + 3 * 2.0 ** -8, 0x3F82)):
+        got = oracle.moe_reduce(one, np.array([[0]], np.int32), np.array([[wt]], np.float32), 1.0, lib=lib)
+        assert int(got[0, 0]) == want, (wt, hex(int(got[0, 0])))
+    rng = np.random.default_rng(13)
+    R, H, T, K = 40, 256, 9, 4
+    yb = _bf16_bits(rng.standard_normal((R, H)))
+    # identity: one slot, weight 1, scale 1 gives the gathered rows back exactly
+    perm = rng.permutation(R)[:T].astype(np.int32)
+    got = oracle.moe_reduce(yb, perm[:, None], np.ones((T, 1), np.float32), 1.0, lib=lib)
+    assert np.array_equal(got, yb[perm])
+    # all slots empty: zeros
+    got = oracle.moe_reduce(yb, np.full((T, K), -1, np.int32), np.ones((T, K), np.float32), 1.0, lib=lib)
+    assert not got.any()
+    # against a float64 einsum rounded to bf16 by torch (<= 1 bf16 ulp: torch may
+    # round through fp32)
+    pos = rng.integers(-1, R, (T, K)).astype(np.int32)
+    w = rng.uniform(0, 1, (T, K)).astype(np.float32)
+    yv = _bf16_to_f64(yb)
+    ref = np.zeros((T, H))
+    for t in range(T):
+        for k in range(K):
+            if pos[t, k] >= 0:
+                ref[t] += float(w[t, k]) * yv[pos[t, k]]
+    ref_b = torch.tensor(0.75 * ref).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.moe_reduce(yb, pos, w, 0.75, lib=lib)
+    diff = np.abs(got.astype(np.int32) - ref_b.astype(np.int32))
+    assert diff.max() <= 1 and (diff == 0).mean() > 0.99, diff.max()
+    # E4M3 rows with 1x128 scales: codes decode through torch's float8 view
+    codes = rng.integers(0, 256, (R, H)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0   # no NaN codes
+    sc = rng.uniform(0.5, 2.0, (R, H // 128)).astype(np.float32)
+    dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy() * np.repeat(sc, 128, axis=1)
+    ref = np.zeros((T, H))
+    for t in range(T):
+        for k in range(K):
+            if pos[t, k] >= 0:
+                ref[t] += float(w[t, k]) * dec[pos[t, k]]
+    ref_b = torch.tensor(ref).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.moe_reduce(codes, pos, w, 1.0, y_scale=sc, lib=lib)
+    diff = np.abs(got.astype(np.int32) - ref_b.astype(np.int32))
+    assert diff.max() <= 1 and (diff == 0).mean() > 0.99, diff.max()
+
+
 ALL_PINS = [
     pin_e4m3_decode_vs_torch,
     pin_e4m3_encode_vs_torch,
@@ -354,4 +439,6 @@ ALL_PINS = [
     pin_zero_and_signed_zero,
     pin_e2m1_packing,
     pin_quant_rows_indexing,
+    pin_scale_layouts,
+    pin_moe_reduce,
 ]

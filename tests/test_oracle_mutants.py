@@ -35,6 +35,13 @@ MUTANTS = {
     "bf16_shift": ("(uint32_t)b << 16", "(uint32_t)b << 15"),
     "zero_scale_kept": ("    if (s == 0.0f)\n        s = 1.0f;", ""),
     "quotient_multiplied": ("float quotient = y[i] / s;", "float quotient = y[i] * s;"),
+    "packed_byte_order": ("[4 * ((j / 4) * ld + t) + (j % 4)]", "[4 * ((j / 4) * ld + t) + (3 - j % 4)]"),
+    "column_major_transposed": ("((float *)out)[j * ld + t] = v;", "((float *)out)[t * ld + j] = v;"),
+    "reduce_weight_dropped": ("acc += (double)w[t * K + k] * v;", "acc += v;"),
+    "reduce_empty_slot_kept": ("if (r < 0)\n                    continue;", "if (r < 0)\n                    r = 0;"),
+    "reduce_global_scale_dropped": ("bf16_rne_from_double((double)gs * acc)", "bf16_rne_from_double(acc)"),
+    "reduce_fp8_scale_index": ("y_scale[r * (hidden / 128) + i / 128]", "y_scale[r * (hidden / 128)]"),
+    "reduce_bf16_ties_odd": ("pick = ((lo_bits >> 16) & 1) ? hi_bits : lo_bits;", "pick = ((lo_bits >> 16) & 1) ? lo_bits : hi_bits;"),
 }
 
 
