@@ -17,8 +17,9 @@ from __future__ import annotations
 import threading
 
 from . import _abi
-from ._abi import (IN_DTYPES, OUT_FMTS, SCALE_FMTS, QuantCastDesc, SwigluQuantDesc, TkError,
-                   tk_fault_word, tk_last_error_message, tk_quant_cast_plan, tk_quant_cast_plan_destroy,
+from ._abi import (IN_DTYPES, OUT_FMTS, SCALE_FMTS, SCALE_LAYOUTS, QuantCastDesc, SwigluQuantDesc,
+                   TkError, tk_fault_word, tk_last_error_message, tk_quant_cast_output_sizes,
+                   tk_quant_cast_plan, tk_quant_cast_plan_destroy,
                    tk_quant_cast_run, tk_quant_cast_validate, tk_status_string,
                    tk_swiglu_quant_host_pipe_create, tk_swiglu_quant_host_pipe_destroy,
                    tk_swiglu_quant_host_workspace_size, tk_swiglu_quant_launch_info,
@@ -34,7 +35,7 @@ __all__ = [
     "SwigluQuantDesc", "QuantCastDesc", "tk_swiglu_quant_validate", "tk_swiglu_quant_plan",
     "tk_swiglu_quant_plan_destroy", "tk_swiglu_quant_output_sizes", "tk_swiglu_quant_run",
     "tk_swiglu_quant_launch_info", "tk_quant_cast_validate", "tk_quant_cast_plan",
-    "tk_quant_cast_plan_destroy", "tk_quant_cast_run", "tk_status_string",
+    "tk_quant_cast_plan_destroy", "tk_quant_cast_output_sizes", "tk_quant_cast_run", "tk_status_string",
     "tk_last_error_message", "tk_fault_word",
 ]
 
@@ -44,12 +45,21 @@ def _torch():
     return torch
 
 
-def _out_shapes(T: int, hidden: int, group_size: int, scale_fmt: str, out_fmt: str):
+def _out_shapes(T: int, hidden: int, group_size: int, scale_fmt: str, out_fmt: str,
+                scale_layout: str = "row"):
+    """(codes shape, scales shape, scales dtype) for T rows. Column-major
+    scales are [G, Tp] with Tp padded to 16 bytes of scale elements; packed
+    UE8M0 scales are int32 words [G/4, Tp4], Tp4 = T padded to 4."""
     torch = _torch()
     G = 1 if group_size == 0 else hidden // group_size
     q_shape = (T, hidden if out_fmt == "e4m3" else hidden // 2)
     s_dtype = torch.float32 if scale_fmt == "fp32" else torch.uint8
-    return q_shape, (T, G), s_dtype
+    if scale_layout == "row":
+        return q_shape, (T, G), s_dtype
+    if scale_layout == "col":
+        per16 = 4 if scale_fmt == "fp32" else 16
+        return q_shape, (G, -(-T // per16) * per16), s_dtype
+    return q_shape, (G // 4, -(-T // 4) * 4), torch.int32
 
 
 def _check_cuda(t, name: str, dtype, shape=None):
@@ -69,16 +79,17 @@ class SwigluQuant:
     def __init__(self, hidden: int, group_size: int = 128, scale_fmt: str = "fp32",
                  out_fmt: str = "e4m3", topk_weights: bool = True,
                  clamp_limit: float | None = None, count_clamped: bool = False,
-                 device: int | None = None):
+                 device: int | None = None, scale_layout: str = "row"):
         torch = _torch()
         self.hidden, self.group_size = int(hidden), int(group_size)
-        self.scale_fmt, self.out_fmt = scale_fmt, out_fmt
+        self.scale_fmt, self.out_fmt, self.scale_layout = scale_fmt, out_fmt, scale_layout
         self.has_w = bool(topk_weights)
         self.clamp_limit = clamp_limit
         self.count_clamped = bool(count_clamped)
         self.desc = SwigluQuantDesc(self.hidden, self.group_size, SCALE_FMTS[scale_fmt],
                                     OUT_FMTS[out_fmt], int(self.has_w), int(clamp_limit is not None),
-                                    float(clamp_limit or 0.0), int(self.count_clamped), 0)
+                                    float(clamp_limit or 0.0), int(self.count_clamped),
+                                    SCALE_LAYOUTS[scale_layout])
         self.device = torch.cuda.current_device() if device is None else int(device)
         self.plan = tk_swiglu_quant_plan(self.desc, self.device)
 
@@ -92,7 +103,8 @@ class SwigluQuant:
             self.plan = None
 
     def output_shapes(self, T: int):
-        return _out_shapes(T, self.hidden, self.group_size, self.scale_fmt, self.out_fmt)
+        return _out_shapes(T, self.hidden, self.group_size, self.scale_fmt, self.out_fmt,
+                           self.scale_layout)
 
     def launch_info(self, T: int) -> dict:
         return tk_swiglu_quant_launch_info(self.plan, T)
@@ -185,12 +197,14 @@ class QuantCast:
     """A plan for the standalone per-token / per-block cast (tk_quant_cast_plan)."""
 
     def __init__(self, hidden: int, group_size: int = 128, scale_fmt: str = "fp32",
-                 out_fmt: str = "e4m3", in_dtype: str = "bf16", device: int | None = None):
+                 out_fmt: str = "e4m3", in_dtype: str = "bf16", device: int | None = None,
+                 scale_layout: str = "row"):
         torch = _torch()
         self.hidden, self.group_size = int(hidden), int(group_size)
         self.scale_fmt, self.out_fmt, self.in_dtype = scale_fmt, out_fmt, in_dtype
+        self.scale_layout = scale_layout
         self.desc = QuantCastDesc(self.hidden, self.group_size, SCALE_FMTS[scale_fmt],
-                                  OUT_FMTS[out_fmt], IN_DTYPES[in_dtype])
+                                  OUT_FMTS[out_fmt], IN_DTYPES[in_dtype], SCALE_LAYOUTS[scale_layout])
         self.device = torch.cuda.current_device() if device is None else int(device)
         self.plan = tk_quant_cast_plan(self.desc, self.device)
 
@@ -204,7 +218,8 @@ class QuantCast:
             self.plan = None
 
     def output_shapes(self, T: int):
-        return _out_shapes(T, self.hidden, self.group_size, self.scale_fmt, self.out_fmt)
+        return _out_shapes(T, self.hidden, self.group_size, self.scale_fmt, self.out_fmt,
+                           self.scale_layout)
 
     def __call__(self, x, *, q=None, scales=None, stream=None):
         torch = _torch()

@@ -16,6 +16,7 @@ STATUS_NAMES = {0: "TK_OK", 1: "TK_ERR_INVALID_ARG", 2: "TK_ERR_UNSUPPORTED",
 SCALE_FMTS = {"fp32": 0, "ue8m0": 1}
 OUT_FMTS = {"e4m3": 0, "e2m1": 1}
 IN_DTYPES = {"bf16": 0, "fp32": 1}
+SCALE_LAYOUTS = {"row": 0, "col": 1, "col_packed": 2}
 
 
 class TkError(RuntimeError):
@@ -29,13 +30,13 @@ class SwigluQuantDesc(ctypes.Structure):
                 ("scale_fmt", ctypes.c_int32), ("out_fmt", ctypes.c_int32),
                 ("has_topk_weights", ctypes.c_int32), ("use_clamp", ctypes.c_int32),
                 ("clamp_limit", ctypes.c_float), ("count_clamped", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("scale_layout", ctypes.c_int32)]
 
 
 class QuantCastDesc(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int64), ("group_size", ctypes.c_int32),
                 ("scale_fmt", ctypes.c_int32), ("out_fmt", ctypes.c_int32),
-                ("in_dtype", ctypes.c_int32)]
+                ("in_dtype", ctypes.c_int32), ("scale_layout", ctypes.c_int32)]
 
 
 _VP = ctypes.c_void_p
@@ -64,6 +65,8 @@ SIGNATURES = {
     "tk_quant_cast_plan": (ctypes.c_int, [ctypes.POINTER(QuantCastDesc), ctypes.c_int,
                                           ctypes.POINTER(_VP)]),
     "tk_quant_cast_plan_destroy": (ctypes.c_int, [_VP]),
+    "tk_quant_cast_output_sizes": (ctypes.c_int, [ctypes.POINTER(QuantCastDesc), ctypes.c_int64,
+                                                  _PSZ, _PSZ]),
     "tk_quant_cast_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP]),
     "tk_fault_word": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -190,6 +193,13 @@ def tk_quant_cast_plan(desc: QuantCastDesc, device: int) -> int:
 
 def tk_quant_cast_plan_destroy(plan: int) -> None:
     check(lib().tk_quant_cast_plan_destroy(plan))
+
+
+def tk_quant_cast_output_sizes(desc: QuantCastDesc, num_tokens: int) -> tuple[int, int]:
+    qb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    check(lib().tk_quant_cast_output_sizes(ctypes.byref(desc), num_tokens, ctypes.byref(qb),
+                                           ctypes.byref(sb)))
+    return qb.value, sb.value
 
 
 def tk_quant_cast_run(plan: int, num_tokens: int, x, q, scales, stream: int | None) -> None:

@@ -139,9 +139,49 @@ int grid_for(const Launch &L, int64_t T)
     return (int)(units < L.max_grid ? units : L.max_grid);
 }
 
-tk::RowShape shape_for(const Launch &L, int64_t T, int64_t hidden)
+// Padded rows per column of a column-major scale layout (elements, or
+// 32-bit words for the packed one): 16 bytes of scale elements.
+int64_t scale_ld(int32_t layout, int32_t scale_fmt, int64_t T)
 {
-    return tk::RowShape{T, (int32_t)hidden, L.tpr, L.tpg_log2, L.rpc, L.groups, L.stages, L.wpr, L.fault};
+    if (layout == TK_SCALE_COL_MAJOR) {
+        const int64_t per16 = scale_fmt == TK_SCALE_FP32 ? 4 : 16;
+        return (T + per16 - 1) / per16 * per16;
+    }
+    if (layout == TK_SCALE_COL_MAJOR_PACKED)
+        return (T + 3) / 4 * 4;
+    return 0;
+}
+
+size_t scale_bytes_for(int32_t layout, int32_t scale_fmt, int64_t T, int64_t groups)
+{
+    const size_t e = scale_fmt == TK_SCALE_FP32 ? 4 : 1;
+    if (layout == TK_SCALE_COL_MAJOR)
+        return (size_t)groups * (size_t)scale_ld(layout, scale_fmt, T) * e;
+    if (layout == TK_SCALE_COL_MAJOR_PACKED)
+        return (size_t)(groups / 4) * (size_t)scale_ld(layout, scale_fmt, T) * 4;
+    return (size_t)T * (size_t)groups * e;
+}
+
+tk::RowShape shape_for(const Launch &L, int64_t T, int64_t hidden, int32_t layout, int32_t scale_fmt)
+{
+    return tk::RowShape{T, (int32_t)hidden, L.tpr, L.tpg_log2, L.rpc, L.groups, L.stages, L.wpr, L.fault,
+                        layout, scale_ld(layout, scale_fmt, T)};
+}
+
+// The scale layout must be known, and the packed one needs UE8M0 scales and
+// a whole number of four-group words per row.
+tk_status check_scale_layout(int32_t layout, int32_t scale_fmt, int64_t hidden, int32_t group)
+{
+    if (layout != TK_SCALE_ROW_MAJOR && layout != TK_SCALE_COL_MAJOR && layout != TK_SCALE_COL_MAJOR_PACKED)
+        return fail(TK_ERR_INVALID_ARG, "unknown scale_layout %d", layout);
+    if (layout == TK_SCALE_COL_MAJOR_PACKED) {
+        const int64_t groups = group ? hidden / group : 1;
+        if (scale_fmt != TK_SCALE_UE8M0)
+            return fail(TK_ERR_UNSUPPORTED, "the packed scale layout holds UE8M0 exponents only");
+        if (groups % 4 != 0)
+            return fail(TK_ERR_UNSUPPORTED, "the packed scale layout needs a multiple of 4 groups per row");
+    }
+    return TK_OK;
 }
 
 // A clamp limit whose fp32 bits end in 16 zeros is a bf16 value: the kernels
@@ -344,9 +384,7 @@ TK_API tk_status tk_swiglu_quant_validate(const tk_swiglu_quant_desc *d)
         return fail(TK_ERR_INVALID_ARG, "clamp_limit must be finite and >= 0 (got %g)", (double)d->clamp_limit);
     if (d->count_clamped && !d->use_clamp)
         return fail(TK_ERR_INVALID_ARG, "count_clamped needs use_clamp");
-    if (d->reserved != 0)
-        return fail(TK_ERR_INVALID_ARG, "reserved must be 0");
-    return ok();
+    return check_scale_layout(d->scale_layout, d->scale_fmt, d->hidden, d->group_size);
 }
 
 TK_API tk_status tk_swiglu_quant_plan(const tk_swiglu_quant_desc *d, int device, tk_swiglu_quant_plan_t *plan)
@@ -390,7 +428,7 @@ TK_API tk_status tk_swiglu_quant_output_sizes(const tk_swiglu_quant_desc *d, int
         return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 and the outputs non-NULL");
     const int64_t groups = d->group_size ? d->hidden / d->group_size : 1;
     *q_bytes = (size_t)T * (size_t)(d->out_fmt == TK_OUT_E4M3 ? d->hidden : d->hidden / 2);
-    *scale_bytes = (size_t)T * (size_t)groups * (d->scale_fmt == TK_SCALE_FP32 ? 4u : 1u);
+    *scale_bytes = scale_bytes_for(d->scale_layout, d->scale_fmt, T, groups);
     return ok();
 }
 
@@ -417,6 +455,8 @@ TK_API tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t T, con
         return fail(TK_ERR_MISALIGNED, "q must be 16-byte aligned");
     if (d.scale_fmt == TK_SCALE_FP32 && !aligned(scales, 4))
         return fail(TK_ERR_MISALIGNED, "fp32 scales must be 4-byte aligned");
+    if (d.scale_layout != TK_SCALE_ROW_MAJOR && !aligned(scales, 16))
+        return fail(TK_ERR_MISALIGNED, "column-major scales must be 16-byte aligned");
     if (d.has_topk_weights && !aligned(topk_weights, 4))
         return fail(TK_ERR_MISALIGNED, "topk_weights must be 4-byte aligned");
     if (d.count_clamped && !aligned(clamped_count, 8))
@@ -434,7 +474,8 @@ TK_API tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t T, con
     set_packed_limit(a);
     tk::OutArgs o{static_cast<uint8_t *>(q), scales};
     const Launch &L = pick(plan->Ls, T);
-    cudaError_t e = tk::launch_swiglu(L.fn, grid_for(L, T), L.block, L.smem, a, o, shape_for(L, T, d.hidden),
+    cudaError_t e = tk::launch_swiglu(L.fn, grid_for(L, T), L.block, L.smem, a, o,
+                                      shape_for(L, T, d.hidden, d.scale_layout, d.scale_fmt),
                                       static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the fused kernel");
@@ -581,6 +622,8 @@ TK_API tk_status tk_swiglu_quant_run_host(tk_swiglu_quant_host_pipe_t pipe, int6
         return ok();
     tk_swiglu_quant_plan_t plan = pipe->plan;
     const tk_swiglu_quant_desc &d = plan->desc;
+    if (d.scale_layout != TK_SCALE_ROW_MAJOR)
+        return fail(TK_ERR_UNSUPPORTED, "the host-buffer call returns row-major scales only");
     if (!x_host || !q_host || !scales_host)
         return fail(TK_ERR_INVALID_ARG, "x_host, q_host and scales_host must be non-NULL");
     if (d.has_topk_weights && !w_host)
@@ -639,8 +682,8 @@ TK_API tk_status tk_swiglu_quant_run_host(tk_swiglu_quant_host_pipe_t pipe, int6
             set_packed_limit(a);
             tk::OutArgs o{sq, ssc};
             const Launch &L = pick(plan->Ls, rows);
-            e = tk::launch_swiglu(L.fn, grid_for(L, rows), L.block, L.smem, a, o, shape_for(L, rows, d.hidden),
-                                  pipe->s_k);
+            e = tk::launch_swiglu(L.fn, grid_for(L, rows), L.block, L.smem, a, o,
+                                  shape_for(L, rows, d.hidden, TK_SCALE_ROW_MAJOR, d.scale_fmt), pipe->s_k);
         }
         if (e == cudaSuccess)
             e = cudaEventRecord(pipe->ev_k[slot], pipe->s_k);
@@ -727,7 +770,7 @@ TK_API tk_status tk_quant_cast_validate(const tk_quant_cast_desc *d)
         return st;
     if (d->in_dtype != TK_IN_BF16 && d->in_dtype != TK_IN_FP32)
         return fail(TK_ERR_INVALID_ARG, "unknown in_dtype %d", d->in_dtype);
-    return ok();
+    return check_scale_layout(d->scale_layout, d->scale_fmt, d->hidden, d->group_size);
 }
 
 TK_API tk_status tk_quant_cast_plan(const tk_quant_cast_desc *d, int device, tk_quant_cast_plan_t *plan)
@@ -755,6 +798,20 @@ TK_API tk_status tk_quant_cast_plan(const tk_quant_cast_desc *d, int device, tk_
     return ok();
 }
 
+TK_API tk_status tk_quant_cast_output_sizes(const tk_quant_cast_desc *d, int64_t T, size_t *q_bytes,
+                                            size_t *scale_bytes_out)
+{
+    tk_status st = tk_quant_cast_validate(d);
+    if (st != TK_OK)
+        return st;
+    if (T < 0 || !q_bytes || !scale_bytes_out)
+        return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 and the outputs non-NULL");
+    const int64_t groups = d->group_size ? d->hidden / d->group_size : 1;
+    *q_bytes = (size_t)T * (size_t)(d->out_fmt == TK_OUT_E4M3 ? d->hidden : d->hidden / 2);
+    *scale_bytes_out = scale_bytes_for(d->scale_layout, d->scale_fmt, T, groups);
+    return ok();
+}
+
 TK_API tk_status tk_quant_cast_plan_destroy(tk_quant_cast_plan_t plan)
 {
     delete plan;
@@ -779,16 +836,145 @@ TK_API tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t T, const v
         return fail(TK_ERR_MISALIGNED, "q must be 16-byte aligned");
     if (d.scale_fmt == TK_SCALE_FP32 && !aligned(scales, 4))
         return fail(TK_ERR_MISALIGNED, "fp32 scales must be 4-byte aligned");
+    if (d.scale_layout != TK_SCALE_ROW_MAJOR && !aligned(scales, 16))
+        return fail(TK_ERR_MISALIGNED, "column-major scales must be 16-byte aligned");
     tk_status st = check_current_device(plan->device);
     if (st != TK_OK)
         return st;
     tk::CastArgs a{x, (int32_t)d.hidden};
     tk::OutArgs o{static_cast<uint8_t *>(q), scales};
     const Launch &L = pick(plan->Ls, T);
-    cudaError_t e = tk::launch_cast(L.fn, grid_for(L, T), L.block, L.smem, a, o, shape_for(L, T, d.hidden),
+    cudaError_t e = tk::launch_cast(L.fn, grid_for(L, T), L.block, L.smem, a, o,
+                                    shape_for(L, T, d.hidden, d.scale_layout, d.scale_fmt),
                                     static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the cast kernel");
+    return ok();
+}
+
+// ------------------------------------------------------- weighted top-k combine
+
+struct tk_moe_reduce_plan_s {
+    tk_moe_reduce_desc desc;
+    int device;
+    const void *fn;
+    int block, rpc, tpr, max_grid;
+    unsigned *fault;
+};
+
+TK_API tk_status tk_moe_reduce_validate(const tk_moe_reduce_desc *d)
+{
+    if (!d)
+        return fail(TK_ERR_INVALID_ARG, "desc is NULL");
+    if (d->hidden <= 0 || d->topk <= 0)
+        return fail(TK_ERR_INVALID_ARG, "hidden and topk must be positive");
+    if (d->hidden % 16 != 0 || d->hidden > 8192)
+        return fail(TK_ERR_UNSUPPORTED, "hidden must be a multiple of 16 in [16, 8192] (got %lld)",
+                    (long long)d->hidden);
+    if (d->topk > 64)
+        return fail(TK_ERR_UNSUPPORTED, "topk must be at most 64 (got %d)", d->topk);
+    if (d->in_fmt != TK_REDUCE_IN_BF16 && d->in_fmt != TK_REDUCE_IN_E4M3)
+        return fail(TK_ERR_INVALID_ARG, "unknown in_fmt %d", d->in_fmt);
+    if (d->in_fmt == TK_REDUCE_IN_E4M3 && d->hidden % 128 != 0)
+        return fail(TK_ERR_UNSUPPORTED, "E4M3 rows need hidden to be a multiple of 128");
+    return ok();
+}
+
+TK_API tk_status tk_moe_reduce_plan(const tk_moe_reduce_desc *d, int device, tk_moe_reduce_plan_t *plan)
+{
+    if (!plan)
+        return fail(TK_ERR_INVALID_ARG, "plan output pointer is NULL");
+    *plan = nullptr;
+    tk_status st = tk_moe_reduce_validate(d);
+    if (st != TK_OK)
+        return st;
+    int count = 0;
+    cudaError_t e = cudaGetDeviceCount(&count);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDeviceCount");
+    if (device < 0 || device >= count)
+        return fail(TK_ERR_INVALID_ARG, "device %d out of range (%d devices)", device, count);
+    DeviceScope scope(device);
+    if (scope.err != cudaSuccess)
+        return cuda_fail(scope.err, "cudaSetDevice");
+    tk_moe_reduce_plan_s p{};
+    p.desc = *d;
+    p.device = device;
+    p.fn = tk::moe_reduce_kernel_fn(d->in_fmt);
+    p.tpr = (int)(d->hidden / tk::kEPT);
+    p.rpc = p.tpr >= 256 ? 1 : 256 / p.tpr;
+    p.block = ((p.tpr * p.rpc + 31) / 32) * 32;   // <= 512 for hidden <= 8192
+    int num_sms = 0, occ = 0;
+    void *fault = nullptr;
+    e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, p.fn, p.block, 0);
+    if (e == cudaSuccess)
+        e = cudaGetSymbolAddress(&fault, g_tk_fault_word);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "querying the device");
+    if (occ < 1)
+        return fail(TK_ERR_UNSUPPORTED, "kernel cannot be resident with %d threads per CTA", p.block);
+    p.max_grid = occ * num_sms;
+    p.fault = static_cast<unsigned *>(fault);
+    auto *h = new (std::nothrow) tk_moe_reduce_plan_s(p);
+    if (!h)
+        return fail(TK_ERR_INVALID_ARG, "out of host memory");
+    *plan = h;
+    return ok();
+}
+
+TK_API tk_status tk_moe_reduce_plan_destroy(tk_moe_reduce_plan_t plan)
+{
+    delete plan;
+    return ok();
+}
+
+TK_API tk_status tk_moe_reduce_run(tk_moe_reduce_plan_t plan, int64_t T, const void *y, const float *y_scale,
+                                   int64_t num_rows, const int32_t *pos, const float *w, float gs, void *out,
+                                   void *stream)
+{
+    if (!plan)
+        return fail(TK_ERR_INVALID_ARG, "plan is NULL");
+    if (T < 0 || num_rows < 0)
+        return fail(TK_ERR_INVALID_ARG, "num_tokens and num_rows must be >= 0");
+    if (T == 0)
+        return ok();
+    const tk_moe_reduce_desc &d = plan->desc;
+    const bool fp8 = d.in_fmt == TK_REDUCE_IN_E4M3;
+    if (!pos || !w || !out || (num_rows > 0 && !y) || (fp8 && num_rows > 0 && !y_scale))
+        return fail(TK_ERR_INVALID_ARG, "y, y_scale (E4M3), token_topk_to_pos, topk_weights and out "
+                                        "must be non-NULL");
+    if (!std::isfinite(gs))
+        return fail(TK_ERR_INVALID_ARG, "global_scale must be finite");
+    if (y && !aligned(y, fp8 ? 16 : 32))
+        return fail(TK_ERR_MISALIGNED, "y must be %d-byte aligned", fp8 ? 16 : 32);
+    if (!aligned(out, 16))
+        return fail(TK_ERR_MISALIGNED, "out must be 16-byte aligned");
+    if (!aligned(pos, 4) || !aligned(w, 4) || (fp8 && y_scale && !aligned(y_scale, 4)))
+        return fail(TK_ERR_MISALIGNED, "token_topk_to_pos, topk_weights and y_scale must be 4-byte aligned");
+    tk_status st = check_current_device(plan->device);
+    if (st != TK_OK)
+        return st;
+    tk::ReduceArgs a{};
+    a.y = y;
+    a.y_scale = fp8 ? y_scale : nullptr;
+    a.R = num_rows;
+    a.H = (int32_t)d.hidden;
+    a.K = d.topk;
+    a.pos = pos;
+    a.w = w;
+    a.T = T;
+    a.gs = gs;
+    a.out = out;
+    a.tpr = plan->tpr;
+    a.rpc = plan->rpc;
+    a.fault = plan->fault;
+    const int64_t ntb = (T + plan->rpc - 1) / plan->rpc;
+    const int grid = (int)(ntb < plan->max_grid ? ntb : plan->max_grid);
+    cudaError_t e = tk::launch_moe_reduce(plan->fn, grid, plan->block, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launch of the combine kernel");
     return ok();
 }
 

@@ -40,6 +40,27 @@ inline cudaError_t launch_pdl(const void *fn, int grid, int block, size_t smem, 
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+// The weighted top-k combine.
+enum { kReduceInBf16 = 0, kReduceInE4M3 = 1 };
+
+struct ReduceArgs {
+    const void *y;            // [R, H] bf16, or E4M3 codes
+    const float *y_scale;     // [R, H / 128] fp32 (E4M3 rows) or null
+    int64_t R;                // rows of y
+    int32_t H;
+    int32_t K;                // slots per token
+    const int32_t *pos;       // [T, K]: row of y, or -1 for an empty slot
+    const float *w;           // [T, K]
+    int64_t T;
+    float gs;                 // global scale
+    void *out;                // [T, H] bf16
+    int32_t tpr, rpc;         // threads per token row (H / 16), tokens per CTA step
+    unsigned *fault;          // bit 1: a position outside [-1, R) was met (and skipped)
+};
+
+const void *moe_reduce_kernel_fn(int in_fmt);
+cudaError_t launch_moe_reduce(const void *fn, int grid, int block, const ReduceArgs &a, cudaStream_t stream);
+
 // Bytes of one warp-ring slot of the stream kernels.
 constexpr int kSwigluSlotBytes = SwigluSrc<false>::kSpans * SwigluSrc<false>::kSpanBytes;
 constexpr int kCastBf16SlotBytes = CastBf16Src::kSpans * CastBf16Src::kSpanBytes;

@@ -64,7 +64,20 @@ struct RowShape {
     int32_t stages;     // warp_stream_kernel: slots per warp ring (>= 2)
     int32_t wpr;        // warp_stream_kernel: warps (512-column slices) per row
     unsigned *fault;    // warp_stream_kernel: device word, bit 0 set if a wait gave up
+    int32_t scale_layout;  // 0 row-major [T, G]; 1 column-major [G, ld]; 2 packed UE8M0 words [G/4, ld]
+    int64_t scale_ld;      // column-major layouts: padded rows per column (elements or words)
 };
+
+// Element index of the scale of group j of row t (layouts 0 and 1), or byte
+// index of its exponent (layout 2, UE8M0).
+__device__ __forceinline__ int64_t scale_index(const RowShape &sh, int64_t t, int j)
+{
+    if (sh.scale_layout == 0)
+        return t * sh.groups + j;
+    if (sh.scale_layout == 1)
+        return (int64_t)j * sh.scale_ld + t;
+    return (((int64_t)(j >> 2) * sh.scale_ld + t) << 2) + (j & 3);
+}
 
 struct OutArgs {
     uint8_t *q;
@@ -307,22 +320,48 @@ __device__ __forceinline__ int ue8m0_exponent(float amax)
     return k < -127 ? -127 : (k > 127 ? 127 : k);
 }
 
-// Two fp32 -> two codes, RNE with saturation to the largest finite value.
-// The first operand of the conversion lands in the upper half of the result,
-// so `lo` (the lower column) is passed second.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
-{
-    uint16_t h;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
-    return (uint32_t)h;
-}
-
-__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi)
+// fp32 -> codes, round-to-nearest-even with saturation to the largest
+// finite value. The first source of a packed conversion lands in the upper
+// half of its result, so the lower column is passed second.
+// four fp32 -> four E4M3 codes in one word, the first column in the low byte
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float d)
 {
     uint32_t r;
-    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
-        : "=r"(r) : "f"(hi), "f"(lo));
+    asm("{\n\t.reg .b16 lo, hi;\n\tcvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\tmov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
     return r;
+}
+
+// eight fp32 -> eight E2M1 codes in one word, column 2k in the low nibble of
+// byte k
+__device__ __forceinline__ uint32_t cvt_e2m1x8(uint64_t v0, uint64_t v1, uint64_t v2, uint64_t v3)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .f32 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+        "mov.b64 {l0, h0}, %1;\n\tmov.b64 {l1, h1}, %2;\n\t"
+        "mov.b64 {l2, h2}, %3;\n\tmov.b64 {l3, h3}, %4;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, h0, l0;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, h1, l1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, h2, l2;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, h3, l3;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r) : "l"(v0), "l"(v1), "l"(v2), "l"(v3));
+    return r;
+}
+
+// Absmax of a scale group spread over the power-of-two lane group that
+// tpg_mask + 1 lanes form: one shuffle for groups of one or two lanes, else
+// five with offsets past the group masked to 0 (a shuffle with oneself). The
+// branch is uniform across the kernel.
+__device__ __forceinline__ float group_max(float v, int tpg_mask)
+{
+    if (tpg_mask <= 1)
+        return fmaxf(v, __shfl_xor_sync(kFull, v, tpg_mask));
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1)
+        v = fmaxf(v, __shfl_xor_sync(kFull, v, off & tpg_mask));
+    return v;
 }
 
 // ------------------------------------------------------- quantize and store
@@ -344,7 +383,7 @@ __device__ __forceinline__ void quantize_store(const uint64_t (&ny)[kEPT / 2], f
         for (int i = 0; i < kEPT / 2; ++i)
             v[i] = mul2(ny[i], ninv);
         if (write_scale)
-            static_cast<uint8_t *>(o.scales)[row * sh.groups + group_idx] = (uint8_t)(k + 127);
+            static_cast<uint8_t *>(o.scales)[scale_index(sh, row, group_idx)] = (uint8_t)(k + 127);
     } else {
         // amax >= 2^-64 keeps s >= 2^-73 and every remainder above the
         // subnormal range, so both divisions can take the Markstein step;
@@ -367,24 +406,18 @@ __device__ __forceinline__ void quantize_store(const uint64_t (&ny)[kEPT / 2], f
                 v[i] = pk(__fdiv_rn(-plo(ny[i]), s), __fdiv_rn(-phi(ny[i]), s));
         }
         if (write_scale)
-            static_cast<float *>(o.scales)[row * sh.groups + group_idx] = s;
+            static_cast<float *>(o.scales)[scale_index(sh, row, group_idx)] = s;
     }
     if (OUT == kOutE4M3) {
         uint32_t w[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            w[j] = cvt_e4m3x2(plo(v[2 * j]), phi(v[2 * j])) |
-                   (cvt_e4m3x2(plo(v[2 * j + 1]), phi(v[2 * j + 1])) << 16);
+            w[j] = cvt_e4m3x4(plo(v[2 * j]), phi(v[2 * j]), plo(v[2 * j + 1]), phi(v[2 * j + 1]));
         st_stream_128(o.q + row * (int64_t)sh.H + col0, w[0], w[1], w[2], w[3]);
     } else {
-        uint32_t w[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-            w[j] = cvt_e2m1x2(plo(v[4 * j]), phi(v[4 * j])) |
-                   (cvt_e2m1x2(plo(v[4 * j + 1]), phi(v[4 * j + 1])) << 8) |
-                   (cvt_e2m1x2(plo(v[4 * j + 2]), phi(v[4 * j + 2])) << 16) |
-                   (cvt_e2m1x2(plo(v[4 * j + 3]), phi(v[4 * j + 3])) << 24);
-        st_stream_64(o.q + row * (int64_t)(sh.H / 2) + col0 / 2, w[0], w[1]);
+        const uint32_t w0 = cvt_e2m1x8(v[0], v[1], v[2], v[3]);
+        const uint32_t w1 = cvt_e2m1x8(v[4], v[5], v[6], v[7]);
+        st_stream_64(o.q + row * (int64_t)(sh.H / 2) + col0 / 2, w0, w1);
     }
 }
 
@@ -443,10 +476,7 @@ row_quant_kernel(typename Src::Args a, OutArgs o, RowShape sh)
             for (int w = 0; w < nwarps; ++w)
                 amax = fmaxf(amax, buf[w]);
         } else {
-            // five shuffles always; offsets past the group mask to 0 (no-op)
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off & tpg_mask));
+            amax = group_max(amax, tpg_mask);
         }
         if (ok)
             quantize_store<OUT, SCALE>(ny, amax, row, col0, group_idx, first_of_group, sh, o);
@@ -576,9 +606,7 @@ warp_stream_kernel(typename Src::Args a, OutArgs o, RowShape sh)
         uint64_t ny[kEPT / 2];
         float amax = 0.0f;
         src.produce(a, regs, true, ny, amax);
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off & tpg_mask));
+        amax = group_max(amax, tpg_mask);
         const int lr = (cbase >> 4) + lane;
         quantize_store<OUT, SCALE>(ny, amax, row, cbase + lane * kEPT, lr >> sh.tpg_log2,
                                    (lr & tpg_mask) == 0, sh, o);

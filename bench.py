@@ -54,6 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle sample for cpu_baseline")
+    p.add_argument("--scale-layout", choices=["row", "col", "col_packed"], default="row",
+                   help="scale layout of the fused op (the host-buffer e2e leg needs row)")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--e2e-chunk-rows", type=int, default=2048)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -293,11 +295,11 @@ def run_ours(args, dist: Dist):
     wl = wls.ALL_WORKLOADS[args.workload]
     T, H = wl.T, wl.H
     if wl.op == "cast":
-        op = tk.QuantCast(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.in_dtype, dev)
+        op = tk.QuantCast(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.in_dtype, dev, args.scale_layout)
         op.count_clamped = False
     else:
         op = tk.SwigluQuant(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.w_dist is not None, wl.clamp,
-                            wl.clamp is not None, dev)
+                            wl.clamp is not None, dev, args.scale_layout)
     algo = wl.algo_bytes()
     per_set = algo
     n_sets = max(2, -(-3 * L2_BYTES // per_set) + 1)   # sets beyond the current one hold > 3x L2
@@ -368,7 +370,7 @@ def run_ours(args, dist: Dist):
     peaks = measured_peaks()
 
     e2e = None
-    if not args.no_e2e and wl.op == "swiglu":
+    if not args.no_e2e and wl.op == "swiglu" and args.scale_layout == "row":
         e2e = measure_e2e(op, wl, x0, w0, dev, args, dist)
 
     cpu = None
@@ -385,7 +387,7 @@ def run_ours(args, dist: Dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {**config_of(wl, args.gpus),
+        "config": {**config_of(wl, args.gpus), "scale_layout": args.scale_layout,
                    "l2": "inputs larger than L2: %d rotating input/output sets, %.0f MB" % (
                        n_sets, n_sets * per_set / 1e6)},
         "hbm_gbs": achieved,

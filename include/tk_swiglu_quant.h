@@ -69,6 +69,22 @@ typedef enum tk_in_dtype {
     TK_IN_FP32 = 1
 } tk_in_dtype;
 
+/* Where the scale of group j of row t goes ("TMA-aligned column-major scale
+ * factors" and "packed" UE8M0 of the quantization section of "TileLang +
+ * TileKernels", zhichai.net/topic/177618740; the exact layouts are this
+ * library's reading). G = groups per row. */
+typedef enum tk_scale_layout {
+    TK_SCALE_ROW_MAJOR = 0,        /* [T, G]: element t*G + j */
+    TK_SCALE_COL_MAJOR = 1,        /* [G, Tp]: element j*Tp + t, Tp = T rounded up to a multiple of
+                                      16 bytes of scale elements (4 fp32 or 16 UE8M0), so every
+                                      column starts on a 16-byte boundary; rows t >= T of the
+                                      padding are not written */
+    TK_SCALE_COL_MAJOR_PACKED = 2  /* UE8M0 only, G % 4 == 0: 32-bit words [G/4, Tp4], word
+                                      m*Tp4 + t holds the exponents of groups 4m..4m+3 of row t,
+                                      group 4m in the low byte; Tp4 = T rounded up to 4; padding
+                                      words are not written */
+} tk_scale_layout;
+
 /* ------------------------------------------------------------------------
  * Fused SwiGLU + top-k weight + cast
  * ---------------------------------------------------------------------- */
@@ -82,7 +98,7 @@ typedef struct tk_swiglu_quant_desc {
     int32_t use_clamp;         /* 1: gate <= clamp_limit, up in [-clamp_limit, clamp_limit] */
     float clamp_limit;         /* finite, >= 0; read only when use_clamp */
     int32_t count_clamped;     /* 1: run() ADDS the clamp counts into a device int64[2]; needs use_clamp */
-    int32_t reserved;          /* must be 0 */
+    int32_t scale_layout;      /* tk_scale_layout */
 } tk_swiglu_quant_desc;
 
 typedef struct tk_swiglu_quant_plan_s *tk_swiglu_quant_plan_t;
@@ -101,8 +117,9 @@ tk_status tk_swiglu_quant_plan(const tk_swiglu_quant_desc *desc, int device,
 tk_status tk_swiglu_quant_plan_destroy(tk_swiglu_quant_plan_t plan);
 
 /* Bytes of the code and scale outputs for num_tokens rows (host only):
- * q: T*H (E4M3) or T*H/2 (E2M1); scales: T*G*4 (fp32) or T*G (UE8M0), with
- * G = H / group_size (1 when group_size == 0). */
+ * q: T*H (E4M3) or T*H/2 (E2M1); scales, with e = 4 (fp32) or 1 (UE8M0) and
+ * G = H / group_size (1 when group_size == 0): T*G*e row-major, G*Tp*e
+ * column-major, (G/4)*Tp4*4 packed (see tk_scale_layout). */
 tk_status tk_swiglu_quant_output_sizes(const tk_swiglu_quant_desc *desc, int64_t num_tokens,
                                        size_t *q_bytes, size_t *scale_bytes);
 
@@ -110,7 +127,8 @@ tk_status tk_swiglu_quant_output_sizes(const tk_swiglu_quant_desc *desc, int64_t
  *   x             [T, 2H] bf16, row-major, gate half first; 32-byte aligned
  *   topk_weights  [T] fp32, 4-byte aligned; required iff has_topk_weights, else ignored
  *   q             codes, [T, H] or [T, H/2] bytes, row-major; 16-byte aligned
- *   scales        [T, G] fp32 (4-byte aligned) or uint8, row-major
+ *   scales        fp32 or uint8 in the plan's scale layout; 4-byte aligned
+ *                 (fp32, row-major), 16-byte aligned (column-major layouts)
  *   clamped_count device int64[2], 8-byte aligned: [0] += gate values above
  *                 the limit, [1] += up values outside [-L, L]; required iff
  *                 count_clamped, else ignored. The caller zeroes it.
@@ -162,7 +180,8 @@ tk_status tk_swiglu_quant_host_workspace_size(tk_swiglu_quant_host_pipe_t pipe, 
  * synchronising: the host outputs are complete once `stream` has reached
  * this point (e.g. cudaStreamSynchronize).
  *   x_host, topk_weights_host    host inputs as in tk_swiglu_quant_run
- *   q_host, scales_host          host outputs as in tk_swiglu_quant_run
+ *   q_host, scales_host          host outputs as in tk_swiglu_quant_run; the
+ *                                plan's scales must be row-major
  *   clamped_count_host           host int64[2], ADDED to like the device
  *                                counter (copied in, added to, copied back);
  *                                required iff count_clamped
@@ -228,6 +247,7 @@ typedef struct tk_quant_cast_desc {
     int32_t scale_fmt;   /* tk_scale_fmt */
     int32_t out_fmt;     /* tk_out_fmt */
     int32_t in_dtype;    /* tk_in_dtype */
+    int32_t scale_layout;  /* tk_scale_layout */
 } tk_quant_cast_desc;
 
 typedef struct tk_quant_cast_plan_s *tk_quant_cast_plan_t;
@@ -236,10 +256,63 @@ tk_status tk_quant_cast_validate(const tk_quant_cast_desc *desc);
 tk_status tk_quant_cast_plan(const tk_quant_cast_desc *desc, int device, tk_quant_cast_plan_t *plan);
 tk_status tk_quant_cast_plan_destroy(tk_quant_cast_plan_t plan);
 
+/* Bytes of the cast's outputs, as tk_swiglu_quant_output_sizes (host only). */
+tk_status tk_quant_cast_output_sizes(const tk_quant_cast_desc *desc, int64_t num_tokens,
+                                     size_t *q_bytes, size_t *scale_bytes);
+
 /* Enqueue the cast. x [T, H] row-major, 32-byte aligned; q, scales as in
  * tk_swiglu_quant_run. num_tokens == 0 is a no-op. */
 tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t num_tokens, const void *x,
                             void *q, void *scales, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Weighted top-k combine after the expert GEMMs
+ *
+ * "TileKernels从入门到精通" (zhichai.net/topic/177618752), chapter 3,
+ * "结算中心的减法工程" and "动态寻址": the expert outputs of each token are
+ * gathered through token_topk_to_pos and combined with the routing weights,
+ * their quantization factors and a global scale in registers, reading every
+ * expert row once and writing every output once:
+ *
+ *     out[t, :] = gs * sum_{k < K, pos[t,k] >= 0} w[t,k] * deq(y[pos[t,k], :])
+ *
+ * with deq(y) = y for bf16 rows, or decode(code) * y_scale[row, col / 128] for
+ * E4M3 rows. The sum is accumulated in fp32 in k order and rounded once to
+ * bf16 (round to nearest even).
+ * ---------------------------------------------------------------------- */
+
+typedef enum tk_reduce_in_fmt {
+    TK_REDUCE_IN_BF16 = 0,   /* y [R, H] bf16 */
+    TK_REDUCE_IN_E4M3 = 1    /* y [R, H] E4M3 codes with y_scale [R, H/128] fp32 */
+} tk_reduce_in_fmt;
+
+typedef struct tk_moe_reduce_desc {
+    int64_t hidden;   /* H: 16 <= H <= 8192, H % 16 == 0 (H % 128 == 0 for E4M3 rows) */
+    int32_t topk;     /* K: 1 <= K <= 64 slots per token */
+    int32_t in_fmt;   /* tk_reduce_in_fmt */
+} tk_moe_reduce_desc;
+
+typedef struct tk_moe_reduce_plan_s *tk_moe_reduce_plan_t;
+
+tk_status tk_moe_reduce_validate(const tk_moe_reduce_desc *desc);
+tk_status tk_moe_reduce_plan(const tk_moe_reduce_desc *desc, int device, tk_moe_reduce_plan_t *plan);
+tk_status tk_moe_reduce_plan_destroy(tk_moe_reduce_plan_t plan);
+
+/* Enqueue the combine of num_tokens tokens.
+ *   y                 [num_rows, H] expert rows, row-major: bf16 (32-byte aligned)
+ *                     or E4M3 codes (16-byte aligned)
+ *   y_scale           [num_rows, H/128] fp32 for E4M3 rows (4-byte aligned); else ignored
+ *   token_topk_to_pos [T, K] int32, row-major: the row of y holding token t's
+ *                     k-th expert output, or -1 for an empty slot. A value
+ *                     outside [-1, num_rows) is not read through: the slot is
+ *                     skipped and bit 1 of the device fault word is set.
+ *   topk_weights      [T, K] fp32
+ *   global_scale      gs
+ *   out               [T, H] bf16, 16-byte aligned
+ * num_tokens == 0 is a no-op. Stream-ordered and asynchronous. */
+tk_status tk_moe_reduce_run(tk_moe_reduce_plan_t plan, int64_t num_tokens, const void *y,
+                            const float *y_scale, int64_t num_rows, const int32_t *token_topk_to_pos,
+                            const float *topk_weights, float global_scale, void *out, void *stream);
 
 /* ------------------------------------------------------------------------
  * Diagnostics
@@ -248,7 +321,8 @@ tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t num_tokens, const
 /* Read, and if `clear` is non-zero reset, the fault word of `device`. Bit 0
  * is set by a kernel that gave up waiting for one of its own asynchronous
  * copies (a wait over a second long, which no correct run reaches) and
- * returned early, leaving that launch's outputs incomplete. The word is
+ * returned early, leaving that launch's outputs incomplete. Bit 1 is set by
+ * the top-k combine when a position outside [-1, num_rows) was skipped. The word is
  * shared by every call on the device; the read is ordered after all work
  * already submitted to the device (it synchronises with it). */
 tk_status tk_fault_word(int device, uint32_t *value, int clear);

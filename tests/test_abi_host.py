@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol():
 
 def D(**kw):
     base = dict(hidden=2048, group_size=128, scale_fmt=0, out_fmt=0, has_topk_weights=1,
-                use_clamp=0, clamp_limit=0.0, count_clamped=0, reserved=0)
+                use_clamp=0, clamp_limit=0.0, count_clamped=0, scale_layout=0)
     base.update(kw)
     return tk.SwigluQuantDesc(**base)
 
@@ -63,7 +63,12 @@ def D(**kw):
     (dict(use_clamp=1, clamp_limit=-1.0), 1),
     (dict(use_clamp=1, clamp_limit=7.0, count_clamped=1), 0),
     (dict(count_clamped=1), 1),
-    (dict(reserved=3), 1),
+    (dict(scale_layout=3), 1),
+    (dict(scale_layout=1), 0),
+    (dict(scale_layout=2, scale_fmt=1), 0),
+    (dict(scale_layout=2, scale_fmt=0), 2),
+    (dict(scale_layout=2, scale_fmt=1, group_size=512), 0),
+    (dict(scale_layout=2, scale_fmt=1, group_size=0), 2),
 ])
 def test_validate(kw, status):
     assert tk.tk_swiglu_quant_validate(D(**kw)) == status
@@ -73,10 +78,25 @@ def test_validate(kw, status):
 
 def test_cast_validate():
     C = tk.QuantCastDesc
-    assert tk.tk_quant_cast_validate(C(4096, 128, 0, 0, 0)) == 0
-    assert tk.tk_quant_cast_validate(C(4096, 0, 1, 1, 1)) == 0
-    assert tk.tk_quant_cast_validate(C(4096, 128, 0, 0, 2)) == 1
-    assert tk.tk_quant_cast_validate(C(100, 0, 0, 0, 0)) == 2
+    assert tk.tk_quant_cast_validate(C(4096, 128, 0, 0, 0, 0)) == 0
+    assert tk.tk_quant_cast_validate(C(4096, 0, 1, 1, 1, 0)) == 0
+    assert tk.tk_quant_cast_validate(C(4096, 128, 0, 0, 2, 0)) == 1
+    assert tk.tk_quant_cast_validate(C(100, 0, 0, 0, 0, 0)) == 2
+    assert tk.tk_quant_cast_validate(C(4096, 128, 1, 0, 0, 2)) == 0
+    assert tk.tk_quant_cast_validate(C(4096, 128, 0, 0, 0, 2)) == 2
+
+
+def test_output_sizes_of_scale_layouts():
+    # column-major: columns padded to 16 bytes of scale elements
+    assert tk.tk_swiglu_quant_output_sizes(D(scale_layout=1), 1001) == (1001 * 2048, 16 * 1004 * 4)
+    assert tk.tk_swiglu_quant_output_sizes(D(scale_layout=1, scale_fmt=1), 1001) == (
+        1001 * 2048, 16 * 1008)
+    # packed UE8M0: 4 exponents per int32 word, rows padded to 4
+    assert tk.tk_swiglu_quant_output_sizes(D(scale_layout=2, scale_fmt=1), 1001) == (
+        1001 * 2048, 4 * 1004 * 4)
+    C = tk.QuantCastDesc
+    assert tk.tk_quant_cast_output_sizes(C(4096, 32, 1, 1, 0, 2), 7) == (7 * 2048, 32 * 8 * 4)
+    assert tk.tk_quant_cast_output_sizes(C(4096, 0, 0, 0, 1, 0), 7) == (7 * 4096, 7 * 4)
 
 
 def test_output_sizes():

@@ -419,3 +419,55 @@ def test_stream_ring_depths(stages, monkeypatch):
 def test_fault_word_clear_after_runs():
     torch.cuda.synchronize()
     assert tk.tk_fault_word(torch.cuda.current_device()) == 0
+
+
+# ------------------------------------------------------------ scale layouts
+
+@pytest.mark.parametrize("kernel", ["rows", "stream"])
+@pytest.mark.parametrize("layout,scale_fmt,group,out_fmt", [
+    ("col", "fp32", 128, "e4m3"), ("col", "ue8m0", 128, "e4m3"), ("col_packed", "ue8m0", 128, "e4m3"),
+    ("col_packed", "ue8m0", 32, "e2m1"), ("col", "fp32", 0, "e4m3")])
+@pytest.mark.parametrize("T", [1, 29, 1001])
+def test_scale_layouts(kernel, layout, scale_fmt, group, out_fmt, T, monkeypatch):
+    """Scales written column-major (padded to 16 bytes per column) or as
+    packed UE8M0 words match the oracle's row-major scales moved by the
+    oracle's layout function; padding is left untouched and the codes are
+    those of the row-major run."""
+    monkeypatch.setenv("TK_KERNEL", kernel)
+    H = 2048
+    wl = wls.WORKLOADS["moe_T32768_H2048_g128_ue8m0_clamp7"].with_rows(T)
+    x, w = wls.make_inputs(wl, "cpu")
+    fused = tk.SwigluQuant(H, group, scale_fmt, out_fmt, True, 7.0, False, scale_layout=layout)
+    flat = tk.SwigluQuant(H, group, scale_fmt, out_fmt, True, 7.0, False)
+    q_ref, s_ref = _run(flat, x.cuda(), w.cuda())
+    q_shape, s_shape, s_dtype = fused.output_shapes(T)
+    sentinel = 0xA7
+    s_buf = torch.full(s_shape, 0, dtype=s_dtype, device="cuda")
+    s_buf.view(torch.uint8).fill_(sentinel)
+    q, s = fused(x.cuda(), w.cuda(), scales=s_buf)
+    torch.cuda.synchronize()
+    assert torch.equal(q, q_ref)
+    want = oracle.scales_to_layout(s_ref.cpu().numpy(), scale_fmt, layout, fill=sentinel)
+    got = s.cpu().contiguous().view(torch.uint8).numpy().reshape(-1)
+    assert np.array_equal(got, want)
+    # and the same layouts from the standalone cast (fp32 input, bit-exact)
+    y = torch.randn(T, H) * 3
+    cast = tk.QuantCast(H, group, scale_fmt, out_fmt, "fp32", scale_layout=layout)
+    cs_buf = torch.full(s_shape, 0, dtype=s_dtype, device="cuda")
+    cs_buf.view(torch.uint8).fill_(sentinel)
+    cq, cs = cast(y.cuda(), scales=cs_buf)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quant_rows_f32(y.numpy(), group, scale_fmt, out_fmt)
+    assert np.array_equal(cq.cpu().numpy(), rq)
+    want = oracle.scales_to_layout(rs, scale_fmt, layout, fill=sentinel)
+    got = cs.cpu().contiguous().view(torch.uint8).numpy().reshape(-1)
+    assert np.array_equal(got, want)
+
+
+def test_host_pipe_refuses_column_major_scales():
+    op = tk.SwigluQuant(2048, 128, "fp32", "e4m3", True, scale_layout="col")
+    with pytest.raises(tk.TkError) as e:
+        pipe = tk.HostPipe(op, 64)
+        pipe(torch.zeros(8, 4096, dtype=torch.bfloat16), torch.ones(8),
+             q=torch.empty(8, 2048, dtype=torch.uint8), scales=torch.empty(op.output_shapes(8)[1]))
+    assert e.value.status == 2
