@@ -17,7 +17,9 @@ from __future__ import annotations
 import threading
 
 from . import _abi
-from ._abi import (IN_DTYPES, OUT_FMTS, SCALE_FMTS, SCALE_LAYOUTS, QuantCastDesc, SwigluQuantDesc,
+from ._abi import (IN_DTYPES, OUT_FMTS, REDUCE_IN_FMTS, SCALE_FMTS, SCALE_LAYOUTS, MoeReduceDesc,
+                   QuantCastDesc, SwigluQuantDesc, tk_moe_reduce_plan, tk_moe_reduce_plan_destroy,
+                   tk_moe_reduce_run, tk_moe_reduce_validate,
                    TkError, tk_fault_word, tk_last_error_message, tk_quant_cast_output_sizes,
                    tk_quant_cast_plan, tk_quant_cast_plan_destroy,
                    tk_quant_cast_run, tk_quant_cast_validate, tk_status_string,
@@ -28,7 +30,9 @@ from ._abi import (IN_DTYPES, OUT_FMTS, SCALE_FMTS, SCALE_LAYOUTS, QuantCastDesc
                    tk_swiglu_quant_validate)
 
 __all__ = [
-    "SwigluQuant", "HostPipe", "QuantCast", "swiglu_quant", "quant_cast", "TkError",
+    "SwigluQuant", "HostPipe", "QuantCast", "MoeReduce", "swiglu_quant", "quant_cast", "TkError",
+    "MoeReduceDesc", "tk_moe_reduce_validate", "tk_moe_reduce_plan", "tk_moe_reduce_plan_destroy",
+    "tk_moe_reduce_run",
     "tk_swiglu_quant_host_pipe_create", "tk_swiglu_quant_host_pipe_destroy",
     "tk_swiglu_quant_host_workspace_size", "tk_swiglu_quant_run_host",
     "tk_swiglu_quant_run_host_static",
@@ -238,6 +242,52 @@ class QuantCast:
         with torch.cuda.device(x.device):
             tk_quant_cast_run(self.plan, T, x, q, scales, stream.cuda_stream)
         return q, scales
+
+
+class MoeReduce:
+    """A plan for the weighted top-k combine (tk_moe_reduce_plan)."""
+
+    def __init__(self, hidden: int, topk: int, in_fmt: str = "bf16", device: int | None = None):
+        torch = _torch()
+        self.hidden, self.topk, self.in_fmt = int(hidden), int(topk), in_fmt
+        self.desc = MoeReduceDesc(self.hidden, self.topk, REDUCE_IN_FMTS[in_fmt])
+        self.device = torch.cuda.current_device() if device is None else int(device)
+        self.plan = tk_moe_reduce_plan(self.desc, self.device)
+
+    def __del__(self):
+        plan = getattr(self, "plan", None)
+        if plan:
+            try:
+                tk_moe_reduce_plan_destroy(plan)
+            except Exception:
+                pass
+            self.plan = None
+
+    def __call__(self, y, token_topk_to_pos, topk_weights, global_scale: float = 1.0, *,
+                 y_scale=None, out=None, stream=None):
+        """y: [R, H] bf16 (or uint8 E4M3 codes with y_scale [R, H/128] fp32);
+        token_topk_to_pos: [T, K] int32 (-1: empty); topk_weights: [T, K] fp32.
+        Returns out [T, H] bf16."""
+        torch = _torch()
+        T = token_topk_to_pos.shape[0]
+        R = y.shape[0]
+        ydt = torch.bfloat16 if self.in_fmt == "bf16" else torch.uint8
+        _check_cuda(y, "y", ydt, (R, self.hidden))
+        if self.in_fmt == "e4m3":
+            _check_cuda(y_scale, "y_scale", torch.float32, (R, self.hidden // 128))
+        else:
+            y_scale = None
+        _check_cuda(token_topk_to_pos, "token_topk_to_pos", torch.int32, (T, self.topk))
+        _check_cuda(topk_weights, "topk_weights", torch.float32, (T, self.topk))
+        if out is None:
+            out = torch.empty((T, self.hidden), dtype=torch.bfloat16, device=y.device)
+        _check_cuda(out, "out", torch.bfloat16, (T, self.hidden))
+        if stream is None:
+            stream = torch.cuda.current_stream(y.device)
+        with torch.cuda.device(y.device):
+            tk_moe_reduce_run(self.plan, T, y, y_scale, R, token_topk_to_pos, topk_weights,
+                              float(global_scale), out, stream.cuda_stream)
+        return out
 
 
 _plans: dict = {}

@@ -39,6 +39,12 @@ class QuantCastDesc(ctypes.Structure):
                 ("in_dtype", ctypes.c_int32), ("scale_layout", ctypes.c_int32)]
 
 
+class MoeReduceDesc(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int64), ("topk", ctypes.c_int32), ("in_fmt", ctypes.c_int32)]
+
+
+REDUCE_IN_FMTS = {"bf16": 0, "e4m3": 1}
+
 _VP = ctypes.c_void_p
 _P64 = ctypes.POINTER(ctypes.c_int64)
 _PINT = ctypes.POINTER(ctypes.c_int)
@@ -68,6 +74,11 @@ SIGNATURES = {
     "tk_quant_cast_output_sizes": (ctypes.c_int, [ctypes.POINTER(QuantCastDesc), ctypes.c_int64,
                                                   _PSZ, _PSZ]),
     "tk_quant_cast_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP]),
+    "tk_moe_reduce_validate": (ctypes.c_int, [ctypes.POINTER(MoeReduceDesc)]),
+    "tk_moe_reduce_plan": (ctypes.c_int, [ctypes.POINTER(MoeReduceDesc), ctypes.c_int, ctypes.POINTER(_VP)]),
+    "tk_moe_reduce_plan_destroy": (ctypes.c_int, [_VP]),
+    "tk_moe_reduce_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, ctypes.c_int64, _VP, _VP,
+                                         ctypes.c_float, _VP, _VP]),
     "tk_fault_word": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tk_last_error_message": (ctypes.c_char_p, []),
@@ -204,6 +215,27 @@ def tk_quant_cast_output_sizes(desc: QuantCastDesc, num_tokens: int) -> tuple[in
 
 def tk_quant_cast_run(plan: int, num_tokens: int, x, q, scales, stream: int | None) -> None:
     check(lib().tk_quant_cast_run(plan, num_tokens, _ptr(x), _ptr(q), _ptr(scales), stream))
+
+
+def tk_moe_reduce_validate(desc: MoeReduceDesc) -> int:
+    return lib().tk_moe_reduce_validate(ctypes.byref(desc))
+
+
+def tk_moe_reduce_plan(desc: MoeReduceDesc, device: int) -> int:
+    h = _VP()
+    check(lib().tk_moe_reduce_plan(ctypes.byref(desc), device, ctypes.byref(h)))
+    return h.value
+
+
+def tk_moe_reduce_plan_destroy(plan: int) -> None:
+    check(lib().tk_moe_reduce_plan_destroy(plan))
+
+
+def tk_moe_reduce_run(plan: int, num_tokens: int, y, y_scale, num_rows: int, token_topk_to_pos,
+                      topk_weights, global_scale: float, out, stream: int | None) -> None:
+    check(lib().tk_moe_reduce_run(plan, num_tokens, _ptr(y), _ptr(y_scale), num_rows,
+                                  _ptr(token_topk_to_pos), _ptr(topk_weights), global_scale, _ptr(out),
+                                  stream))
 
 
 def tk_fault_word(device: int, clear: bool = False) -> int:

@@ -28,8 +28,10 @@ class Workload:
     w_dist: str | None = None   # None | "topk8_norm" | "uniform"
     clamp: float | None = None
     seed: int = 0
-    op: str = "swiglu"          # "swiglu": x is [T, 2H] bf16; "cast": x is [T, H]
-    in_dtype: str = "bf16"      # cast input: "bf16" | "fp32"
+    op: str = "swiglu"          # "swiglu": x is [T, 2H] bf16; "cast": x is [T, H]; "reduce"
+    in_dtype: str = "bf16"      # cast input: "bf16" | "fp32"; reduce rows: "bf16" | "e4m3"
+    topk: int = 8               # reduce: slots per token (T tokens, T * topk expert rows)
+    empty_frac: float = 0.0     # reduce: share of empty slots
 
     @property
     def groups_per_row(self) -> int:
@@ -42,6 +44,12 @@ class Workload:
     def algo_bytes(self, rows: int | None = None) -> int:
         """Minimum HBM bytes one pass moves: input, codes, scales, weights."""
         T = self.T if rows is None else rows
+        if self.op == "reduce":
+            # every expert row read once (bf16, or E4M3 + 1x128 fp32 scales),
+            # positions and weights, one bf16 output row per token
+            row = 2 * self.H if self.in_dtype == "bf16" else self.H + 4 * (self.H // 128)
+            used = round(T * self.topk * (1.0 - self.empty_frac))
+            return used * row + 8 * T * self.topk + 2 * T * self.H
         x = T * self.x_cols * (4 if self.in_dtype == "fp32" else 2)
         q = T * self.H if self.out_fmt == "e4m3" else T * self.H // 2
         s = T * self.groups_per_row * (4 if self.scale_fmt == "fp32" else 1)
@@ -85,7 +93,17 @@ CAST_WORKLOADS = {
     "cast_T8192_H4096_token_fp32": Workload("cast_T8192_H4096_token_fp32", 8192, 4096, 0, "fp32", "e4m3",
                                             "row_lognormal", seed=2003, op="cast", in_dtype="fp32"),
 }
-ALL_WORKLOADS = {**WORKLOADS, **CAST_WORKLOADS}
+# The weighted top-k combine after the expert GEMMs: T tokens, each gathering
+# `topk` expert rows (a random permutation of the T * topk rows, as after a
+# dispatch, with a share of empty slots), weights normalised per token.
+REDUCE_WORKLOADS = {
+    "reduce_T4096_K8_H2048_bf16": Workload("reduce_T4096_K8_H2048_bf16", 4096, 2048, 0, "fp32", "e4m3",
+                                           "normal", seed=3001, op="reduce", topk=8, empty_frac=0.01),
+    "reduce_T4096_K8_H7168_e4m3": Workload("reduce_T4096_K8_H7168_e4m3", 4096, 7168, 0, "fp32", "e4m3",
+                                           "normal", seed=3002, op="reduce", in_dtype="e4m3", topk=8,
+                                           empty_frac=0.01),
+}
+ALL_WORKLOADS = {**WORKLOADS, **CAST_WORKLOADS, **REDUCE_WORKLOADS}
 
 _CHUNK_ROWS = 4096
 
@@ -133,3 +151,32 @@ def make_inputs(wl: Workload, device: str | torch.device = "cpu"):
 def bf16_bits(x: torch.Tensor):
     """View a bf16 tensor's bit patterns as a numpy uint16 array (host copy)."""
     return x.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def make_reduce_inputs(wl: Workload, device: str | torch.device = "cpu") -> dict:
+    """Inputs of a combine workload: y (bf16 [R, H], or E4M3 codes uint8 [R, H]
+    drawn as random non-NaN bytes with fp32 y_scale [R, H/128] in [2^-4, 2^4)),
+    token_topk_to_pos int32 [T, K] (a permutation of the R = T * K rows, a
+    share of slots emptied to -1), topk_weights fp32 [T, K] (U(0,1),
+    normalised per token) and the global scale gs."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(wl.seed)
+    T, K, H = wl.T, wl.topk, wl.H
+    R = T * K
+    if wl.in_dtype == "bf16":
+        y = torch.empty((R, H), dtype=torch.bfloat16, device=device)
+        for r0 in range(0, R, _CHUNK_ROWS):
+            r1 = min(R, r0 + _CHUNK_ROWS)
+            y[r0:r1] = torch.randn((r1 - r0, H), generator=gen, device=device).to(torch.bfloat16)
+        y_scale = None
+    else:
+        y = torch.randint(0, 256, (R, H), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+        y[(y & 0x7F) == 0x7F] = 0          # no NaN codes
+        y_scale = torch.exp2(torch.rand((R, H // 128), generator=gen, device=device) * 8 - 4)
+    perm = torch.randperm(R, generator=gen, device=device).to(torch.int32).view(T, K)
+    empty = torch.rand((T, K), generator=gen, device=device) < wl.empty_frac
+    pos = torch.where(empty, torch.full_like(perm, -1), perm)
+    w = torch.rand((T, K), generator=gen, device=device)
+    w = w / w.sum(dim=1, keepdim=True)
+    return {"y": y, "y_scale": y_scale, "pos": pos.contiguous(), "w": w.contiguous(), "gs": 2.5}

@@ -192,11 +192,11 @@ def time_oracle(wl, seconds: float, seed_rows: int = 8) -> dict:
     lib = oracle.load()
     small = wl.with_rows(max(8, seed_rows))
     t = time.perf_counter()
-    oracle_step(wl, *wls.make_inputs(small, "cpu"), lib)()
+    oracle_step(wl, *cpu_inputs(small), lib)()
     per_row = (time.perf_counter() - t) / small.T
     rows = int(max(8, min(wl.T, seconds / max(per_row, 1e-9))))
     rows = max(8, (rows // 8) * 8)
-    step = oracle_step(wl, *wls.make_inputs(wl.with_rows(rows), "cpu"), lib)
+    step = oracle_step(wl, *cpu_inputs(wl.with_rows(rows)), lib)
     t = time.perf_counter()
     step()
     dt = time.perf_counter() - t
@@ -204,11 +204,27 @@ def time_oracle(wl, seconds: float, seed_rows: int = 8) -> dict:
             "gbs": wl.algo_bytes(rows) / dt / 1e9}
 
 
+def cpu_inputs(wl):
+    """(x, w) for the fused op and the cast; (inputs dict, None) for the combine."""
+    from activation_fp8_quantization_gb300 import workloads as wls
+    if wl.op == "reduce":
+        return wls.make_reduce_inputs(wl, "cpu"), None
+    return wls.make_inputs(wl, "cpu")
+
+
 def oracle_step(wl, x, w, lib):
     """A closure running the CPU oracle once on these rows (inputs prepared)."""
     import oracle
     from activation_fp8_quantization_gb300 import workloads as wls
 
+    if wl.op == "reduce":
+        d = x
+        pos, wt = d["pos"].numpy(), d["w"].numpy()
+        if d["y_scale"] is None:
+            yb = wls.bf16_bits(d["y"])
+            return lambda: oracle.moe_reduce(yb, pos, wt, d["gs"], lib=lib)
+        yc, ys = d["y"].numpy(), d["y_scale"].numpy()
+        return lambda: oracle.moe_reduce(yc, pos, wt, d["gs"], y_scale=ys, lib=lib)
     if wl.op == "cast":
         y = x.float().numpy()
         return lambda: oracle.quant_rows_f32(y, wl.group, wl.scale_fmt, wl.out_fmt, lib=lib)
@@ -232,7 +248,7 @@ def run_reference(args, dist):
     per_row = calib["seconds"] / calib["rows"]
     budget = 120.0 / max(1, args.steps + args.warmup)
     rows = int(max(8, min(wl.T, budget / per_row)))
-    step = oracle_step(wl, *wls.make_inputs(wl.with_rows(rows), "cpu"), lib)
+    step = oracle_step(wl, *cpu_inputs(wl.with_rows(rows)), lib)
 
     for _ in range(args.warmup):
         step()
@@ -267,6 +283,8 @@ def config_of(wl, n: int) -> dict:
 
 
 def metric_of(wl) -> str:
+    if wl.op == "reduce":
+        return "tokens/s and achieved HBM GB/s (fraction of GB300 peak) for the weighted top-k combine"
     if wl.op == "cast":
         return "tokens/s and achieved HBM GB/s (fraction of GB300 peak) for the standalone FP8 cast"
     return METRIC
@@ -294,7 +312,9 @@ def run_ours(args, dist: Dist):
     torch.cuda.set_device(dev)
     wl = wls.ALL_WORKLOADS[args.workload]
     T, H = wl.T, wl.H
-    if wl.op == "cast":
+    if wl.op == "reduce":
+        op = None
+    elif wl.op == "cast":
         op = tk.QuantCast(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.in_dtype, dev, args.scale_layout)
         op.count_clamped = False
     else:
@@ -303,6 +323,8 @@ def run_ours(args, dist: Dist):
     algo = wl.algo_bytes()
     per_set = algo
     n_sets = max(2, -(-3 * L2_BYTES // per_set) + 1)   # sets beyond the current one hold > 3x L2
+    if wl.op == "reduce":
+        return run_reduce(args, dist, wl, dev, n_sets)
 
     x0, w0 = wls.make_inputs(wl, "cuda")
     q_shape, s_shape, s_dtype = op.output_shapes(T)
@@ -398,6 +420,103 @@ def run_ours(args, dist: Dist):
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clk,
+    }
+    emit(line, args)
+    return 0
+
+
+def time_graph(args, dist, stream, launch, n_sets, dev):
+    """Warm up, capture `chunk` launches in a CUDA graph, replay to exactly
+    K launches, timed with events on `stream`; returns (ms, clocks)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            launch(i)
+    stream.synchronize()
+    chunk = min(args.steps, n_sets * max(1, 600 // n_sets))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(chunk):
+            launch(i)
+    reps, rem = divmod(args.steps, chunk)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    stream.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device()) if dist.local_rank == 0 else None
+    if clocks:
+        clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        for i in range(rem):
+            launch(i)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    return ev0.elapsed_time(ev1), (clocks.stop() if clocks else None)
+
+
+def run_reduce(args, dist, wl, dev, n_sets):
+    """The combine on its workload: tokens/s over rotating input sets."""
+    import torch
+    import activation_fp8_quantization_gb300 as tk
+    from activation_fp8_quantization_gb300 import _abi
+    from activation_fp8_quantization_gb300 import workloads as wls
+
+    op = tk.MoeReduce(wl.H, wl.topk, wl.in_dtype, dev)
+    d0 = wls.make_reduce_inputs(wl, "cuda")
+    sets = []
+    for i in range(n_sets):
+        d = d0 if i == 0 else {k: (v.clone() if torch.is_tensor(v) else v) for k, v in d0.items()}
+        d["out"] = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=dev)
+        sets.append(d)
+    lib = _abi.lib()
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    R = d0["y"].shape[0]
+    ptrs = [(d["y"].data_ptr(), None if d["y_scale"] is None else d["y_scale"].data_ptr(),
+             d["pos"].data_ptr(), d["w"].data_ptr(), d["out"].data_ptr()) for d in sets]
+
+    def launch(i):
+        yp, ysp, pp, wp, op_ = ptrs[i % n_sets]
+        st = lib.tk_moe_reduce_run(op.plan, wl.T, yp, ysp, R, pp, wp, d0["gs"], op_, sh)
+        if st != 0:
+            raise tk.TkError(st, _abi.tk_last_error_message())
+
+    ms, clk = time_graph(args, dist, stream, launch, n_sets, dev)
+    ms_max = dist.max(ms, device=dev)
+    ms_per_step = ms_max / args.steps
+    value = dist.sum(float(wl.T * args.steps), device=dev) / (ms_max / 1e3)
+    algo = wl.algo_bytes()
+    achieved = algo / (ms_per_step / 1e3) / 1e9
+    peaks = measured_peaks()
+    cpu = None
+    if dist.rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
+        r = time_oracle(wl, args.cpu_seconds)
+        cpu = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": "%d of %d tokens of the same workload, single-threaded C oracle, %.1f s"
+                         % (r["rows"], wl.T, r["seconds"])}
+    if dist.rank != 0:
+        return 0
+    line = {
+        "metric": metric_of(wl), "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "K": wl.topk, "H": wl.H, "in_fmt": wl.in_dtype,
+                   "empty_slots": wl.empty_frac, "parallelism": "replicas x%d" % args.gpus,
+                   "l2": "inputs larger than L2: %d rotating input/output sets, %.0f MB" % (
+                       n_sets, n_sets * algo / 1e6)},
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peaks["source"],
+                     "algo_bytes_per_launch": algo},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clk,
     }
     emit(line, args)
     return 0

@@ -130,3 +130,17 @@ def test_plan_without_gpu_reports_cuda_error():
     with pytest.raises(tk.TkError) as e:
         tk.tk_swiglu_quant_plan(D(), 0)
     assert e.value.status in (1, 4)
+
+
+def test_reduce_validate():
+    R = tk.MoeReduceDesc
+    assert tk.tk_moe_reduce_validate(R(2048, 8, 0)) == 0
+    assert tk.tk_moe_reduce_validate(R(7168, 8, 1)) == 0
+    assert tk.tk_moe_reduce_validate(R(8192, 64, 0)) == 0
+    assert tk.tk_moe_reduce_validate(R(0, 8, 0)) == 1
+    assert tk.tk_moe_reduce_validate(R(2048, 0, 0)) == 1
+    assert tk.tk_moe_reduce_validate(R(2048, 8, 2)) == 1
+    assert tk.tk_moe_reduce_validate(R(2040, 8, 0)) == 2
+    assert tk.tk_moe_reduce_validate(R(8208, 8, 0)) == 2
+    assert tk.tk_moe_reduce_validate(R(2048, 65, 0)) == 2
+    assert tk.tk_moe_reduce_validate(R(2064, 8, 1)) == 2
