@@ -19,7 +19,7 @@ import threading
 from . import _abi
 from ._abi import (IN_DTYPES, OUT_FMTS, REDUCE_IN_FMTS, SCALE_FMTS, SCALE_LAYOUTS, MoeReduceDesc,
                    QuantCastDesc, SwigluQuantDesc, tk_moe_reduce_plan, tk_moe_reduce_plan_destroy,
-                   tk_moe_reduce_run, tk_moe_reduce_validate,
+                   tk_moe_reduce_launch_info, tk_moe_reduce_run, tk_moe_reduce_validate,
                    TkError, tk_fault_word, tk_last_error_message, tk_quant_cast_output_sizes,
                    tk_quant_cast_plan, tk_quant_cast_plan_destroy,
                    tk_quant_cast_run, tk_quant_cast_validate, tk_status_string,
@@ -32,7 +32,7 @@ from ._abi import (IN_DTYPES, OUT_FMTS, REDUCE_IN_FMTS, SCALE_FMTS, SCALE_LAYOUT
 __all__ = [
     "SwigluQuant", "HostPipe", "QuantCast", "MoeReduce", "swiglu_quant", "quant_cast", "TkError",
     "MoeReduceDesc", "tk_moe_reduce_validate", "tk_moe_reduce_plan", "tk_moe_reduce_plan_destroy",
-    "tk_moe_reduce_run",
+    "tk_moe_reduce_run", "tk_moe_reduce_launch_info",
     "tk_swiglu_quant_host_pipe_create", "tk_swiglu_quant_host_pipe_destroy",
     "tk_swiglu_quant_host_workspace_size", "tk_swiglu_quant_run_host",
     "tk_swiglu_quant_run_host_static",
@@ -262,6 +262,10 @@ class MoeReduce:
             except Exception:
                 pass
             self.plan = None
+
+    def launch_info(self, num_tokens: int, y=None, y_scale=None) -> dict:
+        """Kernel ("bulk" or "regs") and launch shape a run would use."""
+        return tk_moe_reduce_launch_info(self.plan, num_tokens, y, y_scale)
 
     def __call__(self, y, token_topk_to_pos, topk_weights, global_scale: float = 1.0, *,
                  y_scale=None, out=None, stream=None):

@@ -79,6 +79,8 @@ SIGNATURES = {
     "tk_moe_reduce_plan_destroy": (ctypes.c_int, [_VP]),
     "tk_moe_reduce_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, ctypes.c_int64, _VP, _VP,
                                          ctypes.c_float, _VP, _VP]),
+    "tk_moe_reduce_launch_info": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _PINT, _PINT, _PINT,
+                                                 _PINT]),
     "tk_fault_word": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tk_last_error_message": (ctypes.c_char_p, []),
@@ -236,6 +238,14 @@ def tk_moe_reduce_run(plan: int, num_tokens: int, y, y_scale, num_rows: int, tok
     check(lib().tk_moe_reduce_run(plan, num_tokens, _ptr(y), _ptr(y_scale), num_rows,
                                   _ptr(token_topk_to_pos), _ptr(topk_weights), global_scale, _ptr(out),
                                   stream))
+
+
+def tk_moe_reduce_launch_info(plan: int, num_tokens: int, y=None, y_scale=None) -> dict:
+    v = [ctypes.c_int() for _ in range(4)]
+    check(lib().tk_moe_reduce_launch_info(plan, num_tokens, _ptr(y), _ptr(y_scale),
+                                          *[ctypes.byref(x) for x in v]))
+    return {"kernel": ("regs", "bulk")[v[0].value], "grid": v[1].value, "block": v[2].value,
+            "smem_bytes": v[3].value}
 
 
 def tk_fault_word(device: int, clear: bool = False) -> int:

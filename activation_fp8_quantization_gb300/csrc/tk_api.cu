@@ -860,7 +860,97 @@ struct tk_moe_reduce_plan_s {
     const void *fn;
     int block, rpc, tpr, max_grid;
     unsigned *fault;
+    // bulk kernel (has_bulk: the shape allows it)
+    bool has_bulk;
+    int forced;   // 0: by alignment, 1: register kernel, 2: bulk kernel where allowed
+    const void *bulk_fn;
+    int nchunks, wc, stages, slot_bytes, rb, sb, smem, bulk_grid;
 };
+
+namespace {
+
+// Chunking of the bulk combine: the fewest equal chunks per token whose slot
+// (K row chunks, their scales, the metadata) fits kReduceSlotTarget bytes,
+// with every copy 16-byte aligned; then as many slots as shared memory holds,
+// up to kReduceMaxStages. Returns false where the bulk kernel does not apply (K > 32, rows
+// under 2 KB, E4M3 rows with H not a multiple of 512, fewer than 2 slots).
+// TK_REDUCE_SLOT_KB=<n> (read when the plan is made) overrides the target.
+// E4M3 rows gather fastest as whole rows (fewer, larger copies per task).
+constexpr int kReduceSlotTargetBf16 = 48 << 10;
+constexpr int kReduceSlotTargetE4M3 = 64 << 10;
+
+bool plan_reduce_bulk(tk_moe_reduce_plan_s *p, int optin)
+{
+    const tk_moe_reduce_desc &d = p->desc;
+    const bool fp8 = d.in_fmt == TK_REDUCE_IN_E4M3;
+    const int64_t elt = fp8 ? 1 : 2;
+    if (d.topk > tk::kReduceBulkMaxK || d.hidden * elt < 2048 || (fp8 && d.hidden % 512 != 0))
+        return false;
+    const int64_t unit = fp8 ? 512 : 8;   // chunk widths keep copies aligned (and E4M3 scale rows)
+    const int kb = env_int("TK_REDUCE_SLOT_KB", 0);
+    const int64_t target = kb > 0 ? (int64_t)kb << 10 : (fp8 ? kReduceSlotTargetE4M3 : kReduceSlotTargetBf16);
+    for (int64_t n = 1; n <= d.hidden / unit; ++n) {
+        if (d.hidden % n != 0 || (d.hidden / n) % unit != 0)
+            continue;
+        const int64_t wc = d.hidden / n;
+        const int64_t rb = wc * elt;
+        const int64_t sb = fp8 ? wc / 128 * 4 : 0;
+        const int64_t meta = 16 + 4 * (int64_t)d.topk;
+        const int64_t slot = (d.topk * (rb + sb) + meta + 127) / 128 * 128;
+        if (slot > target && n < d.hidden / unit)
+            continue;
+        const int64_t fit = (optin - 1024 - tk::kReduceMetaBytes) / (slot + 16);   // 1 KB for the runtime's reserve
+        const int stages = (int)(fit < tk::kReduceMaxStages ? fit : tk::kReduceMaxStages);
+        if (stages < 2)
+            return false;
+        p->nchunks = (int)n;
+        p->wc = (int)wc;
+        p->rb = (int)rb;
+        p->sb = (int)sb;
+        p->slot_bytes = (int)slot;
+        p->stages = stages;
+        p->smem = stages * (int)slot + 16 * stages + tk::kReduceMetaBytes;
+        return true;
+    }
+    return false;
+}
+
+struct ReduceLaunch {
+    bool bulk;
+    const void *fn;
+    int grid, block, smem;
+};
+
+// The bulk kernel runs for E4M3 rows where the plan allows it and y and
+// y_scale are 16-byte aligned: there it gathers faster than the register
+// kernel, whose bytes in flight are capped by registers at 16 bytes of row
+// per thread and slot. bf16 rows (32 bytes per thread and slot) go to the
+// register kernel, which was the faster of the two for them. Forcing the
+// bulk kernel applies it wherever the plan and the alignment allow.
+ReduceLaunch reduce_launch(const tk_moe_reduce_plan_s *p, int64_t T, const void *y, const float *y_scale)
+{
+    const bool fp8 = p->desc.in_fmt == TK_REDUCE_IN_E4M3;
+    const bool wanted = p->forced == 2 || (p->forced == 0 && fp8);
+    const bool bulk = p->has_bulk && wanted && aligned(y, 16) && (!fp8 || aligned(y_scale, 16));
+    ReduceLaunch L{};
+    L.bulk = bulk;
+    if (bulk) {
+        const int64_t tasks = T * p->nchunks;
+        L.fn = p->bulk_fn;
+        L.grid = (int)(tasks < p->bulk_grid ? (tasks > 0 ? tasks : 1) : p->bulk_grid);
+        L.block = tk::kReduceBulkThreads;
+        L.smem = p->smem;
+    } else {
+        const int64_t ntb = (T + p->rpc - 1) / p->rpc;
+        L.fn = p->fn;
+        L.grid = (int)(ntb < p->max_grid ? (ntb > 0 ? ntb : 1) : p->max_grid);
+        L.block = p->block;
+        L.smem = 0;
+    }
+    return L;
+}
+
+}  // namespace
 
 TK_API tk_status tk_moe_reduce_validate(const tk_moe_reduce_desc *d)
 {
@@ -917,6 +1007,26 @@ TK_API tk_status tk_moe_reduce_plan(const tk_moe_reduce_desc *d, int device, tk_
         return fail(TK_ERR_UNSUPPORTED, "kernel cannot be resident with %d threads per CTA", p.block);
     p.max_grid = occ * num_sms;
     p.fault = static_cast<unsigned *>(fault);
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "querying the device");
+    p.has_bulk = plan_reduce_bulk(&p, optin);
+    if (p.has_bulk) {
+        p.bulk_fn = tk::moe_reduce_bulk_kernel_fn(d->in_fmt);
+        e = cudaFuncSetAttribute(p.bulk_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
+        int bocc = 0;
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bocc, p.bulk_fn, tk::kReduceBulkThreads, p.smem);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "configuring the bulk combine kernel");
+        p.has_bulk = bocc >= 1;
+        p.bulk_grid = bocc * num_sms;
+    }
+    // TK_REDUCE_KERNEL=regs or =bulk (read when the plan is made) forces one
+    // kernel where the shape (and, for bulk, the alignment) allows it.
+    const char *force = getenv("TK_REDUCE_KERNEL");
+    p.forced = !force ? 0 : (strcmp(force, "regs") == 0 ? 1 : (strcmp(force, "bulk") == 0 ? 2 : 0));
     auto *h = new (std::nothrow) tk_moe_reduce_plan_s(p);
     if (!h)
         return fail(TK_ERR_INVALID_ARG, "out of host memory");
@@ -970,11 +1080,32 @@ TK_API tk_status tk_moe_reduce_run(tk_moe_reduce_plan_t plan, int64_t T, const v
     a.tpr = plan->tpr;
     a.rpc = plan->rpc;
     a.fault = plan->fault;
-    const int64_t ntb = (T + plan->rpc - 1) / plan->rpc;
-    const int grid = (int)(ntb < plan->max_grid ? ntb : plan->max_grid);
-    cudaError_t e = tk::launch_moe_reduce(plan->fn, grid, plan->block, a, static_cast<cudaStream_t>(stream));
+    const ReduceLaunch L = reduce_launch(plan, T, y, y_scale);
+    a.nchunks = plan->nchunks;
+    a.wc = plan->wc;
+    a.stages = plan->stages;
+    a.slot_bytes = plan->slot_bytes;
+    a.rb = plan->rb;
+    a.sb = plan->sb;
+    cudaError_t e = tk::launch_moe_reduce(L.fn, L.grid, L.block, L.smem, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the combine kernel");
+    return ok();
+}
+
+TK_API tk_status tk_moe_reduce_launch_info(tk_moe_reduce_plan_t plan, int64_t num_tokens, const void *y,
+                                           const float *y_scale, int *kernel, int *grid, int *block,
+                                           int *smem_bytes)
+{
+    if (!plan || !kernel || !grid || !block || !smem_bytes)
+        return fail(TK_ERR_INVALID_ARG, "plan and outputs must be non-NULL");
+    if (num_tokens < 0)
+        return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0");
+    const ReduceLaunch L = reduce_launch(plan, num_tokens, y, y_scale);
+    *kernel = L.bulk ? 1 : 0;
+    *grid = L.grid;
+    *block = L.block;
+    *smem_bytes = L.smem;
     return ok();
 }
 

@@ -54,12 +54,28 @@ struct ReduceArgs {
     int64_t T;
     float gs;                 // global scale
     void *out;                // [T, H] bf16
-    int32_t tpr, rpc;         // threads per token row (H / 16), tokens per CTA step
-    unsigned *fault;          // bit 1: a position outside [-1, R) was met (and skipped)
+    int32_t tpr, rpc;         // register kernel: threads per token row (H / 16), tokens per CTA step
+    unsigned *fault;          // bit 0: a wait gave up; bit 1: a position outside [-1, R) was met (and skipped)
+    // bulk kernel: a task is one column chunk of one token
+    int32_t nchunks;          // chunks per token
+    int32_t wc;               // columns per chunk
+    int32_t stages;           // ring slots per CTA
+    int32_t slot_bytes;       // bytes per slot (rows, then scales, then the slot's metadata)
+    int32_t rb;               // bytes of one row's chunk
+    int32_t sb;               // bytes of one row's chunk scales (E4M3), else 0
 };
 
+// Bulk kernel: 1 producer warp + kReduceConsumerWarps consumer warps per CTA.
+constexpr int kReduceConsumerWarps = 8;
+constexpr int kReduceBulkThreads = 32 * (1 + kReduceConsumerWarps);
+constexpr int kReduceBulkMaxK = 32;   // one producer lane per slot
+constexpr int kReduceMetaBytes = 8 * 32 * 8;   // the producer's metadata ring (8 tasks x 32 lanes x 8 B)
+constexpr int kReduceMaxStages = 16;
+
 const void *moe_reduce_kernel_fn(int in_fmt);
-cudaError_t launch_moe_reduce(const void *fn, int grid, int block, const ReduceArgs &a, cudaStream_t stream);
+const void *moe_reduce_bulk_kernel_fn(int in_fmt);
+cudaError_t launch_moe_reduce(const void *fn, int grid, int block, int smem, const ReduceArgs &a,
+                              cudaStream_t stream);
 
 // Bytes of one warp-ring slot of the stream kernels.
 constexpr int kSwigluSlotBytes = SwigluSrc<false>::kSpans * SwigluSrc<false>::kSpanBytes;

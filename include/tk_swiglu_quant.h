@@ -314,6 +314,17 @@ tk_status tk_moe_reduce_run(tk_moe_reduce_plan_t plan, int64_t num_tokens, const
                             const float *y_scale, int64_t num_rows, const int32_t *token_topk_to_pos,
                             const float *topk_weights, float global_scale, void *out, void *stream);
 
+/* Which kernel and launch shape a run would use (host only). kernel: 1 for
+ * the bulk-copy kernel (a producer warp per CTA gathers each token's K row
+ * chunks into a shared-memory ring with TMA bulk copies), 0 for the register
+ * kernel (any valid shape). The bulk kernel runs for E4M3 rows with K <= 32,
+ * H % 512 == 0 and H >= 2048, and y and y_scale 16-byte aligned; bf16 rows
+ * take the register kernel. Both give bit-identical outputs. grid and block
+ * in CTAs and threads, smem_bytes the dynamic shared memory per CTA. */
+tk_status tk_moe_reduce_launch_info(tk_moe_reduce_plan_t plan, int64_t num_tokens, const void *y,
+                                    const float *y_scale, int *kernel, int *grid, int *block,
+                                    int *smem_bytes);
+
 /* ------------------------------------------------------------------------
  * Diagnostics
  * ---------------------------------------------------------------------- */

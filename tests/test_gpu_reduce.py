@@ -93,21 +93,45 @@ def _run(op, d):
     return out
 
 
+KERNELS = ["regs", "bulk"]
+
+
+def _plan(monkeypatch, kernel, H, K, in_fmt="bf16"):
+    """A plan made with the kernel choice forced (read when the plan is made)."""
+    monkeypatch.setenv("TK_REDUCE_KERNEL", kernel)
+    op = tk.MoeReduce(H, K, in_fmt)
+    monkeypatch.delenv("TK_REDUCE_KERNEL")
+    return op
+
+
+def _expect_kernel(op, d, kernel):
+    info = op.launch_info(d["pos"].shape[0], d["y"], d["y_scale"])
+    bulk_ok = op.topk <= 32 and op.hidden * (2 if op.in_fmt == "bf16" else 1) >= 2048 and (
+        op.in_fmt == "bf16" or op.hidden % 512 == 0)
+    assert info["kernel"] == ("bulk" if kernel == "bulk" and bulk_ok else "regs"), info
+    return info
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("name", list(wls.REDUCE_WORKLOADS))
-def test_reduce_small_parity(name):
+def test_reduce_small_parity(name, kernel, monkeypatch):
     wl = wls.REDUCE_WORKLOADS[name].with_rows(3001)
     d = wls.make_reduce_inputs(wl, "cuda")
-    op = tk.MoeReduce(wl.H, wl.topk, wl.in_dtype)
+    op = _plan(monkeypatch, kernel, wl.H, wl.topk, wl.in_dtype)
+    _expect_kernel(op, d, kernel)
     got = _bits(_run(op, d))
     same = check_close(got, _oracle(d), d, what=name)
-    print(name, "identical %.6f" % same)
+    print(name, kernel, "identical %.6f" % same)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("name", list(wls.REDUCE_WORKLOADS))
-def test_reduce_full_size(name):
+def test_reduce_full_size(name, kernel, monkeypatch):
     wl = wls.REDUCE_WORKLOADS[name]
     d = wls.make_reduce_inputs(wl, "cuda")
-    op = tk.MoeReduce(wl.H, wl.topk, wl.in_dtype)
+    op = _plan(monkeypatch, kernel, wl.H, wl.topk, wl.in_dtype)
+    _expect_kernel(op, d, kernel)
+    tk.tk_fault_word(torch.cuda.current_device(), clear=True)
     out = _run(op, d)
     rng = np.random.default_rng(wl.seed)
     idx = np.unique(np.concatenate([np.arange(16), np.arange(wl.T - 16, wl.T),
@@ -117,14 +141,9 @@ def test_reduce_full_size(name):
     assert tk.tk_fault_word(torch.cuda.current_device()) == 0
 
 
-@pytest.mark.parametrize("in_fmt", ["bf16", "e4m3"])
-@pytest.mark.parametrize("H,K", [(16, 1), (48, 3), (128, 17), (2048, 8), (7168, 8), (8192, 2)])
-def test_reduce_shapes(H, K, in_fmt):
-    if in_fmt == "e4m3" and H % 128:
-        pytest.skip("E4M3 rows need 1x128 scale groups")
-    T = 77
-    R = 3 * T
-    g = torch.Generator().manual_seed(H * 31 + K)
+def _random_case(H, K, in_fmt, T, seed):
+    R = 3 * T + 1
+    g = torch.Generator().manual_seed(seed)
     if in_fmt == "bf16":
         y = torch.randn((R, H), generator=g).to(torch.bfloat16)
         ys = None
@@ -135,10 +154,55 @@ def test_reduce_shapes(H, K, in_fmt):
     # positions may repeat (rows shared by tokens) and include empty slots
     pos = torch.randint(-1, R, (T, K), generator=g, dtype=torch.int32)
     w = torch.rand((T, K), generator=g)
-    d = {"y": y.cuda(), "y_scale": None if ys is None else ys.cuda(), "pos": pos.cuda(), "w": w.cuda(),
-         "gs": 0.5}
-    got = _bits(_run(tk.MoeReduce(H, K, in_fmt), d))
-    check_close(got, _oracle(d), d, what="H=%d K=%d %s" % (H, K, in_fmt))
+    return {"y": y.cuda(), "y_scale": None if ys is None else ys.cuda(), "pos": pos.cuda(), "w": w.cuda(),
+            "gs": 0.5}
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("in_fmt", ["bf16", "e4m3"])
+@pytest.mark.parametrize("H,K", [(16, 1), (48, 3), (128, 17), (1024, 5), (2048, 8), (4096, 32),
+                                 (7168, 8), (8192, 2), (8192, 33)])
+def test_reduce_shapes(H, K, in_fmt, kernel, monkeypatch):
+    if in_fmt == "e4m3" and H % 128:
+        pytest.skip("E4M3 rows need 1x128 scale groups")
+    d = _random_case(H, K, in_fmt, 77, H * 31 + K)
+    op = _plan(monkeypatch, kernel, H, K, in_fmt)
+    _expect_kernel(op, d, kernel)
+    got = _bits(_run(op, d))
+    check_close(got, _oracle(d), d, what="H=%d K=%d %s %s" % (H, K, in_fmt, kernel))
+
+
+@pytest.mark.parametrize("in_fmt", ["bf16", "e4m3"])
+@pytest.mark.parametrize("H,K,T", [(1024, 1, 1), (2048, 8, 5), (2048, 3, 151), (4096, 17, 153),
+                                   (7168, 8, 300), (7168, 32, 64), (8192, 8, 1000), (3584, 6, 77)])
+def test_reduce_kernels_agree_bit_for_bit(H, K, T, in_fmt, monkeypatch):
+    """Both kernels take the same arithmetic in the same order: identical bits,
+    including where tokens are fewer than CTAs and where a token spans chunks."""
+    if in_fmt == "e4m3" and H % 128:
+        pytest.skip("E4M3 rows need 1x128 scale groups")
+    d = _random_case(H, K, in_fmt, T, H + 7 * K + T)
+    outs = {}
+    for kernel in KERNELS:
+        op = _plan(monkeypatch, kernel, H, K, in_fmt)
+        _expect_kernel(op, d, kernel)
+        outs[kernel] = _bits(_run(op, d))
+    assert np.array_equal(outs["regs"], outs["bulk"])
+    check_close(outs["bulk"], _oracle(d), d, what="H=%d K=%d T=%d %s" % (H, K, T, in_fmt))
+
+
+def test_reduce_unaligned_scales_take_the_register_kernel():
+    H, K, T = 2048, 8, 50
+    d = _random_case(H, K, "e4m3", T, 5)
+    R = d["y"].shape[0]
+    buf = torch.empty(R * (H // 128) + 1, dtype=torch.float32, device="cuda")
+    ys = buf[1:].view(R, H // 128)          # 4-byte but not 16-byte aligned
+    ys.copy_(d["y_scale"])
+    op = tk.MoeReduce(H, K, "e4m3")
+    assert op.launch_info(T, d["y"], d["y_scale"])["kernel"] == "bulk"
+    assert op.launch_info(T, d["y"], ys)["kernel"] == "regs"
+    a = _bits(_run(op, d))
+    b = _bits(_run(op, dict(d, y_scale=ys)))
+    assert np.array_equal(a, b)
 
 
 def test_reduce_exact_cases():
@@ -158,19 +222,47 @@ def test_reduce_exact_cases():
     op(y, torch.empty((0, 4), dtype=torch.int32).cuda(), torch.empty((0, 4)).cuda(), 1.0)
 
 
-def test_reduce_invalid_positions_are_skipped_and_flagged():
-    H, T, R, K = 256, 32, 50, 2
+@pytest.mark.parametrize("H", [256, 2048])
+def test_reduce_invalid_positions_are_skipped_and_flagged(H):
+    """Also run through the bulk kernel below (E4M3 rows take it by default)."""
+    T, R, K = 32, 50, 2
     dev = torch.cuda.current_device()
     tk.tk_fault_word(dev, clear=True)
     y = torch.randn((R, H)).to(torch.bfloat16).cuda()
     pos = torch.tensor([[0, R]] * (T // 2) + [[1, -7]] * (T // 2), dtype=torch.int32).cuda()
     w = torch.ones((T, K)).cuda()
-    out = tk.MoeReduce(H, K)(y, pos, w, 1.0)
+    op = tk.MoeReduce(H, K)
+    assert op.launch_info(T, y)["kernel"] == "regs"       # bf16 rows: the register kernel by default
+    out = op(y, pos, w, 1.0)
     torch.cuda.synchronize()
     assert tk.tk_fault_word(dev, clear=True) & 2
     # the bad slot contributed nothing
     assert torch.equal(out[: T // 2], y[0].expand(T // 2, H))
     assert torch.equal(out[T // 2:], y[1].expand(T // 2, H))
+    assert tk.tk_fault_word(dev) == 0
+
+
+def test_reduce_invalid_positions_bulk_kernel():
+    H, T, R, K = 2048, 32, 50, 2
+    dev = torch.cuda.current_device()
+    tk.tk_fault_word(dev, clear=True)
+    y = torch.randint(0, 0x7E, (R, H), dtype=torch.int32).to(torch.uint8).cuda()
+    ys = torch.full((R, H // 128), 0.5).cuda()
+    pos = torch.tensor([[0, R]] * (T // 2) + [[1, -7]] * (T // 2), dtype=torch.int32).cuda()
+    w = torch.ones((T, K)).cuda()
+    op = tk.MoeReduce(H, K, "e4m3")
+    assert op.launch_info(T, y, ys)["kernel"] == "bulk"
+    out = op(y, pos, w, 1.0, y_scale=ys)
+    torch.cuda.synchronize()
+    assert tk.tk_fault_word(dev, clear=True) & 2
+    one = tk.MoeReduce(H, 1, "e4m3")   # the valid slot alone, through the same kernel
+    want0 = one(y, torch.zeros((T // 2, 1), dtype=torch.int32).cuda(), torch.ones((T // 2, 1)).cuda(), 1.0,
+                y_scale=ys)
+    want1 = one(y, torch.ones((T // 2, 1), dtype=torch.int32).cuda(), torch.ones((T // 2, 1)).cuda(), 1.0,
+                y_scale=ys)
+    torch.cuda.synchronize()
+    assert torch.equal(out[: T // 2], want0)
+    assert torch.equal(out[T // 2:], want1)
     assert tk.tk_fault_word(dev) == 0
 
 
