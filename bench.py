@@ -404,6 +404,9 @@ def run_ours(args, dist: Dist):
     if dist.rank != 0:
         return 0
     traffic = load_traffic(wl.name)
+    kernel = None
+    if wl.op == "swiglu":
+        kernel = "warp_stream_kernel" if op.launch_info(T)["rows_per_cta"] == 0 else "row_quant_kernel"
     line = {
         "metric": metric_of(wl), "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -414,7 +417,7 @@ def run_ours(args, dist: Dist):
                        n_sets, n_sets * per_set / 1e6)},
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": kernel,
                      "peak_source": peaks["source"], "algo_bytes_per_launch": algo},
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -488,6 +491,7 @@ def run_reduce(args, dist, wl, dev, n_sets):
         if st != 0:
             raise tk.TkError(st, _abi.tk_last_error_message())
 
+    info = op.launch_info(wl.T, d0["y"], d0["y_scale"])
     ms, clk = time_graph(args, dist, stream, launch, n_sets, dev)
     ms_max = dist.max(ms, device=dev)
     ms_per_step = ms_max / args.steps
@@ -514,8 +518,9 @@ def run_reduce(args, dist, wl, dev, n_sets):
                        n_sets, n_sets * algo / 1e6)},
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "peak_source": peaks["source"],
-                     "algo_bytes_per_launch": algo},
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(wl.name),
+                     "kernel": "moe_reduce_%s" % ("bulk_kernel" if info["kernel"] == "bulk" else "kernel"),
+                     "peak_source": peaks["source"], "algo_bytes_per_launch": algo},
         "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clk,
     }
     emit(line, args)
@@ -537,12 +542,15 @@ def kernel_source_hash() -> str:
 
 def load_traffic(workload: str):
     """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
-    from the committed ncu summary profiles/swiglu_quant_<workload>.md, or
-    None if there is none or it was taken on other kernel sources."""
-    path = os.path.join(ROOT, "profiles", "swiglu_quant_%s.md" % workload)
+    from the committed ncu summary profiles/<kernel>_<workload>.md, or None
+    if there is none or it was taken on other kernel sources."""
+    import glob
+    paths = sorted(glob.glob(os.path.join(ROOT, "profiles", "*_%s.md" % workload)))
+    if not paths:
+        return None
     fields = {}
     try:
-        with open(path) as f:
+        with open(paths[0]) as f:
             for line in f:
                 if line.startswith("- ") and ": " in line:
                     k, v = line[2:].strip().split(": ", 1)
