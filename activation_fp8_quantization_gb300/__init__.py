@@ -27,6 +27,7 @@ from ._abi import (IN_DTYPES, OUT_FMTS, REDUCE_IN_FMTS, SCALE_FMTS, SCALE_LAYOUT
                    tk_swiglu_quant_host_workspace_size, tk_swiglu_quant_launch_info,
                    tk_swiglu_quant_output_sizes, tk_swiglu_quant_plan, tk_swiglu_quant_plan_destroy,
                    tk_swiglu_quant_run, tk_swiglu_quant_run_host, tk_swiglu_quant_run_host_static,
+                   tk_swiglu_quant_run_transposed, tk_swiglu_quant_transposed_size,
                    tk_swiglu_quant_validate)
 
 __all__ = [
@@ -38,7 +39,8 @@ __all__ = [
     "tk_swiglu_quant_run_host_static",
     "SwigluQuantDesc", "QuantCastDesc", "tk_swiglu_quant_validate", "tk_swiglu_quant_plan",
     "tk_swiglu_quant_plan_destroy", "tk_swiglu_quant_output_sizes", "tk_swiglu_quant_run",
-    "tk_swiglu_quant_launch_info", "tk_quant_cast_validate", "tk_quant_cast_plan",
+    "tk_swiglu_quant_launch_info", "tk_swiglu_quant_run_transposed", "tk_swiglu_quant_transposed_size",
+    "tk_quant_cast_validate", "tk_quant_cast_plan",
     "tk_quant_cast_plan_destroy", "tk_quant_cast_output_sizes", "tk_quant_cast_run", "tk_status_string",
     "tk_last_error_message", "tk_fault_word",
 ]
@@ -144,6 +146,40 @@ class SwigluQuant:
             tk_swiglu_quant_run(self.plan, T, x, topk_weights, q, scales, clamped_count,
                                 stream.cuda_stream)
         return q, scales
+
+    def transposed(self, x, topk_weights=None, *, qt=None, scales=None, clamped_count=None,
+                   stream=None):
+        """The same op with the codes stored transposed (tk_swiglu_quant_run_transposed):
+        returns (qt [H, ld] uint8 with ld = T rounded up to 16, scales)."""
+        torch = _torch()
+        T = x.shape[0]
+        _check_cuda(x, "x", torch.bfloat16, (T, 2 * self.hidden))
+        if self.has_w:
+            if topk_weights is None:
+                raise ValueError("this op was planned with top-k weights")
+            _check_cuda(topk_weights, "topk_weights", torch.float32, (T,))
+        else:
+            topk_weights = None
+        if self.count_clamped:
+            if clamped_count is None:
+                raise ValueError("this op was planned with count_clamped; pass an int64[2] tensor")
+            _check_cuda(clamped_count, "clamped_count", torch.int64, (2,))
+        else:
+            clamped_count = None
+        _, ld = tk_swiglu_quant_transposed_size(self.plan, T)
+        _, s_shape, s_dtype = self.output_shapes(T)
+        if qt is None:
+            qt = torch.empty((self.hidden, ld), dtype=torch.uint8, device=x.device)
+        _check_cuda(qt, "qt", torch.uint8, (self.hidden, ld))
+        if scales is None:
+            scales = torch.empty(s_shape, dtype=s_dtype, device=x.device)
+        _check_cuda(scales, "scales", s_dtype, s_shape)
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device)
+        with torch.cuda.device(x.device):
+            tk_swiglu_quant_run_transposed(self.plan, T, x, topk_weights, qt, scales, clamped_count,
+                                           stream.cuda_stream)
+        return qt, scales
 
 
 class HostPipe:

@@ -60,6 +60,9 @@ SIGNATURES = {
                                                     _PSZ, _PSZ]),
     "tk_swiglu_quant_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP]),
     "tk_swiglu_quant_launch_info": (ctypes.c_int, [_VP, ctypes.c_int64, _PINT, _PINT, _PINT, _PINT]),
+    "tk_swiglu_quant_transposed_size": (ctypes.c_int, [_VP, ctypes.c_int64, _PSZ,
+                                                       ctypes.POINTER(ctypes.c_int64)]),
+    "tk_swiglu_quant_run_transposed": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP]),
     "tk_swiglu_quant_host_pipe_create": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.POINTER(_VP)]),
     "tk_swiglu_quant_host_pipe_destroy": (ctypes.c_int, [_VP]),
     "tk_swiglu_quant_host_workspace_size": (ctypes.c_int, [_VP, _PSZ]),
@@ -150,6 +153,20 @@ def tk_swiglu_quant_run(plan: int, num_tokens: int, x, topk_weights, q, scales, 
                         stream: int | None) -> None:
     check(lib().tk_swiglu_quant_run(plan, num_tokens, _ptr(x), _ptr(topk_weights), _ptr(q),
                                     _ptr(scales), _ptr(clamped_count), stream))
+
+
+def tk_swiglu_quant_transposed_size(plan: int, num_tokens: int) -> tuple[int, int]:
+    """(bytes of qt, ld) for num_tokens rows."""
+    n = ctypes.c_size_t()
+    ld = ctypes.c_int64()
+    check(lib().tk_swiglu_quant_transposed_size(plan, num_tokens, ctypes.byref(n), ctypes.byref(ld)))
+    return n.value, ld.value
+
+
+def tk_swiglu_quant_run_transposed(plan: int, num_tokens: int, x, topk_weights, qt, scales, clamped_count,
+                                   stream: int | None) -> None:
+    check(lib().tk_swiglu_quant_run_transposed(plan, num_tokens, _ptr(x), _ptr(topk_weights), _ptr(qt),
+                                               _ptr(scales), _ptr(clamped_count), stream))
 
 
 def tk_swiglu_quant_launch_info(plan: int, num_tokens: int) -> dict:

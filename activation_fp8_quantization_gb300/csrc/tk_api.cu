@@ -361,6 +361,9 @@ struct tk_swiglu_quant_plan_s {
     tk_swiglu_quant_desc desc;
     int device;
     Launches Ls;
+    // transposed-codes kernel (null where the shape does not allow it)
+    const void *tfn;
+    int tgrid;
 };
 
 struct tk_quant_cast_plan_s {
@@ -405,7 +408,22 @@ TK_API tk_status tk_swiglu_quant_plan(const tk_swiglu_quant_desc *d, int device,
     st = make_launches(device, d->hidden, d->group_size, row_fn, stream_fn, tk::kSwigluSlotBytes, &Ls);
     if (st != TK_OK)
         return st;
-    auto *p = new (std::nothrow) tk_swiglu_quant_plan_s{*d, device, Ls};
+    // The transposed-codes kernel: E4M3, groups of 32, 64 or 128 columns
+    // inside its 128-column tiles.
+    const void *tfn = nullptr;
+    int tgrid = 0;
+    if (d->out_fmt == TK_OUT_E4M3 && d->hidden % 128 == 0 &&
+        (d->group_size == 32 || d->group_size == 64 || d->group_size == 128)) {
+        tfn = tk::transpose_kernel_fn(d->scale_fmt, clamp);
+        int occ = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, tfn, tk::transpose_threads(), 0);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "occupancy of the transposed kernel");
+        tgrid = occ * Ls.rows.num_sms;
+        if (tgrid < 1)
+            tfn = nullptr;
+    }
+    auto *p = new (std::nothrow) tk_swiglu_quant_plan_s{*d, device, Ls, tfn, tgrid};
     if (!p)
         return fail(TK_ERR_INVALID_ARG, "out of host memory");
     *plan = p;
@@ -432,16 +450,12 @@ TK_API tk_status tk_swiglu_quant_output_sizes(const tk_swiglu_quant_desc *d, int
     return ok();
 }
 
-TK_API tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t T, const void *x,
-                                     const float *topk_weights, void *q, void *scales,
-                                     int64_t *clamped_count, void *stream)
+namespace {
+
+// The argument checks shared by the row-major and the transposed call.
+tk_status check_swiglu_args(const tk_swiglu_quant_plan_s *plan, const void *x, const float *topk_weights,
+                            const void *q, const void *scales, const int64_t *clamped_count)
 {
-    if (!plan)
-        return fail(TK_ERR_INVALID_ARG, "plan is NULL");
-    if (T < 0)
-        return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)T);
-    if (T == 0)
-        return ok();
     const tk_swiglu_quant_desc &d = plan->desc;
     if (!x || !q || !scales)
         return fail(TK_ERR_INVALID_ARG, "x, q and scales must be non-NULL");
@@ -461,10 +475,12 @@ TK_API tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t T, con
         return fail(TK_ERR_MISALIGNED, "topk_weights must be 4-byte aligned");
     if (d.count_clamped && !aligned(clamped_count, 8))
         return fail(TK_ERR_MISALIGNED, "clamped_count must be 8-byte aligned");
-    tk_status st = check_current_device(plan->device);
-    if (st != TK_OK)
-        return st;
+    return check_current_device(plan->device);
+}
 
+tk::SwigluArgs swiglu_args(const tk_swiglu_quant_desc &d, const void *x, const float *topk_weights,
+                           int64_t *clamped_count)
+{
     tk::SwigluArgs a{};
     a.x = static_cast<const uint16_t *>(x);
     a.w = d.has_topk_weights ? topk_weights : nullptr;
@@ -472,6 +488,26 @@ TK_API tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t T, con
     a.limit = d.use_clamp ? d.clamp_limit : 0.0f;
     a.H = (int32_t)d.hidden;
     set_packed_limit(a);
+    return a;
+}
+
+}  // namespace
+
+TK_API tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t T, const void *x,
+                                     const float *topk_weights, void *q, void *scales,
+                                     int64_t *clamped_count, void *stream)
+{
+    if (!plan)
+        return fail(TK_ERR_INVALID_ARG, "plan is NULL");
+    if (T < 0)
+        return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)T);
+    if (T == 0)
+        return ok();
+    const tk_swiglu_quant_desc &d = plan->desc;
+    tk_status st = check_swiglu_args(plan, x, topk_weights, q, scales, clamped_count);
+    if (st != TK_OK)
+        return st;
+    const tk::SwigluArgs a = swiglu_args(d, x, topk_weights, clamped_count);
     tk::OutArgs o{static_cast<uint8_t *>(q), scales};
     const Launch &L = pick(plan->Ls, T);
     cudaError_t e = tk::launch_swiglu(L.fn, grid_for(L, T), L.block, L.smem, a, o,
@@ -479,6 +515,54 @@ TK_API tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t T, con
                                       static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the fused kernel");
+    return ok();
+}
+
+TK_API tk_status tk_swiglu_quant_transposed_size(tk_swiglu_quant_plan_t plan, int64_t T, size_t *qt_bytes,
+                                                 int64_t *ld)
+{
+    if (!plan || T < 0 || !qt_bytes || !ld)
+        return fail(TK_ERR_INVALID_ARG, "plan and outputs must be non-NULL and num_tokens >= 0");
+    if (!plan->tfn)
+        return fail(TK_ERR_UNSUPPORTED, "transposed codes need E4M3, group_size 32, 64 or 128 and "
+                                        "hidden % 128 == 0");
+    *ld = (T + 15) / 16 * 16;
+    *qt_bytes = (size_t)plan->desc.hidden * (size_t)*ld;
+    return ok();
+}
+
+TK_API tk_status tk_swiglu_quant_run_transposed(tk_swiglu_quant_plan_t plan, int64_t T, const void *x,
+                                                const float *topk_weights, void *qt, void *scales,
+                                                int64_t *clamped_count, void *stream)
+{
+    if (!plan)
+        return fail(TK_ERR_INVALID_ARG, "plan is NULL");
+    if (T < 0)
+        return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)T);
+    if (!plan->tfn)
+        return fail(TK_ERR_UNSUPPORTED, "transposed codes need E4M3, group_size 32, 64 or 128 and "
+                                        "hidden % 128 == 0");
+    if (T == 0)
+        return ok();
+    const tk_swiglu_quant_desc &d = plan->desc;
+    tk_status st = check_swiglu_args(plan, x, topk_weights, qt, scales, clamped_count);
+    if (st != TK_OK)
+        return st;
+    const tk::SwigluArgs a = swiglu_args(d, x, topk_weights, clamped_count);
+    tk::OutArgs o{static_cast<uint8_t *>(qt), scales};
+    const Launch &L = plan->Ls.rows;
+    tk::RowShape sh = shape_for(L, T, d.hidden, d.scale_layout, d.scale_fmt);
+    int lg = 0;
+    while ((16 << lg) < d.group_size)
+        ++lg;
+    sh.tpg_log2 = lg;
+    sh.groups = (int32_t)(d.hidden / d.group_size);
+    const int64_t ldq = (T + 15) / 16 * 16;
+    const int64_t tiles = (T + 63) / 64 * (d.hidden / 128);
+    const int grid = (int)(tiles < plan->tgrid ? tiles : plan->tgrid);
+    cudaError_t e = tk::launch_transpose(plan->tfn, grid, a, o, sh, ldq, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launch of the transposed kernel");
     return ok();
 }
 

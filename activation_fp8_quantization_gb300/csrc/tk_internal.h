@@ -72,6 +72,12 @@ constexpr int kReduceBulkMaxK = 32;   // one producer lane per slot
 constexpr int kReduceMetaBytes = 8 * 32 * 8;   // the producer's metadata ring (8 tasks x 32 lanes x 8 B)
 constexpr int kReduceMaxStages = 16;
 
+// Fused op with the codes written transposed (E4M3, groups of 32/64/128).
+const void *transpose_kernel_fn(int scale_fmt, bool clamp);
+int transpose_threads();
+cudaError_t launch_transpose(const void *fn, int grid, const SwigluArgs &a, const OutArgs &o, const RowShape &sh,
+                             int64_t ldq, cudaStream_t stream);
+
 const void *moe_reduce_kernel_fn(int in_fmt);
 const void *moe_reduce_bulk_kernel_fn(int in_fmt);
 cudaError_t launch_moe_reduce(const void *fn, int grid, int block, int smem, const ReduceArgs &a,

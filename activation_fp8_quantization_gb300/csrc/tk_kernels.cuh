@@ -375,27 +375,25 @@ __device__ __forceinline__ float group_max(float v, int tpg_mask)
 // Scale the thread's 16 values (held negated, as 8 pairs) by 1/s, with s
 // from the group's amax, encode and store them; the group's first thread
 // also stores the scale.
+// The quotients y / s of one thread's 16 activations (given as -y pairs) and
+// the group's scale: s (fp32 mode) or the UE8M0 exponent k. The codes are the
+// format's round-to-nearest-even, saturating conversion of v.
 template <int OUT, int SCALE>
-__device__ __forceinline__ void quantize_store(const uint64_t (&ny)[kEPT / 2], float amax, int64_t row,
-                                               int col0, int group_idx, bool write_scale,
-                                               const RowShape &sh, const OutArgs &o)
+__device__ __forceinline__ void quantize_values(const uint64_t (&ny)[kEPT / 2], float amax,
+                                                uint64_t (&v)[kEPT / 2], float &s, int &k)
 {
-    uint64_t v[kEPT / 2];
     if (SCALE == kScaleUE8M0) {
-        const int k = ue8m0_exponent<OUT>(amax);
+        k = ue8m0_exponent<OUT>(amax);
         // -2^-k (k <= 126 here): the product is the exact power-of-two scaling
         const uint64_t ninv = splat(-__uint_as_float((uint32_t)(127 - k) << 23));
 #pragma unroll
         for (int i = 0; i < kEPT / 2; ++i)
             v[i] = mul2(ny[i], ninv);
-        if (write_scale)
-            static_cast<uint8_t *>(o.scales)[scale_index(sh, row, group_idx)] = (uint8_t)(k + 127);
     } else {
         // amax >= 2^-64 keeps s >= 2^-73 and every remainder above the
         // subnormal range, so both divisions can take the Markstein step;
         // smaller groups (a uniform branch, never taken by ordinary data) use
         // the IEEE division directly.
-        float s;
         if (amax >= 0x1p-64f) {
             s = div_markstein1(amax, Fmt<OUT>::kQmax, Fmt<OUT>::kRcpQmax);
             const uint64_t s2 = splat(s);
@@ -411,14 +409,42 @@ __device__ __forceinline__ void quantize_store(const uint64_t (&ny)[kEPT / 2], f
             for (int i = 0; i < kEPT / 2; ++i)
                 v[i] = pk(__fdiv_rn(-plo(ny[i]), s), __fdiv_rn(-phi(ny[i]), s));
         }
-        if (write_scale)
-            static_cast<float *>(o.scales)[scale_index(sh, row, group_idx)] = s;
     }
+}
+
+// Store the group's scale (fp32 s, or the UE8M0 byte k + 127) at its index.
+template <int SCALE>
+__device__ __forceinline__ void store_scale(const RowShape &sh, const OutArgs &o, int64_t row, int group_idx,
+                                            float s, int k)
+{
+    if (SCALE == kScaleUE8M0)
+        static_cast<uint8_t *>(o.scales)[scale_index(sh, row, group_idx)] = (uint8_t)(k + 127);
+    else
+        static_cast<float *>(o.scales)[scale_index(sh, row, group_idx)] = s;
+}
+
+// 16 quotients -> 16 E4M3 codes, column order, in four words
+__device__ __forceinline__ void e4m3_words(const uint64_t (&v)[kEPT / 2], uint32_t (&w)[4])
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        w[j] = cvt_e4m3x4(plo(v[2 * j]), phi(v[2 * j]), plo(v[2 * j + 1]), phi(v[2 * j + 1]));
+}
+
+template <int OUT, int SCALE>
+__device__ __forceinline__ void quantize_store(const uint64_t (&ny)[kEPT / 2], float amax, int64_t row,
+                                               int col0, int group_idx, bool write_scale,
+                                               const RowShape &sh, const OutArgs &o)
+{
+    uint64_t v[kEPT / 2];
+    float s = 0.0f;
+    int k = 0;
+    quantize_values<OUT, SCALE>(ny, amax, v, s, k);
+    if (write_scale)
+        store_scale<SCALE>(sh, o, row, group_idx, s, k);
     if (OUT == kOutE4M3) {
         uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            w[j] = cvt_e4m3x4(plo(v[2 * j]), phi(v[2 * j]), plo(v[2 * j + 1]), phi(v[2 * j + 1]));
+        e4m3_words(v, w);
         st_stream_128(o.q + row * (int64_t)sh.H + col0, w[0], w[1], w[2], w[3]);
     } else {
         const uint32_t w0 = cvt_e2m1x8(v[0], v[1], v[2], v[3]);

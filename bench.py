@@ -58,6 +58,8 @@ def parse_args(argv=None):
                    help="scale layout of the fused op (the host-buffer e2e leg needs row)")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--e2e-chunk-rows", type=int, default=2048)
+    p.add_argument("--transposed", action="store_true",
+                   help="fused workloads: write the codes transposed (tk_swiglu_quant_run_transposed)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--jsonl", default=None, help="also append the JSON line to this file")
@@ -328,6 +330,9 @@ def run_ours(args, dist: Dist):
 
     x0, w0 = wls.make_inputs(wl, "cuda")
     q_shape, s_shape, s_dtype = op.output_shapes(T)
+    transposed = args.transposed and wl.op == "swiglu"
+    if transposed:
+        q_shape = (wl.H, tk.tk_swiglu_quant_transposed_size(op.plan, T)[1])
     xs, ws, qs, ss = [], [], [], []
     for i in range(n_sets):
         xs.append(x0 if i == 0 else x0.clone())
@@ -346,6 +351,8 @@ def run_ours(args, dist: Dist):
         xp, wp, qp, spp = ptrs[i % n_sets]
         if wl.op == "cast":
             st = lib.tk_quant_cast_run(op.plan, T, xp, qp, spp, sh)
+        elif transposed:
+            st = lib.tk_swiglu_quant_run_transposed(op.plan, T, xp, wp, qp, spp, cp, sh)
         else:
             st = lib.tk_swiglu_quant_run(op.plan, T, xp, wp, qp, spp, cp, sh)
         if st != 0:
@@ -392,7 +399,7 @@ def run_ours(args, dist: Dist):
     peaks = measured_peaks()
 
     e2e = None
-    if not args.no_e2e and wl.op == "swiglu" and args.scale_layout == "row":
+    if not args.no_e2e and wl.op == "swiglu" and args.scale_layout == "row" and not transposed:
         e2e = measure_e2e(op, wl, x0, w0, dev, args, dist)
 
     cpu = None
@@ -403,9 +410,11 @@ def run_ours(args, dist: Dist):
                          % (r["rows"], wl.T, r["seconds"])}
     if dist.rank != 0:
         return 0
-    traffic = load_traffic(wl.name)
+    traffic = None if transposed else load_traffic(wl.name)
     kernel = None
-    if wl.op == "swiglu":
+    if transposed:
+        kernel = "transpose_quant_kernel"
+    elif wl.op == "swiglu":
         kernel = "warp_stream_kernel" if op.launch_info(T)["rows_per_cta"] == 0 else "row_quant_kernel"
     line = {
         "metric": metric_of(wl), "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
@@ -413,6 +422,7 @@ def run_ours(args, dist: Dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": {**config_of(wl, args.gpus), "scale_layout": args.scale_layout,
+                   "codes": "transposed [H, ld]" if transposed else "row-major [T, H]",
                    "l2": "inputs larger than L2: %d rotating input/output sets, %.0f MB" % (
                        n_sets, n_sets * per_set / 1e6)},
         "hbm_gbs": achieved,

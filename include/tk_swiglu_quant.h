@@ -139,6 +139,34 @@ tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t num_tokens,
                               const void *x, const float *topk_weights, void *q,
                               void *scales, int64_t *clamped_count, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Fused op with the codes written transposed
+ *
+ * "TileKernels从入门到精通" (zhichai.net/topic/177618752), closing section
+ * "结语：工程化极致的胜利": SwiGLU, the per-token quant and the transpose are
+ * fused into one kernel launch. The grouping (g consecutive columns of one
+ * row), the scales (in the plan's scale layout) and the codes are exactly
+ * those of tk_swiglu_quant_run; only the codes are stored transposed:
+ *
+ *     qt[i * ld + t] = code of row t, column i      (0 <= i < H, 0 <= t < T)
+ *
+ * with ld = T rounded up to a multiple of 16, so every row of qt starts
+ * 16-byte aligned; qt[i * ld + t] for T <= t < ld is written as 0. This is
+ * the operand layout of a following GEMM that contracts over the rows.
+ * Requires a plan with E4M3 codes, group_size 32, 64 or 128 and H % 128 == 0
+ * (TK_ERR_UNSUPPORTED otherwise). Arguments, alignment and errors are those
+ * of tk_swiglu_quant_run, with qt (H * ld bytes, 16-byte aligned) in place
+ * of q; the clamp counters are added to as there.
+ * ---------------------------------------------------------------------- */
+
+/* ld and the bytes of qt for num_tokens rows (host only). */
+tk_status tk_swiglu_quant_transposed_size(tk_swiglu_quant_plan_t plan, int64_t num_tokens, size_t *qt_bytes,
+                                          int64_t *ld);
+
+tk_status tk_swiglu_quant_run_transposed(tk_swiglu_quant_plan_t plan, int64_t num_tokens, const void *x,
+                                         const float *topk_weights, void *qt, void *scales,
+                                         int64_t *clamped_count, void *stream);
+
 /* Launch shape a run of num_tokens rows would use (host only): CTAs in the
  * persistent grid, threads per CTA, rows one CTA processes per iteration (0
  * when the warp-stream kernel runs: each warp then streams 512-column

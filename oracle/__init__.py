@@ -78,6 +78,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.tko_scale_ld.restype = c.c_int64
     lib.tko_scales_to_layout.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_int, c.c_int, c.c_void_p]
     lib.tko_scales_to_layout.restype = c.c_int
+    lib.tko_codes_transposed.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_int64, c.c_void_p]
+    lib.tko_codes_transposed.restype = c.c_int
     lib.tko_moe_reduce.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_int64, c.c_int64,
                                    c.c_void_p, c.c_void_p, c.c_int64, c.c_int64, c.c_float, c.c_void_p]
     lib.tko_moe_reduce.restype = c.c_int
@@ -178,6 +180,18 @@ def scales_to_layout(scales: np.ndarray, scale_fmt: str, layout: str, fill=0,
     rc = lib.tko_scales_to_layout(_ptr(scales), rows, groups, SCALE_FMTS[scale_fmt], code, _ptr(out))
     if rc != 0:
         raise ValueError("no such scale layout for these scales")
+    return out
+
+
+def codes_transposed(q: np.ndarray, ld: int, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Row-major codes q [rows, H] -> qt [H, ld] with qt[i, t] = q[t, i] and
+    zero padding for rows <= t < ld."""
+    lib = lib or load()
+    q = np.ascontiguousarray(q, np.uint8)
+    rows, hidden = q.shape
+    out = np.full((hidden, ld), 0xAB, np.uint8)   # every byte is written
+    if lib.tko_codes_transposed(_ptr(q), rows, hidden, ld, _ptr(out)) != 0:
+        raise ValueError("ld must be at least the number of rows")
     return out
 
 

@@ -365,6 +365,19 @@ int tko_scales_to_layout(const void *row_major, int64_t rows, int64_t groups, in
     return 0;
 }
 
+/* Codes stored transposed (the fused-transpose output of "TileKernels从入门到
+ * 精通", closing section): out[i * ld + t] = q[t * hidden + i] for t < rows,
+ * and 0 for rows <= t < ld. q is the row-major E4M3 code matrix [rows, hidden]. */
+int tko_codes_transposed(const uint8_t *q, int64_t rows, int64_t hidden, int64_t ld, uint8_t *out)
+{
+    if (ld < rows)
+        return -1;
+    for (int64_t i = 0; i < hidden; ++i)
+        for (int64_t t = 0; t < ld; ++t)
+            out[i * ld + t] = t < rows ? q[t * hidden + i] : 0;
+    return 0;
+}
+
 /* ------------------------------------------------------ top-k combine (reduce) */
 
 /* RNE of a double to bf16 (the upper half of an fp32), through fp32: a double

@@ -362,6 +362,20 @@ def pin_scale_layouts(lib):
     assert words[0, 2] == 0 and words[1, 3] == 0     # padding rows 2, 3 not written
 
 
+def pin_codes_transposed(lib):
+    # hand example: 2 rows x 3 columns, ld 4 -> column i holds rows 0, 1 then zeros
+    q = np.array([[1, 2, 3], [4, 5, 6]], np.uint8)
+    got = oracle.codes_transposed(q, 4, lib=lib)
+    assert got.tolist() == [[1, 4, 0, 0], [2, 5, 0, 0], [3, 6, 0, 0]]
+    # numpy's transpose into a zero-padded array
+    rng = np.random.default_rng(21)
+    for rows, ld in ((1, 16), (17, 32), (64, 64)):
+        q = rng.integers(0, 256, (rows, 48)).astype(np.uint8)
+        want = np.zeros((48, ld), np.uint8)
+        want[:, :rows] = q.T
+        assert np.array_equal(oracle.codes_transposed(q, ld, lib=lib), want), (rows, ld)
+
+
 def _bf16_to_f64(bits):
     return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
 
@@ -440,5 +454,6 @@ ALL_PINS = [
     pin_e2m1_packing,
     pin_quant_rows_indexing,
     pin_scale_layouts,
+    pin_codes_transposed,
     pin_moe_reduce,
 ]

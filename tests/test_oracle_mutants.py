@@ -37,6 +37,10 @@ MUTANTS = {
     "quotient_multiplied": ("float quotient = y[i] / s;", "float quotient = y[i] * s;"),
     "packed_byte_order": ("[4 * ((j / 4) * ld + t) + (j % 4)]", "[4 * ((j / 4) * ld + t) + (3 - j % 4)]"),
     "column_major_transposed": ("((float *)out)[j * ld + t] = v;", "((float *)out)[t * ld + j] = v;"),
+    "transposed_index_swapped": ("out[i * ld + t] = t < rows ? q[t * hidden + i] : 0;",
+                                 "out[i * ld + t] = t < rows ? q[i * rows + t] : 0;"),
+    "transposed_padding_kept": ("out[i * ld + t] = t < rows ? q[t * hidden + i] : 0;",
+                                "if (t < rows) out[i * ld + t] = q[t * hidden + i];"),
     "reduce_weight_dropped": ("acc += (double)w[t * K + k] * v;", "acc += v;"),
     "reduce_empty_slot_kept": ("if (r < 0)\n                    continue;", "if (r < 0)\n                    r = 0;"),
     "reduce_global_scale_dropped": ("bf16_rne_from_double((double)gs * acc)", "bf16_rne_from_double(acc)"),
