@@ -78,6 +78,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.tko_scale_ld.restype = c.c_int64
     lib.tko_scales_to_layout.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_int, c.c_int, c.c_void_p]
     lib.tko_scales_to_layout.restype = c.c_int
+    lib.tko_swiglu_backward.argtypes = [c.c_void_p, c.c_void_p, c.c_int64, c.c_int64, c.c_void_p, c.c_int,
+                                        c.c_float, c.c_void_p, c.c_void_p]
+    lib.tko_swiglu_backward.restype = c.c_int
     lib.tko_codes_transposed.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_int64, c.c_void_p]
     lib.tko_codes_transposed.restype = c.c_int
     lib.tko_moe_reduce.argtypes = [c.c_void_p, c.c_void_p, c.c_void_p, c.c_int64, c.c_int64,
@@ -181,6 +184,24 @@ def scales_to_layout(scales: np.ndarray, scale_fmt: str, layout: str, fill=0,
     if rc != 0:
         raise ValueError("no such scale layout for these scales")
     return out
+
+
+def swiglu_backward(x_bits: np.ndarray, dy_bits: np.ndarray, w: np.ndarray | None,
+                    clamp: float | None = None, lib: ctypes.CDLL | None = None):
+    """SwiGLU backward on bf16 bit patterns x [rows, 2H] and dy [rows, H]
+    (uint16); returns (dx bf16 bits [rows, 2H], dw float32 [rows])."""
+    lib = lib or load()
+    x_bits = np.ascontiguousarray(x_bits, np.uint16)
+    dy_bits = np.ascontiguousarray(dy_bits, np.uint16)
+    rows, two_h = x_bits.shape
+    assert dy_bits.shape == (rows, two_h // 2)
+    dx = np.zeros((rows, two_h), np.uint16)
+    dw = np.zeros(rows, np.float32)
+    wa = None if w is None else np.ascontiguousarray(w, np.float32)
+    if lib.tko_swiglu_backward(_ptr(x_bits), _ptr(dy_bits), rows, two_h // 2, _ptr(wa), int(clamp is not None),
+                               float(clamp or 0.0), _ptr(dx), _ptr(dw)) != 0:
+        raise ValueError("oracle rejected the sizes")
+    return dx, dw
 
 
 def codes_transposed(q: np.ndarray, ld: int, lib: ctypes.CDLL | None = None) -> np.ndarray:

@@ -365,6 +365,59 @@ int tko_scales_to_layout(const void *row_major, int64_t rows, int64_t groups, in
     return 0;
 }
 
+/* SwiGLU backward (not on the pages; the plain derivation of the forward
+ * above). With g' = min(g, L), u' = clamp(u, -L, L) when clamping is on,
+ * s = sigmoid(g'), silu(g') = g' s and silu'(g') = s (1 + g' (1 - s)):
+ *   dgate = dy * w * u' * silu'(g')   where g <= L, else 0
+ *   dup   = dy * w * silu(g')         where |u| <= L, else 0
+ *   dw    = sum_i dy_i * silu(g'_i) * u'_i
+ * all in double; dx [rows, 2*hidden] (gate half first) rounded once to bf16
+ * (nearest even), dw [rows] rounded once to fp32 (may be NULL). x and dy are
+ * bf16 bit patterns; w may be NULL (weight 1). A clamped element's gradient
+ * is +0. Returns 0, or -1 on bad sizes. */
+static uint16_t bf16_rne_from_double(double v);
+
+int tko_swiglu_backward(const uint16_t *x, const uint16_t *dy, int64_t rows, int64_t hidden, const float *w,
+                        int use_clamp, float clamp_limit, uint16_t *dx, float *dw)
+{
+    if (rows < 0 || hidden <= 0)
+        return -1;
+    double lim = (double)clamp_limit;
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *xr = x + r * 2 * hidden;
+        double wr = w ? (double)w[r] : 1.0;
+        double acc = 0.0;
+        for (int64_t i = 0; i < hidden; ++i) {
+            double g = bf16_to_double(xr[i]);
+            double u = bf16_to_double(xr[hidden + i]);
+            double d = bf16_to_double(dy[r * hidden + i]);
+            int pass_g = 1, pass_u = 1;
+            if (use_clamp) {
+                if (g > lim) {
+                    g = lim;
+                    pass_g = 0;
+                }
+                if (u > lim) {
+                    u = lim;
+                    pass_u = 0;
+                } else if (u < -lim) {
+                    u = -lim;
+                    pass_u = 0;
+                }
+            }
+            double sig = 1.0 / (1.0 + exp(-g));
+            double silu = g * sig;
+            double dsilu = sig * (1.0 + g * (1.0 - sig));
+            dx[r * 2 * hidden + i] = bf16_rne_from_double(pass_g ? d * wr * u * dsilu : 0.0);
+            dx[r * 2 * hidden + hidden + i] = bf16_rne_from_double(pass_u ? d * wr * silu : 0.0);
+            acc += d * silu * u;
+        }
+        if (dw)
+            dw[r] = (float)acc;
+    }
+    return 0;
+}
+
 /* Codes stored transposed (the fused-transpose output of "TileKernels从入门到
  * 精通", closing section): out[i * ld + t] = q[t * hidden + i] for t < rows,
  * and 0 for rows <= t < ld. q is the row-major E4M3 code matrix [rows, hidden]. */

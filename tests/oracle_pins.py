@@ -376,6 +376,64 @@ def pin_codes_transposed(lib):
         assert np.array_equal(oracle.codes_transposed(q, ld, lib=lib), want), (rows, ld)
 
 
+def _ulp(v, mant_bits):
+    v = np.maximum(np.abs(v), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(v)) - mant_bits)
+
+
+def pin_swiglu_backward(lib):
+    from scipy.special import expit
+    # hand-worked, L = 7, w = 0.5: column 0 has g = 0, u = 2, dy = 1:
+    # sigmoid(0) = 1/2, silu = 0, silu' = 1/2 -> dgate = 1 * 0.5 * 2 * 0.5 = 0.5
+    # (bf16 0x3F00), dup = 0; column 1 has g = 8 > L (clamped, so dgate = 0),
+    # u = 1, dy = 2 -> dup = 2 * 0.5 * silu(7), silu(7) = 7 * expit(7) = 6.99362,
+    # nearest bf16 7.0 (0x40E0); dw = 2 * silu(7) * 1 = 13.98724.
+    x = np.array([[0x0000, 0x4100, 0x4000, 0x3F80]], np.uint16)     # g = (0, 8), u = (2, 1)
+    dy = np.array([[0x3F80, 0x4000]], np.uint16)                     # (1, 2)
+    dx, dw = oracle.swiglu_backward(x, dy, np.array([0.5], np.float32), clamp=7.0, lib=lib)
+    assert dx.tolist() == [[0x3F00, 0x0000, 0x0000, 0x40E0]], [hex(v) for v in dx[0]]
+    assert abs(float(dw[0]) - 2 * 7 * expit(7.0)) <= 2e-6
+    # central differences of an independent forward (scipy's expit), in float64,
+    # for the gate, the up half and the weight, with and without clamping
+    rng = np.random.default_rng(31)
+    rows, H = 3, 64
+    for L in (None, 1.5):
+        g = rng.normal(0, 2, (rows, H))
+        u = rng.normal(0, 1.5, (rows, H))
+        if L is not None:   # keep every value away from the clamp's kink
+            g = np.where(np.abs(g - L) < 0.05, g + 0.2, g)
+            u = np.where(np.abs(np.abs(u) - L) < 0.05, u * 1.1, u)
+        xb = _bf16_bits(np.concatenate([g, u], axis=1))
+        db = _bf16_bits(rng.normal(0, 1, (rows, H)))
+        wv = rng.uniform(0.1, 1.0, rows).astype(np.float32)
+        dx, dw = oracle.swiglu_backward(xb, db, wv, clamp=L, lib=lib)
+        xv, dv = _bf16_to_f64(xb), _bf16_to_f64(db)
+        gv, uv, w64 = xv[:, :H], xv[:, H:], wv.astype(np.float64)[:, None]
+
+        def F(gg, uu, ww):   # the loss sum(dy * y) of the forward, per element
+            if L is not None:
+                gg = np.minimum(gg, L)
+                uu = np.clip(uu, -L, L)
+            return dv * gg * expit(gg) * uu * ww
+
+        hg = 1e-6 * np.maximum(1.0, np.abs(gv))
+        hu = 1e-6 * np.maximum(1.0, np.abs(uv))
+        fd_g = (F(gv + hg, uv, w64) - F(gv - hg, uv, w64)) / (2 * hg)
+        fd_u = (F(gv, uv + hu, w64) - F(gv, uv - hu, w64)) / (2 * hu)
+        fd_w = (F(gv, uv, w64 + 1e-3) - F(gv, uv, w64 - 1e-3)).sum(axis=1) / 2e-3
+        got = _bf16_to_f64(dx)
+        for name, want, have in (("gate", fd_g, got[:, :H]), ("up", fd_u, got[:, H:])):
+            tol = 0.5 * _ulp(want, 7) * (1 + 1e-6) + 1e-9 * np.abs(want) + 1e-30
+            assert (np.abs(have - want) <= tol).all(), (name, L, np.abs(have - want).max())
+        scale = np.abs(F(gv, uv, 1.0)).sum(axis=1)
+        tol = 0.5 * _ulp(fd_w, 23) * (1 + 1e-6) + 1e-9 * scale
+        assert (np.abs(dw.astype(np.float64) - fd_w) <= tol).all(), (L, np.abs(dw - fd_w).max())
+    # no weights: w = 1
+    dx1, dw1 = oracle.swiglu_backward(xb, db, None, clamp=L, lib=lib)
+    dxw, dww = oracle.swiglu_backward(xb, db, np.ones(rows, np.float32), clamp=L, lib=lib)
+    assert np.array_equal(dx1, dxw) and np.array_equal(dw1, dww)
+
+
 def _bf16_to_f64(bits):
     return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
 
@@ -455,5 +513,6 @@ ALL_PINS = [
     pin_quant_rows_indexing,
     pin_scale_layouts,
     pin_codes_transposed,
+    pin_swiglu_backward,
     pin_moe_reduce,
 ]

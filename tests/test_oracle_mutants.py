@@ -41,6 +41,13 @@ MUTANTS = {
                                  "out[i * ld + t] = t < rows ? q[i * rows + t] : 0;"),
     "transposed_padding_kept": ("out[i * ld + t] = t < rows ? q[t * hidden + i] : 0;",
                                 "if (t < rows) out[i * ld + t] = q[t * hidden + i];"),
+    "backward_dsilu_drops_one_minus_sigmoid": ("dsilu = sig * (1.0 + g * (1.0 - sig));",
+                                               "dsilu = sig * (1.0 + g * sig);"),
+    "backward_dsilu_sign": ("dsilu = sig * (1.0 + g * (1.0 - sig));", "dsilu = sig * (1.0 - g * (1.0 - sig));"),
+    "backward_gate_mask_ignored": ("pass_g ? d * wr * u * dsilu : 0.0", "d * wr * u * dsilu"),
+    "backward_up_mask_ignored": ("pass_u ? d * wr * silu : 0.0", "d * wr * silu"),
+    "backward_dw_drops_up": ("acc += d * silu * u;", "acc += d * silu;"),
+    "backward_weight_dropped": ("pass_g ? d * wr * u * dsilu : 0.0", "pass_g ? d * u * dsilu : 0.0"),
     "reduce_weight_dropped": ("acc += (double)w[t * K + k] * v;", "acc += v;"),
     "reduce_empty_slot_kept": ("if (r < 0)\n                    continue;", "if (r < 0)\n                    r = 0;"),
     "reduce_global_scale_dropped": ("bf16_rne_from_double((double)gs * acc)", "bf16_rne_from_double(acc)"),
