@@ -18,7 +18,8 @@ import threading
 
 from . import _abi
 from ._abi import (IN_DTYPES, OUT_FMTS, REDUCE_IN_FMTS, SCALE_FMTS, SCALE_LAYOUTS, MoeReduceDesc,
-                   QuantCastDesc, SwigluQuantDesc, tk_moe_reduce_plan, tk_moe_reduce_plan_destroy,
+                   QuantCastDesc, SwigluBackwardDesc, SwigluQuantDesc, tk_swiglu_backward_plan,
+                   tk_swiglu_backward_plan_destroy, tk_swiglu_backward_run, tk_swiglu_backward_validate, tk_moe_reduce_plan, tk_moe_reduce_plan_destroy,
                    tk_moe_reduce_launch_info, tk_moe_reduce_run, tk_moe_reduce_validate,
                    TkError, tk_fault_word, tk_last_error_message, tk_quant_cast_output_sizes,
                    tk_quant_cast_plan, tk_quant_cast_plan_destroy,
@@ -31,7 +32,9 @@ from ._abi import (IN_DTYPES, OUT_FMTS, REDUCE_IN_FMTS, SCALE_FMTS, SCALE_LAYOUT
                    tk_swiglu_quant_validate)
 
 __all__ = [
-    "SwigluQuant", "HostPipe", "QuantCast", "MoeReduce", "swiglu_quant", "quant_cast", "TkError",
+    "SwigluQuant", "HostPipe", "QuantCast", "MoeReduce", "SwigluBackward", "swiglu_quant", "quant_cast",
+    "TkError", "SwigluBackwardDesc", "tk_swiglu_backward_validate", "tk_swiglu_backward_plan",
+    "tk_swiglu_backward_plan_destroy", "tk_swiglu_backward_run",
     "MoeReduceDesc", "tk_moe_reduce_validate", "tk_moe_reduce_plan", "tk_moe_reduce_plan_destroy",
     "tk_moe_reduce_run", "tk_moe_reduce_launch_info",
     "tk_swiglu_quant_host_pipe_create", "tk_swiglu_quant_host_pipe_destroy",
@@ -278,6 +281,78 @@ class QuantCast:
         with torch.cuda.device(x.device):
             tk_quant_cast_run(self.plan, T, x, q, scales, stream.cuda_stream)
         return q, scales
+
+
+class SwigluBackward:
+    """A plan for the SwiGLU backward (tk_swiglu_backward_plan). With
+    ``recompute`` = dict(group_size=..., scale_fmt=..., out_fmt=..., scale_layout=...)
+    it also writes the forward's codes and scales."""
+
+    def __init__(self, hidden: int, topk_weights: bool = True, clamp_limit: float | None = None,
+                 recompute: dict | None = None, device: int | None = None):
+        torch = _torch()
+        self.hidden = int(hidden)
+        self.has_w = bool(topk_weights)
+        self.clamp_limit = clamp_limit
+        self.recompute = dict(recompute) if recompute else None
+        r = self.recompute or {}
+        self.group_size = int(r.get("group_size", 128)) if r else 0
+        self.scale_fmt = r.get("scale_fmt", "fp32")
+        self.out_fmt = r.get("out_fmt", "e4m3")
+        self.scale_layout = r.get("scale_layout", "row")
+        self.desc = SwigluBackwardDesc(self.hidden, int(self.has_w), int(clamp_limit is not None),
+                                       float(clamp_limit or 0.0), int(bool(r)), self.group_size,
+                                       SCALE_FMTS[self.scale_fmt], OUT_FMTS[self.out_fmt],
+                                       SCALE_LAYOUTS[self.scale_layout])
+        self.device = torch.cuda.current_device() if device is None else int(device)
+        self.plan = tk_swiglu_backward_plan(self.desc, self.device)
+
+    def __del__(self):
+        plan = getattr(self, "plan", None)
+        if plan:
+            try:
+                tk_swiglu_backward_plan_destroy(plan)
+            except Exception:
+                pass
+            self.plan = None
+
+    def __call__(self, x, dy, topk_weights=None, *, want_dw: bool = True, dx=None, dw=None, q=None,
+                 scales=None, stream=None):
+        """Returns (dx [T, 2H] bf16, dw [T] fp32 or None, q, scales) (q, scales
+        None unless the plan recomputes the codes)."""
+        torch = _torch()
+        T = x.shape[0]
+        _check_cuda(x, "x", torch.bfloat16, (T, 2 * self.hidden))
+        _check_cuda(dy, "dy", torch.bfloat16, (T, self.hidden))
+        if self.has_w:
+            if topk_weights is None:
+                raise ValueError("this op was planned with top-k weights")
+            _check_cuda(topk_weights, "topk_weights", torch.float32, (T,))
+        else:
+            topk_weights = None
+        if dx is None:
+            dx = torch.empty((T, 2 * self.hidden), dtype=torch.bfloat16, device=x.device)
+        _check_cuda(dx, "dx", torch.bfloat16, (T, 2 * self.hidden))
+        if want_dw and dw is None:
+            dw = torch.empty((T,), dtype=torch.float32, device=x.device)
+        if dw is not None:
+            _check_cuda(dw, "dw", torch.float32, (T,))
+        if self.recompute:
+            q_shape, s_shape, s_dtype = _out_shapes(T, self.hidden, self.group_size, self.scale_fmt,
+                                                    self.out_fmt, self.scale_layout)
+            if q is None:
+                q = torch.empty(q_shape, dtype=torch.uint8, device=x.device)
+            _check_cuda(q, "q", torch.uint8, q_shape)
+            if scales is None:
+                scales = torch.empty(s_shape, dtype=s_dtype, device=x.device)
+            _check_cuda(scales, "scales", s_dtype, s_shape)
+        else:
+            q = scales = None
+        if stream is None:
+            stream = torch.cuda.current_stream(x.device)
+        with torch.cuda.device(x.device):
+            tk_swiglu_backward_run(self.plan, T, x, topk_weights, dy, dx, dw, q, scales, stream.cuda_stream)
+        return dx, dw, q, scales
 
 
 class MoeReduce:

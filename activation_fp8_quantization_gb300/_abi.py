@@ -39,6 +39,13 @@ class QuantCastDesc(ctypes.Structure):
                 ("in_dtype", ctypes.c_int32), ("scale_layout", ctypes.c_int32)]
 
 
+class SwigluBackwardDesc(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int64), ("has_topk_weights", ctypes.c_int32),
+                ("use_clamp", ctypes.c_int32), ("clamp_limit", ctypes.c_float),
+                ("recompute_quant", ctypes.c_int32), ("group_size", ctypes.c_int32),
+                ("scale_fmt", ctypes.c_int32), ("out_fmt", ctypes.c_int32), ("scale_layout", ctypes.c_int32)]
+
+
 class MoeReduceDesc(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int64), ("topk", ctypes.c_int32), ("in_fmt", ctypes.c_int32)]
 
@@ -84,6 +91,11 @@ SIGNATURES = {
                                          ctypes.c_float, _VP, _VP]),
     "tk_moe_reduce_launch_info": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _PINT, _PINT, _PINT,
                                                  _PINT]),
+    "tk_swiglu_backward_validate": (ctypes.c_int, [ctypes.POINTER(SwigluBackwardDesc)]),
+    "tk_swiglu_backward_plan": (ctypes.c_int, [ctypes.POINTER(SwigluBackwardDesc), ctypes.c_int,
+                                               ctypes.POINTER(_VP)]),
+    "tk_swiglu_backward_plan_destroy": (ctypes.c_int, [_VP]),
+    "tk_swiglu_backward_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "tk_fault_word": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
     "tk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tk_last_error_message": (ctypes.c_char_p, []),
@@ -263,6 +275,26 @@ def tk_moe_reduce_launch_info(plan: int, num_tokens: int, y=None, y_scale=None) 
                                           *[ctypes.byref(x) for x in v]))
     return {"kernel": ("regs", "bulk")[v[0].value], "grid": v[1].value, "block": v[2].value,
             "smem_bytes": v[3].value}
+
+
+def tk_swiglu_backward_validate(desc: SwigluBackwardDesc) -> int:
+    return lib().tk_swiglu_backward_validate(ctypes.byref(desc))
+
+
+def tk_swiglu_backward_plan(desc: SwigluBackwardDesc, device: int) -> int:
+    h = _VP()
+    check(lib().tk_swiglu_backward_plan(ctypes.byref(desc), device, ctypes.byref(h)))
+    return h.value
+
+
+def tk_swiglu_backward_plan_destroy(plan: int) -> None:
+    check(lib().tk_swiglu_backward_plan_destroy(plan))
+
+
+def tk_swiglu_backward_run(plan: int, num_tokens: int, x, topk_weights, dy, dx, dw, q, scales,
+                           stream: int | None) -> None:
+    check(lib().tk_swiglu_backward_run(plan, num_tokens, _ptr(x), _ptr(topk_weights), _ptr(dy), _ptr(dx),
+                                       _ptr(dw), _ptr(q), _ptr(scales), stream))
 
 
 def tk_fault_word(device: int, clear: bool = False) -> int:

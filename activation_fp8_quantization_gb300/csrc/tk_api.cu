@@ -1193,6 +1193,156 @@ TK_API tk_status tk_moe_reduce_launch_info(tk_moe_reduce_plan_t plan, int64_t nu
     return ok();
 }
 
+// ------------------------------------------------------------------ backward
+
+struct tk_swiglu_backward_plan_s {
+    tk_swiglu_backward_desc desc;
+    int device;
+    const void *fn;
+    int block, tpr, rpc, tpg_log2, groups, max_grid;
+    unsigned *fault;
+};
+
+TK_API tk_status tk_swiglu_backward_validate(const tk_swiglu_backward_desc *d)
+{
+    if (!d)
+        return fail(TK_ERR_INVALID_ARG, "desc is NULL");
+    const int64_t H = d->hidden;
+    if (H <= 0)
+        return fail(TK_ERR_INVALID_ARG, "hidden must be positive (got %lld)", (long long)H);
+    const bool small = H == 16 || H == 32 || H == 64 || H == 128 || H == 256;
+    if (!small && !(H % 512 == 0 && H <= 8192))
+        return fail(TK_ERR_UNSUPPORTED, "hidden must be 16, 32, 64, 128, 256 or a multiple of 512 up to 8192 "
+                                        "(got %lld)", (long long)H);
+    if (!is_flag(d->has_topk_weights) || !is_flag(d->use_clamp) || !is_flag(d->recompute_quant))
+        return fail(TK_ERR_INVALID_ARG, "has_topk_weights, use_clamp and recompute_quant must be 0 or 1");
+    if (d->use_clamp && !(d->clamp_limit > 0.0f && std::isfinite(d->clamp_limit)))
+        return fail(TK_ERR_INVALID_ARG, "clamp_limit must be finite and > 0");
+    if (d->recompute_quant) {
+        if (d->group_size == 0)
+            return fail(TK_ERR_UNSUPPORTED, "the recompute needs group_size 16 ... 512 (no per-token scale)");
+        tk_swiglu_quant_desc f{};
+        f.hidden = H;
+        f.group_size = d->group_size;
+        f.scale_fmt = d->scale_fmt;
+        f.out_fmt = d->out_fmt;
+        f.has_topk_weights = d->has_topk_weights;
+        f.use_clamp = d->use_clamp;
+        f.clamp_limit = d->clamp_limit;
+        f.count_clamped = 0;
+        f.scale_layout = d->scale_layout;
+        return tk_swiglu_quant_validate(&f);
+    }
+    return ok();
+}
+
+TK_API tk_status tk_swiglu_backward_plan(const tk_swiglu_backward_desc *d, int device, tk_swiglu_backward_plan_t *plan)
+{
+    if (!plan)
+        return fail(TK_ERR_INVALID_ARG, "plan output pointer is NULL");
+    *plan = nullptr;
+    tk_status st = tk_swiglu_backward_validate(d);
+    if (st != TK_OK)
+        return st;
+    int count = 0;
+    cudaError_t e = cudaGetDeviceCount(&count);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDeviceCount");
+    if (device < 0 || device >= count)
+        return fail(TK_ERR_INVALID_ARG, "device %d out of range (%d devices)", device, count);
+    DeviceScope scope(device);
+    if (scope.err != cudaSuccess)
+        return cuda_fail(scope.err, "cudaSetDevice");
+    tk_swiglu_backward_plan_s p{};
+    p.desc = *d;
+    p.device = device;
+    p.fn = tk::backward_kernel_fn(d->use_clamp != 0, d->recompute_quant != 0, d->out_fmt, d->scale_fmt);
+    p.tpr = (int)(d->hidden / tk::kEPT);
+    p.rpc = p.tpr >= 256 ? 1 : 256 / p.tpr;
+    p.block = ((p.tpr * p.rpc + 31) / 32) * 32;   // <= 512 for hidden <= 8192
+    if (d->recompute_quant) {
+        p.tpg_log2 = ilog2(d->group_size / tk::kEPT);
+        p.groups = (int)(d->hidden / d->group_size);
+    }
+    int num_sms = 0, occ = 0;
+    void *fault = nullptr;
+    e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, p.fn, p.block, 0);
+    if (e == cudaSuccess)
+        e = cudaGetSymbolAddress(&fault, g_tk_fault_word);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "querying the device");
+    if (occ < 1)
+        return fail(TK_ERR_UNSUPPORTED, "kernel cannot be resident with %d threads per CTA", p.block);
+    p.max_grid = occ * num_sms;
+    p.fault = static_cast<unsigned *>(fault);
+    auto *h = new (std::nothrow) tk_swiglu_backward_plan_s(p);
+    if (!h)
+        return fail(TK_ERR_INVALID_ARG, "out of host memory");
+    *plan = h;
+    return ok();
+}
+
+TK_API tk_status tk_swiglu_backward_plan_destroy(tk_swiglu_backward_plan_t plan)
+{
+    delete plan;
+    return ok();
+}
+
+TK_API tk_status tk_swiglu_backward_run(tk_swiglu_backward_plan_t plan, int64_t T, const void *x,
+                                        const float *topk_weights, const void *dy, void *dx, float *dw, void *q,
+                                        void *scales, void *stream)
+{
+    if (!plan)
+        return fail(TK_ERR_INVALID_ARG, "plan is NULL");
+    if (T < 0)
+        return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)T);
+    if (T == 0)
+        return ok();
+    const tk_swiglu_backward_desc &d = plan->desc;
+    if (!x || !dy || !dx)
+        return fail(TK_ERR_INVALID_ARG, "x, dy and dx must be non-NULL");
+    if (d.has_topk_weights && !topk_weights)
+        return fail(TK_ERR_INVALID_ARG, "the plan expects topk_weights");
+    if (d.recompute_quant && (!q || !scales))
+        return fail(TK_ERR_INVALID_ARG, "the plan recomputes the codes: q and scales must be non-NULL");
+    if (!aligned(x, 32) || !aligned(dy, 32))
+        return fail(TK_ERR_MISALIGNED, "x and dy must be 32-byte aligned");
+    if (!aligned(dx, 16))
+        return fail(TK_ERR_MISALIGNED, "dx must be 16-byte aligned");
+    if ((dw && !aligned(dw, 4)) || (d.has_topk_weights && !aligned(topk_weights, 4)))
+        return fail(TK_ERR_MISALIGNED, "dw and topk_weights must be 4-byte aligned");
+    if (d.recompute_quant) {
+        if (!aligned(q, 16))
+            return fail(TK_ERR_MISALIGNED, "q must be 16-byte aligned");
+        if ((d.scale_fmt == TK_SCALE_FP32 && !aligned(scales, 4)) ||
+            (d.scale_layout != TK_SCALE_ROW_MAJOR && !aligned(scales, 16)))
+            return fail(TK_ERR_MISALIGNED, "scales must be 4-byte (fp32) or 16-byte (column-major) aligned");
+    }
+    tk_status st = check_current_device(plan->device);
+    if (st != TK_OK)
+        return st;
+    tk::BackwardArgs a{};
+    a.x = static_cast<const uint16_t *>(x);
+    a.dy = static_cast<const uint16_t *>(dy);
+    a.w = d.has_topk_weights ? topk_weights : nullptr;
+    a.dx = static_cast<uint16_t *>(dx);
+    a.dw = dw;
+    a.limit = d.use_clamp ? d.clamp_limit : 0.0f;
+    a.H = (int32_t)d.hidden;
+    tk::OutArgs o{static_cast<uint8_t *>(q), scales};
+    const int32_t layout = d.recompute_quant ? d.scale_layout : TK_SCALE_ROW_MAJOR;
+    const tk::RowShape sh{T, (int32_t)d.hidden, plan->tpr, plan->tpg_log2, plan->rpc, plan->groups, 0, 0,
+                          plan->fault, layout, scale_ld(layout, d.scale_fmt, T)};
+    const int64_t nrb = (T + plan->rpc - 1) / plan->rpc;
+    const int grid = (int)(nrb < plan->max_grid ? nrb : plan->max_grid);
+    cudaError_t e = tk::launch_backward(plan->fn, grid, plan->block, a, o, sh, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launch of the backward kernel");
+    return ok();
+}
+
 // ---------------------------------------------------------------- diagnostics
 
 TK_API tk_status tk_fault_word(int device, uint32_t *value, int clear)

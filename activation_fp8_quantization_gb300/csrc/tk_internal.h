@@ -78,6 +78,20 @@ int transpose_threads();
 cudaError_t launch_transpose(const void *fn, int grid, const SwigluArgs &a, const OutArgs &o, const RowShape &sh,
                              int64_t ldq, cudaStream_t stream);
 
+// SwiGLU backward (optionally recomputing the forward's codes and scales).
+struct BackwardArgs {
+    const uint16_t *x;    // [T, 2H] bf16, gate half first
+    const uint16_t *dy;   // [T, H] bf16
+    const float *w;       // [T] or null (weight 1)
+    uint16_t *dx;         // [T, 2H] bf16: dgate, then dup
+    float *dw;            // [T] or null
+    float limit;          // clamp limit (clamping instantiations)
+    int32_t H;
+};
+const void *backward_kernel_fn(bool clamp, bool recompute, int out_fmt, int scale_fmt);
+cudaError_t launch_backward(const void *fn, int grid, int block, const BackwardArgs &a, const OutArgs &o,
+                            const RowShape &sh, cudaStream_t stream);
+
 const void *moe_reduce_kernel_fn(int in_fmt);
 const void *moe_reduce_bulk_kernel_fn(int in_fmt);
 cudaError_t launch_moe_reduce(const void *fn, int grid, int block, int smem, const ReduceArgs &a,

@@ -50,6 +50,11 @@ class Workload:
             row = 2 * self.H if self.in_dtype == "bf16" else self.H + 4 * (self.H // 128)
             used = round(T * self.topk * (1.0 - self.empty_frac))
             return used * row + 8 * T * self.topk + 2 * T * self.H
+        if self.op == "backward":
+            # x and dy read, dx and dw written, the recomputed codes and scales written
+            q = T * self.H if self.out_fmt == "e4m3" else T * self.H // 2
+            s = T * self.groups_per_row * (4 if self.scale_fmt == "fp32" else 1)
+            return T * (4 * self.H + 2 * self.H + 4 * self.H + 4 + (4 if self.w_dist else 0)) + q + s
         x = T * self.x_cols * (4 if self.in_dtype == "fp32" else 2)
         q = T * self.H if self.out_fmt == "e4m3" else T * self.H // 2
         s = T * self.groups_per_row * (4 if self.scale_fmt == "fp32" else 1)
@@ -103,7 +108,17 @@ REDUCE_WORKLOADS = {
                                            "normal", seed=3002, op="reduce", in_dtype="e4m3", topk=8,
                                            empty_frac=0.01),
 }
-ALL_WORKLOADS = {**WORKLOADS, **CAST_WORKLOADS, **REDUCE_WORKLOADS}
+# The SwiGLU backward with the forward's codes recomputed: x and w as the
+# fused workloads of the same shape, dy ~ N(0, 1) in bf16.
+BACKWARD_WORKLOADS = {
+    "bwd_T8192_H2048_g128": Workload("bwd_T8192_H2048_g128", 8192, 2048, 128, "fp32", "e4m3", "row_lognormal",
+                                     w_dist="topk8_norm", seed=4001, op="backward"),
+    "bwd_T32768_H2048_g128_ue8m0_clamp7": Workload("bwd_T32768_H2048_g128_ue8m0_clamp7", 32768, 2048, 128,
+                                                   "ue8m0", "e4m3", "outliers", w_dist="topk8_norm", clamp=7.0,
+                                                   seed=4002, op="backward"),
+}
+
+ALL_WORKLOADS = {**WORKLOADS, **CAST_WORKLOADS, **REDUCE_WORKLOADS, **BACKWARD_WORKLOADS}
 
 _CHUNK_ROWS = 4096
 
@@ -151,6 +166,20 @@ def make_inputs(wl: Workload, device: str | torch.device = "cpu"):
 def bf16_bits(x: torch.Tensor):
     """View a bf16 tensor's bit patterns as a numpy uint16 array (host copy)."""
     return x.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def make_backward_inputs(wl: Workload, device: str | torch.device = "cpu"):
+    """(x, w, dy) of a backward workload: x and w as make_inputs draws them for
+    the same shape and seed, dy [T, H] bf16 N(0, 1) from seed + 1."""
+    x, w = make_inputs(Workload(**{**wl.__dict__, "op": "swiglu"}), device)
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(wl.seed + 1)
+    dy = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device)
+    for r0 in range(0, wl.T, _CHUNK_ROWS):
+        r1 = min(wl.T, r0 + _CHUNK_ROWS)
+        dy[r0:r1] = torch.randn((r1 - r0, wl.H), generator=gen, device=device).to(torch.bfloat16)
+    return x, w, dy
 
 
 def make_reduce_inputs(wl: Workload, device: str | torch.device = "cpu") -> dict:

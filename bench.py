@@ -211,6 +211,9 @@ def cpu_inputs(wl):
     from activation_fp8_quantization_gb300 import workloads as wls
     if wl.op == "reduce":
         return wls.make_reduce_inputs(wl, "cpu"), None
+    if wl.op == "backward":
+        x, w, dy = wls.make_backward_inputs(wl, "cpu")
+        return x, (w, dy)
     return wls.make_inputs(wl, "cpu")
 
 
@@ -219,6 +222,14 @@ def oracle_step(wl, x, w, lib):
     import oracle
     from activation_fp8_quantization_gb300 import workloads as wls
 
+    if wl.op == "backward":
+        xb, db = wls.bf16_bits(x), wls.bf16_bits(w[1])
+        wv = w[0].numpy()
+
+        def step():
+            oracle.swiglu_backward(xb, db, wv, clamp=wl.clamp, lib=lib)
+            oracle.swiglu_quant(xb, wv, wl.group, wl.scale_fmt, wl.out_fmt, clamp=wl.clamp, lib=lib)
+        return step
     if wl.op == "reduce":
         d = x
         pos, wt = d["pos"].numpy(), d["w"].numpy()
@@ -285,6 +296,8 @@ def config_of(wl, n: int) -> dict:
 
 
 def metric_of(wl) -> str:
+    if wl.op == "backward":
+        return "tokens/s and achieved HBM GB/s (fraction of GB300 peak) for the SwiGLU backward with FP8 recompute"
     if wl.op == "reduce":
         return "tokens/s and achieved HBM GB/s (fraction of GB300 peak) for the weighted top-k combine"
     if wl.op == "cast":
@@ -327,6 +340,8 @@ def run_ours(args, dist: Dist):
     n_sets = max(2, -(-3 * L2_BYTES // per_set) + 1)   # sets beyond the current one hold > 3x L2
     if wl.op == "reduce":
         return run_reduce(args, dist, wl, dev, n_sets)
+    if wl.op == "backward":
+        return run_backward(args, dist, wl, dev, n_sets)
 
     x0, w0 = wls.make_inputs(wl, "cuda")
     q_shape, s_shape, s_dtype = op.output_shapes(T)
@@ -531,6 +546,72 @@ def run_reduce(args, dist, wl, dev, n_sets):
                      "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(wl.name),
                      "kernel": "moe_reduce_%s" % ("bulk_kernel" if info["kernel"] == "bulk" else "kernel"),
                      "peak_source": peaks["source"], "algo_bytes_per_launch": algo},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clk,
+    }
+    emit(line, args)
+    return 0
+
+
+def run_backward(args, dist, wl, dev, n_sets):
+    """The SwiGLU backward (dx, dw and the recomputed codes and scales) over
+    rotating input/output sets."""
+    import torch
+    import activation_fp8_quantization_gb300 as tk
+    from activation_fp8_quantization_gb300 import _abi
+    from activation_fp8_quantization_gb300 import workloads as wls
+
+    op = tk.SwigluBackward(wl.H, True, wl.clamp, recompute=dict(group_size=wl.group, scale_fmt=wl.scale_fmt,
+                                                                out_fmt=wl.out_fmt, scale_layout=args.scale_layout))
+    T = wl.T
+    x0, w0, dy0 = wls.make_backward_inputs(wl, "cuda")
+    q_shape, s_shape, s_dtype = tk._out_shapes(T, wl.H, wl.group, wl.scale_fmt, wl.out_fmt, args.scale_layout)
+    sets = []
+    for i in range(n_sets):
+        sets.append(dict(
+            x=x0 if i == 0 else x0.clone(), w=w0 if i == 0 else w0.clone(), dy=dy0 if i == 0 else dy0.clone(),
+            dx=torch.empty((T, 2 * wl.H), dtype=torch.bfloat16, device=dev),
+            dw=torch.empty((T,), dtype=torch.float32, device=dev),
+            q=torch.empty(q_shape, dtype=torch.uint8, device=dev),
+            s=torch.empty(s_shape, dtype=s_dtype, device=dev)))
+    ptrs = [tuple(d[k].data_ptr() for k in ("x", "w", "dy", "dx", "dw", "q", "s")) for d in sets]
+    lib = _abi.lib()
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+
+    def launch(i):
+        xp, wp, dyp, dxp, dwp, qp, sp = ptrs[i % n_sets]
+        st = lib.tk_swiglu_backward_run(op.plan, T, xp, wp, dyp, dxp, dwp, qp, sp, sh)
+        if st != 0:
+            raise tk.TkError(st, _abi.tk_last_error_message())
+
+    ms, clk = time_graph(args, dist, stream, launch, n_sets, dev)
+    ms_max = dist.max(ms, device=dev)
+    ms_per_step = ms_max / args.steps
+    value = dist.sum(float(T * args.steps), device=dev) / (ms_max / 1e3)
+    algo = wl.algo_bytes()
+    achieved = algo / (ms_per_step / 1e3) / 1e9
+    peaks = measured_peaks()
+    cpu = None
+    if dist.rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
+        r = time_oracle(wl, args.cpu_seconds)
+        cpu = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": "%d of %d rows of the same workload (backward and recomputed forward), "
+                         "single-threaded C oracle, %.1f s" % (r["rows"], T, r["seconds"])}
+    if dist.rank != 0:
+        return 0
+    line = {
+        "metric": metric_of(wl), "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {**config_of(wl, args.gpus), "scale_layout": args.scale_layout,
+                   "l2": "inputs larger than L2: %d rotating input/output sets, %.0f MB" % (
+                       n_sets, n_sets * algo / 1e6)},
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(wl.name),
+                     "kernel": "swiglu_backward_kernel", "peak_source": peaks["source"],
+                     "algo_bytes_per_launch": algo},
         "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clk,
     }
     emit(line, args)

@@ -354,6 +354,56 @@ tk_status tk_moe_reduce_launch_info(tk_moe_reduce_plan_t plan, int64_t num_token
                                     int *smem_bytes);
 
 /* ------------------------------------------------------------------------
+ * SwiGLU backward, with the forward's FP8 codes optionally recomputed
+ *
+ * Not described on the pages, which give the forward only; this is the plain
+ * derivation of the forward above. With g' = min(g, L) and u' = clamp(u, -L,
+ * L) when clamping is on, s = sigmoid(g') and silu(g') = g' s:
+ *
+ *     dgate = dy * w * u' * s * (1 + g' * (1 - s))   (0 where g > L)
+ *     dup   = dy * w * silu(g')                      (0 where |u| > L)
+ *     dw    = sum over the row of dy * silu(g') * u'
+ *
+ * computed in fp32 and rounded to bf16 (dx) or kept in fp32 (dw, summed in a
+ * fixed order, so runs repeat bit for bit). With recompute_quant the call
+ * also writes the forward's codes and scales, recomputed from the same read
+ * of x and bit-identical to tk_swiglu_quant_run's, for a following GEMM that
+ * needs the quantized activation.
+ * ---------------------------------------------------------------------- */
+
+typedef struct tk_swiglu_backward_desc {
+    int64_t hidden;            /* H: 16, 32, 64, 128, 256, or a multiple of 512 up to 8192 */
+    int32_t has_topk_weights;  /* w: fp32 [T] (else weight 1) */
+    int32_t use_clamp;
+    float clamp_limit;         /* L > 0, as the forward */
+    int32_t recompute_quant;   /* also write the forward's codes and scales */
+    int32_t group_size;        /* recompute: 16 ... 512 (power of two, divides H); no per-token scale */
+    int32_t scale_fmt;         /* recompute: tk_scale_fmt */
+    int32_t out_fmt;           /* recompute: tk_out_fmt */
+    int32_t scale_layout;      /* recompute: tk_scale_layout */
+} tk_swiglu_backward_desc;
+
+typedef struct tk_swiglu_backward_plan_s *tk_swiglu_backward_plan_t;
+
+tk_status tk_swiglu_backward_validate(const tk_swiglu_backward_desc *desc);
+tk_status tk_swiglu_backward_plan(const tk_swiglu_backward_desc *desc, int device,
+                                  tk_swiglu_backward_plan_t *plan);
+tk_status tk_swiglu_backward_plan_destroy(tk_swiglu_backward_plan_t plan);
+
+/* Enqueue the backward of num_tokens rows.
+ *   x             [T, 2H] bf16, the forward's input, 32-byte aligned
+ *   topk_weights  [T] fp32, 4-byte aligned (required iff has_topk_weights)
+ *   dy            [T, H] bf16, the gradient of the forward's output y, 32-byte aligned
+ *   dx            [T, 2H] bf16: dgate in columns [0, H), dup in [H, 2H); 16-byte aligned
+ *   dw            [T] fp32 or NULL; 4-byte aligned
+ *   q, scales     recompute_quant only: as tk_swiglu_quant_run's outputs (else ignored)
+ * num_tokens == 0 is a no-op. Stream-ordered and asynchronous; inputs and
+ * outputs must not overlap. */
+tk_status tk_swiglu_backward_run(tk_swiglu_backward_plan_t plan, int64_t num_tokens, const void *x,
+                                 const float *topk_weights, const void *dy, void *dx, float *dw, void *q,
+                                 void *scales, void *stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics
  * ---------------------------------------------------------------------- */
 

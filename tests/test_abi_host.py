@@ -144,3 +144,23 @@ def test_reduce_validate():
     assert tk.tk_moe_reduce_validate(R(8208, 8, 0)) == 2
     assert tk.tk_moe_reduce_validate(R(2048, 65, 0)) == 2
     assert tk.tk_moe_reduce_validate(R(2064, 8, 1)) == 2
+
+
+def test_backward_validate():
+    B = tk.SwigluBackwardDesc
+    v = tk.tk_swiglu_backward_validate
+    # hidden, has_w, use_clamp, L, recompute, group, scale_fmt, out_fmt, layout
+    assert v(B(2048, 1, 0, 0.0, 0, 0, 0, 0, 0)) == 0
+    assert v(B(7168, 1, 1, 7.0, 0, 0, 0, 0, 0)) == 0
+    assert v(B(128, 0, 0, 0.0, 0, 0, 0, 0, 0)) == 0
+    assert v(B(2048, 1, 1, 7.0, 1, 128, 1, 0, 2)) == 0     # recompute, UE8M0, packed scales
+    assert v(B(2048, 1, 0, 0.0, 1, 32, 1, 1, 0)) == 0      # recompute into E2M1
+    assert v(B(0, 1, 0, 0.0, 0, 0, 0, 0, 0)) == 1
+    assert v(B(2048, 2, 0, 0.0, 0, 0, 0, 0, 0)) == 1
+    assert v(B(2048, 1, 1, -1.0, 0, 0, 0, 0, 0)) == 1      # clamp limit must be > 0
+    assert v(B(2048, 1, 1, float("inf"), 0, 0, 0, 0, 0)) == 1
+    assert v(B(96, 1, 0, 0.0, 0, 0, 0, 0, 0)) == 2         # neither a small power of two nor % 512
+    assert v(B(3000, 1, 0, 0.0, 0, 0, 0, 0, 0)) == 2
+    assert v(B(16384, 1, 0, 0.0, 0, 0, 0, 0, 0)) == 2      # above 8192
+    assert v(B(2048, 1, 0, 0.0, 1, 0, 0, 0, 0)) == 2       # recompute needs a group size
+    assert v(B(2048, 1, 0, 0.0, 1, 128, 0, 0, 2)) == 2     # packed layout needs UE8M0
