@@ -425,7 +425,7 @@ def run_ours(args, dist: Dist):
                          % (r["rows"], wl.T, r["seconds"])}
     if dist.rank != 0:
         return 0
-    traffic = None if transposed else load_traffic(wl.name)
+    traffic = load_traffic(wl.name, PROFILE_FAMILY["transposed" if transposed else wl.op])
     kernel = None
     if transposed:
         kernel = "transpose_quant_kernel"
@@ -543,7 +543,7 @@ def run_reduce(args, dist, wl, dev, n_sets):
                        n_sets, n_sets * algo / 1e6)},
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(wl.name),
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(wl.name, PROFILE_FAMILY["reduce"]),
                      "kernel": "moe_reduce_%s" % ("bulk_kernel" if info["kernel"] == "bulk" else "kernel"),
                      "peak_source": peaks["source"], "algo_bytes_per_launch": algo},
         "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clk,
@@ -609,7 +609,7 @@ def run_backward(args, dist, wl, dev, n_sets):
                        n_sets, n_sets * algo / 1e6)},
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(wl.name),
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(wl.name, PROFILE_FAMILY["backward"]),
                      "kernel": "swiglu_backward_kernel", "peak_source": peaks["source"],
                      "algo_bytes_per_launch": algo},
         "cpu_baseline": cpu, "e2e": None, "gpu_launches": args.steps, "clocks": clk,
@@ -631,17 +631,18 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def load_traffic(workload: str):
+PROFILE_FAMILY = {"swiglu": "swiglu_quant", "cast": "quant_cast", "reduce": "moe_reduce",
+                  "backward": "swiglu_backward", "transposed": "transposed_quant"}
+
+
+def load_traffic(workload: str, family: str):
     """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
-    from the committed ncu summary profiles/<kernel>_<workload>.md, or None
+    from the committed ncu summary profiles/<family>_<workload>.md, or None
     if there is none or it was taken on other kernel sources."""
-    import glob
-    paths = sorted(glob.glob(os.path.join(ROOT, "profiles", "*_%s.md" % workload)))
-    if not paths:
-        return None
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (family, workload))
     fields = {}
     try:
-        with open(paths[0]) as f:
+        with open(path) as f:
             for line in f:
                 if line.startswith("- ") and ": " in line:
                     k, v = line[2:].strip().split(": ", 1)
