@@ -28,7 +28,7 @@ from ._abi import (IN_DTYPES, OUT_FMTS, REDUCE_IN_FMTS, SCALE_FMTS, SCALE_LAYOUT
                    tk_swiglu_quant_host_workspace_size, tk_swiglu_quant_launch_info,
                    tk_swiglu_quant_output_sizes, tk_swiglu_quant_plan, tk_swiglu_quant_plan_destroy,
                    tk_swiglu_quant_run, tk_swiglu_quant_run_host, tk_swiglu_quant_run_host_static,
-                   tk_swiglu_quant_run_transposed, tk_swiglu_quant_transposed_size,
+                   tk_swiglu_quant_run_mapped, tk_swiglu_quant_run_transposed, tk_swiglu_quant_transposed_size,
                    tk_swiglu_quant_validate)
 
 __all__ = [
@@ -43,6 +43,7 @@ __all__ = [
     "SwigluQuantDesc", "QuantCastDesc", "tk_swiglu_quant_validate", "tk_swiglu_quant_plan",
     "tk_swiglu_quant_plan_destroy", "tk_swiglu_quant_output_sizes", "tk_swiglu_quant_run",
     "tk_swiglu_quant_launch_info", "tk_swiglu_quant_run_transposed", "tk_swiglu_quant_transposed_size",
+    "tk_swiglu_quant_run_mapped",
     "tk_quant_cast_validate", "tk_quant_cast_plan",
     "tk_quant_cast_plan_destroy", "tk_quant_cast_output_sizes", "tk_quant_cast_run", "tk_status_string",
     "tk_last_error_message", "tk_fault_word",
@@ -148,6 +149,27 @@ class SwigluQuant:
         with torch.cuda.device(x.device):
             tk_swiglu_quant_run(self.plan, T, x, topk_weights, q, scales, clamped_count,
                                 stream.cuda_stream)
+        return q, scales
+
+    def mapped(self, x_host, topk_weights_host=None, *, q=None, scales=None, clamped_count=None,
+               stream=None):
+        """The op on page-locked host tensors, read and written in place by the
+        kernel across the host link (tk_swiglu_quant_run_mapped). Outputs are
+        page-locked host tensors; they are complete once ``stream`` is."""
+        torch = _torch()
+        T = x_host.shape[0]
+        q_shape, s_shape, s_dtype = self.output_shapes(T)
+        if q is None:
+            q = torch.empty(q_shape, dtype=torch.uint8).pin_memory()
+        if scales is None:
+            scales = torch.empty(s_shape, dtype=s_dtype).pin_memory()
+        for t, name, shape in ((x_host, "x", (T, 2 * self.hidden)), (q, "q", q_shape), (scales, "scales", s_shape)):
+            if t.is_cuda or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+                raise ValueError("%s must be a contiguous host tensor of shape %s" % (name, shape))
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        tk_swiglu_quant_run_mapped(self.plan, T, x_host, topk_weights_host if self.has_w else None, q, scales,
+                                   clamped_count if self.count_clamped else None, stream.cuda_stream)
         return q, scales
 
     def transposed(self, x, topk_weights=None, *, qt=None, scales=None, clamped_count=None,

@@ -67,6 +67,7 @@ SIGNATURES = {
                                                     _PSZ, _PSZ]),
     "tk_swiglu_quant_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP]),
     "tk_swiglu_quant_launch_info": (ctypes.c_int, [_VP, ctypes.c_int64, _PINT, _PINT, _PINT, _PINT]),
+    "tk_swiglu_quant_run_mapped": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP]),
     "tk_swiglu_quant_transposed_size": (ctypes.c_int, [_VP, ctypes.c_int64, _PSZ,
                                                        ctypes.POINTER(ctypes.c_int64)]),
     "tk_swiglu_quant_run_transposed": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP]),
@@ -165,6 +166,12 @@ def tk_swiglu_quant_run(plan: int, num_tokens: int, x, topk_weights, q, scales, 
                         stream: int | None) -> None:
     check(lib().tk_swiglu_quant_run(plan, num_tokens, _ptr(x), _ptr(topk_weights), _ptr(q),
                                     _ptr(scales), _ptr(clamped_count), stream))
+
+
+def tk_swiglu_quant_run_mapped(plan: int, num_tokens: int, x_host, topk_weights_host, q_host, scales_host,
+                               clamped_count_host, stream: int | None) -> None:
+    check(lib().tk_swiglu_quant_run_mapped(plan, num_tokens, _ptr(x_host), _ptr(topk_weights_host),
+                                           _ptr(q_host), _ptr(scales_host), _ptr(clamped_count_host), stream))
 
 
 def tk_swiglu_quant_transposed_size(plan: int, num_tokens: int) -> tuple[int, int]:

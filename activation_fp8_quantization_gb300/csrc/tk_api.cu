@@ -518,6 +518,58 @@ TK_API tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t T, con
     return ok();
 }
 
+namespace {
+
+// The device address of page-locked host memory `p` (null stays null), or an
+// error if `p` is not such memory.
+tk_status mapped_address(const void *p, const char *what, void **dev)
+{
+    *dev = nullptr;
+    if (!p)
+        return TK_OK;
+    cudaPointerAttributes attr{};
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaPointerGetAttributes");
+    if (attr.type != cudaMemoryTypeHost || !attr.devicePointer)
+        return fail(TK_ERR_INVALID_ARG, "%s must be page-locked host memory the device can address", what);
+    *dev = attr.devicePointer;
+    return TK_OK;
+}
+
+}  // namespace
+
+TK_API tk_status tk_swiglu_quant_run_mapped(tk_swiglu_quant_plan_t plan, int64_t T, const void *x_host,
+                                            const float *topk_weights_host, void *q_host, void *scales_host,
+                                            int64_t *clamped_count_host, void *stream)
+{
+    if (!plan)
+        return fail(TK_ERR_INVALID_ARG, "plan is NULL");
+    if (T < 0)
+        return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)T);
+    if (T == 0)
+        return ok();
+    const tk_swiglu_quant_desc &d = plan->desc;
+    tk_status st = check_swiglu_args(plan, x_host, topk_weights_host, q_host, scales_host, clamped_count_host);
+    if (st != TK_OK)
+        return st;
+    void *x = nullptr, *w = nullptr, *q = nullptr, *s = nullptr, *c = nullptr;
+    if ((st = mapped_address(x_host, "x", &x)) != TK_OK ||
+        (st = mapped_address(d.has_topk_weights ? topk_weights_host : nullptr, "topk_weights", &w)) != TK_OK ||
+        (st = mapped_address(q_host, "q", &q)) != TK_OK || (st = mapped_address(scales_host, "scales", &s)) != TK_OK ||
+        (st = mapped_address(d.count_clamped ? clamped_count_host : nullptr, "clamped_count", &c)) != TK_OK)
+        return st;
+    const tk::SwigluArgs a = swiglu_args(d, x, static_cast<const float *>(w), static_cast<int64_t *>(c));
+    tk::OutArgs o{static_cast<uint8_t *>(q), s};
+    const Launch &L = plan->Ls.rows;
+    cudaError_t e = tk::launch_swiglu(L.fn, grid_for(L, T), L.block, L.smem, a, o,
+                                      shape_for(L, T, d.hidden, d.scale_layout, d.scale_fmt),
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launch of the fused kernel");
+    return ok();
+}
+
 TK_API tk_status tk_swiglu_quant_transposed_size(tk_swiglu_quant_plan_t plan, int64_t T, size_t *qt_bytes,
                                                  int64_t *ld)
 {

@@ -264,6 +264,20 @@ tk_status tk_swiglu_quant_run_host_static(tk_swiglu_quant_host_pipe_t pipe, int6
                                           void *q_host, void *scales_host,
                                           int64_t *clamped_count_host, void *stream);
 
+/* Host buffers read and written in place by the kernel (no staging copies):
+ * every buffer must be page-locked host memory that the device can address
+ * (cudaHostAlloc / cudaMallocHost, or cudaHostRegister'ed), which this call
+ * checks with cudaPointerGetAttributes (TK_ERR_INVALID_ARG otherwise). The
+ * kernel loads x and stores the codes and scales across the host link
+ * directly, so the link carries each byte once with no device copy in
+ * between; the row-block kernel always runs (no TMA copies from host
+ * memory). Arguments, layout and alignment as tk_swiglu_quant_run; the
+ * clamp counters, if requested, are host memory too. Stream-ordered: the
+ * outputs are complete when the stream is. */
+tk_status tk_swiglu_quant_run_mapped(tk_swiglu_quant_plan_t plan, int64_t num_tokens, const void *x_host,
+                                     const float *topk_weights_host, void *q_host, void *scales_host,
+                                     int64_t *clamped_count_host, void *stream);
+
 /* ------------------------------------------------------------------------
  * Standalone per-token / per-block cast: x [T, H] (bf16 or fp32) -> codes + scales,
  * with the same grouping, scale and code rules as the fused call.
