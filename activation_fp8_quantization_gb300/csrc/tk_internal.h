@@ -66,7 +66,7 @@ struct ReduceArgs {
 };
 
 // Bulk kernel: 1 producer warp + kReduceConsumerWarps consumer warps per CTA.
-constexpr int kReduceConsumerWarps = 8;
+constexpr int kReduceConsumerWarps = 16;
 constexpr int kReduceBulkThreads = 32 * (1 + kReduceConsumerWarps);
 constexpr int kReduceBulkMaxK = 32;   // one producer lane per slot
 constexpr int kReduceMetaBytes = 8 * 32 * 8;   // the producer's metadata ring (8 tasks x 32 lanes x 8 B)

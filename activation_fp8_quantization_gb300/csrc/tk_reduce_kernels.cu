@@ -20,7 +20,7 @@
 //    each persistent CTA is the producer: lane k fetches the token's k-th
 //    position and weight (eight tasks ahead), then copies row k's chunk (and its
 //    scales) into a ring slot of shared memory with one TMA bulk copy, an
-//    mbarrier per slot counting the bytes in. Eight consumer warps wait on the
+//    mbarrier per slot counting the bytes in. Sixteen consumer warps wait on the
 //    slot, accumulate the chunk from shared memory together, store it as bf16
 //    and release the slot on a second mbarrier. The bytes in flight (the
 //    ring, ~200 KB per SM) cost no registers.
