@@ -610,7 +610,7 @@ TK_API tk_status tk_swiglu_quant_run_transposed(tk_swiglu_quant_plan_t plan, int
     sh.tpg_log2 = lg;
     sh.groups = (int32_t)(d.hidden / d.group_size);
     const int64_t ldq = (T + 15) / 16 * 16;
-    const int64_t tiles = (T + 63) / 64 * (d.hidden / 128);
+    const int64_t tiles = (T + 31) / 32 * (d.hidden / 128);
     const int grid = (int)(tiles < plan->tgrid ? tiles : plan->tgrid);
     cudaError_t e = tk::launch_transpose(plan->tfn, grid, a, o, sh, ldq, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)

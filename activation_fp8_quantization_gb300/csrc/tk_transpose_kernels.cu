@@ -10,13 +10,14 @@
 // qT[H, ldq], element (column i, row t) at i * ldq + t, so that a following
 // GEMM that contracts over the rows reads it row-major.
 //
-// A CTA owns a tile of 64 rows x 128 columns at a time (persistent grid
-// stride over tiles). Phase 1: eight threads per row, 16 columns each, run the
-// fused op and the quantizer of the row-major kernels (same arithmetic, same
-// order) for two passes of 32 rows and store the 16 codes row-major into a
-// shared tile. Phase 2: each thread gathers 32 consecutive rows of one column
-// from the tile and writes them as two 16-byte stores, so every warp writes
-// full 32-byte sectors of 32 rows of qT. Rows T <= t < ldq of the last tile
+// A CTA of 128 threads owns a tile of 32 rows x 128 columns at a time
+// (persistent grid stride over tiles; small CTAs, up to eight per SM, so that
+// one CTA's loads overlap another's quantization and write-out). Phase 1:
+// eight threads per row, 16 columns each, run the fused op and the quantizer
+// of the row-major kernels (same arithmetic, same order) for two passes of 16
+// rows and store the 16 codes row-major into a shared tile. Phase 2: each
+// thread gathers the tile's 32 rows of one column and writes them as two
+// 16-byte stores, so every warp writes full 32-byte sectors of 32 rows of qT. Rows T <= t < ldq of the last tile
 // are written as zero codes; nothing at or past ldq is written.
 #include "tk_internal.h"
 
@@ -24,10 +25,11 @@ namespace tk {
 
 namespace {
 
-constexpr int kTileRows = 64;
+constexpr int kTileRows = 32;
 constexpr int kTileCols = 128;
 constexpr int kTileStride = 144;   // bytes per shared row: 16-byte aligned, conflict-free in both phases
-constexpr int kTransposeThreads = 256;
+constexpr int kTransposeThreads = 128;
+constexpr int kPassRows = kTransposeThreads / 8;
 
 template <int SCALE, bool CLAMP>
 __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(SwigluArgs a, OutArgs o, RowShape sh,
@@ -36,13 +38,13 @@ __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(Swig
     __shared__ __align__(16) uint8_t tile[kTileRows * kTileStride];
     SwigluSrc<CLAMP> src;
     const int tid = threadIdx.x;
-    const int rr = tid >> 3;           // row of the pass (0..31)
+    const int rr = tid >> 3;           // row of the pass (0..15)
     const int cc = (tid & 7) * kEPT;   // first column within the tile
     const int tpg_mask = (1 << sh.tpg_log2) - 1;
     const int ncb = sh.H / kTileCols;
     const int64_t ntiles = (sh.T + kTileRows - 1) / kTileRows * ncb;
     const int oc = tid & (kTileCols - 1);   // phase 2: column within the tile
-    const int oh = tid >> 7;                // phase 2: rows oh*32 .. oh*32+31
+    const int oh = tid >> 7;                // phase 2: rows oh*32 .. oh*32+31 (oh = 0 with 128 threads)
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t tl = blockIdx.x; tl < ntiles; tl += gridDim.x) {
@@ -52,7 +54,7 @@ __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(Swig
         typename SwigluSrc<CLAMP>::Regs regs[2];
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
-            const int64_t row = t0 + p * 32 + rr;
+            const int64_t row = t0 + p * kPassRows + rr;
             if (row < sh.T)
                 SwigluSrc<CLAMP>::load(a, row, c0 + cc, regs[p]);
             else
@@ -60,7 +62,7 @@ __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(Swig
         }
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
-            const int64_t row = t0 + p * 32 + rr;
+            const int64_t row = t0 + p * kPassRows + rr;
             const bool ok = row < sh.T;
             uint64_t ny[kEPT / 2];
             float amax = 0.0f;
@@ -76,7 +78,7 @@ __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(Swig
                 if ((tid & tpg_mask) == 0)
                     store_scale<SCALE>(sh, o, row, (c0 + cc) >> (sh.tpg_log2 + 4), s, k);
             }
-            *reinterpret_cast<uint4 *>(tile + (p * 32 + rr) * kTileStride + cc) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4 *>(tile + (p * kPassRows + rr) * kTileStride + cc) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         __syncthreads();
         uint32_t out[8];
