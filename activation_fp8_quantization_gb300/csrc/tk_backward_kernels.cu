@@ -32,10 +32,15 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
     return r;
 }
 
+// Registers are capped at 64 (two 512-thread or four 256-thread CTAs per SM):
+// left to itself the compiler gives the clamping, recomputing forms over 100,
+// which halves the CTAs per SM and was measured 25% slower than the few
+// bytes of spills the cap costs.
 template <bool CLAMP, bool RECOMPUTE, int OUT, int SCALE>
-__global__ void __launch_bounds__(512) swiglu_backward_kernel(BackwardArgs a, OutArgs o, RowShape sh)
+__global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a, OutArgs o, RowShape sh)
 {
-    __shared__ float red[16];
+    __shared__ float red[2][16];   // per-warp partial dw, double-buffered by row block
+    int buf = 0;
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int slot = tid / sh.tpr;
@@ -135,16 +140,19 @@ __global__ void __launch_bounds__(512) swiglu_backward_kernel(BackwardArgs a, Ou
                 if (ok && lr == 0)
                     a.dw[row] = part;
             } else {
+                // red[buf] is rewritten two row blocks later, after the next
+                // block's barrier, which the reading thread reaches only after
+                // its read: one barrier per row block suffices.
                 if ((tid & 31) == 0)
-                    red[warp] = part;
+                    red[buf][warp] = part;
                 __syncthreads();
                 if (ok && lr == 0) {
-                    float s = red[slot * nwr];
+                    float s = red[buf][slot * nwr];
                     for (int j = 1; j < nwr; ++j)
-                        s += red[slot * nwr + j];
+                        s += red[buf][slot * nwr + j];
                     a.dw[row] = s;
                 }
-                __syncthreads();
+                buf ^= 1;
             }
         }
         if (RECOMPUTE) {
