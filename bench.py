@@ -327,14 +327,6 @@ def run_ours(args, dist: Dist):
     torch.cuda.set_device(dev)
     wl = wls.ALL_WORKLOADS[args.workload]
     T, H = wl.T, wl.H
-    if wl.op == "reduce":
-        op = None
-    elif wl.op == "cast":
-        op = tk.QuantCast(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.in_dtype, dev, args.scale_layout)
-        op.count_clamped = False
-    else:
-        op = tk.SwigluQuant(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.w_dist is not None, wl.clamp,
-                            wl.clamp is not None, dev, args.scale_layout)
     algo = wl.algo_bytes()
     per_set = algo
     n_sets = max(2, -(-3 * L2_BYTES // per_set) + 1)   # sets beyond the current one hold > 3x L2
@@ -342,6 +334,12 @@ def run_ours(args, dist: Dist):
         return run_reduce(args, dist, wl, dev, n_sets)
     if wl.op == "backward":
         return run_backward(args, dist, wl, dev, n_sets)
+    if wl.op == "cast":
+        op = tk.QuantCast(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.in_dtype, dev, args.scale_layout)
+        op.count_clamped = False
+    else:
+        op = tk.SwigluQuant(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.w_dist is not None, wl.clamp,
+                            wl.clamp is not None, dev, args.scale_layout)
 
     x0, w0 = wls.make_inputs(wl, "cuda")
     q_shape, s_shape, s_dtype = op.output_shapes(T)
