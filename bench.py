@@ -729,6 +729,10 @@ def main(argv=None):
     if args.impl == "reference":
         # rank 0 alone times the CPU oracle; other ranks exit without work
         return run_reference(args, RankOnly())
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != world:
+        raise SystemExit("--gpus %d does not match the %d process(es) launched: for N > 1 run "
+                         "python -m torch.distributed.run --nproc-per-node N bench.py --gpus N" % (args.gpus, world))
     dist = Dist("nccl")
     try:
         return run_ours(args, dist)
