@@ -1,6 +1,13 @@
 /*
  * tk_swiglu_quant.h -- C ABI of the fused SwiGLU + MoE top-k weight +
- * FP8/FP4 activation cast, and of the standalone per-token / per-block cast.
+ * FP8/FP4 activation cast and the operations around it:
+ *   tk_swiglu_quant_*     the fused op (device buffers; host buffers staged
+ *                         through device memory, or read and written in place
+ *                         by the kernel; codes row-major or transposed)
+ *   tk_quant_cast_*       the standalone per-token / per-block cast
+ *   tk_moe_reduce_*       the weighted top-k combine after the expert GEMMs
+ *   tk_swiglu_backward_*  the SwiGLU backward, optionally recomputing the codes
+ *   tk_fault_word, tk_status_string, tk_last_error_message   diagnostics
  *
  * The operation ("TileKernels从入门到精通" / "TileKernels from Beginner to
  * Master", zhichai.net/topic/177618752 and zhichai.net/en/topic/177618752,
