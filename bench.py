@@ -61,6 +61,7 @@ def parse_args(argv=None):
     p.add_argument("--transposed", action="store_true",
                    help="fused workloads: write the codes transposed (tk_swiglu_quant_run_transposed)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-context", action="store_true", help="skip the unfused PyTorch context timing")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--jsonl", default=None, help="also append the JSON line to this file")
     return p.parse_args(argv)
@@ -215,6 +216,37 @@ def cpu_inputs(wl):
         x, w, dy = wls.make_backward_inputs(wl, "cpu")
         return x, (w, dy)
     return wls.make_inputs(wl, "cpu")
+
+
+def _oracle_worker(job):
+    """One spawned worker: time the oracle on `rows` rows of the workload."""
+    name, rows = job
+    import oracle
+    from activation_fp8_quantization_gb300 import workloads as wls
+    wl = wls.ALL_WORKLOADS[name]
+    lib = oracle.load()
+    step = oracle_step(wl, *cpu_inputs(wl.with_rows(rows)), lib)
+    t = time.perf_counter()
+    step()
+    return rows, time.perf_counter() - t
+
+
+def time_oracle_all_cores(wl, seconds: float) -> dict:
+    """The oracle over every host core: one spawned process per core (a pool
+    started with spawn, so no process is forked from a CUDA context), each
+    timing its own share of about `seconds` of work; throughput is all rows
+    over the slowest worker's time."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    one = time_oracle(wl, 0.5)
+    per_row = one["seconds"] / one["rows"]
+    rows = int(max(8, min(wl.T, seconds / max(per_row, 1e-9))))
+    with mp.get_context("spawn").Pool(cores) as pool:
+        pool.map(_oracle_worker, [(wl.name, 8)] * cores)          # start-up and library load
+        res = pool.map(_oracle_worker, [(wl.name, rows)] * cores)
+    slowest = max(dt for _, dt in res)
+    total = sum(r for r, _ in res)
+    return {"rows": total, "seconds": slowest, "tokens_per_s": total / slowest, "cores": cores}
 
 
 def oracle_step(wl, x, w, lib):
@@ -414,6 +446,9 @@ def run_ours(args, dist: Dist):
     e2e = None
     if not args.no_e2e and wl.op == "swiglu" and args.scale_layout == "row" and not transposed:
         e2e = measure_e2e(op, wl, x0, w0, dev, args, dist)
+    context = None
+    if dist.rank == 0 and not transposed and not args.no_context:
+        context = torch_unfused_context(wl, xs, ws, stream)
 
     cpu = None
     if dist.rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
@@ -421,6 +456,10 @@ def run_ours(args, dist: Dist):
         cpu = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": "%d of %d rows of the same workload, single-threaded C oracle, %.1f s"
                          % (r["rows"], wl.T, r["seconds"])}
+        ra = time_oracle_all_cores(wl, args.cpu_seconds)
+        cpu["all_cores"] = {"value": ra["tokens_per_s"], "unit": "tokens/s", "cores": ra["cores"],
+                            "sample": "%d rows per core, one spawned process per core, slowest %.1f s"
+                                      % (ra["rows"] // ra["cores"], ra["seconds"])}
     if dist.rank != 0:
         return 0
     traffic = load_traffic(wl.name, PROFILE_FAMILY["transposed" if transposed else wl.op])
@@ -444,11 +483,59 @@ def run_ours(args, dist: Dist):
                      "peak_source": peaks["source"], "algo_bytes_per_launch": algo},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "context_torch_unfused": context,
         "gpu_launches": args.steps,
         "clocks": clk,
     }
     emit(line, args)
     return 0
+
+
+def torch_unfused_context(wl, xs, ws, stream, steps: int = 100):
+    """The same op as PyTorch eager ops on the device, unfused, for context
+    only: silu(g') * u' * w, the group absmax, the scale and a cast to
+    torch.float8_e4m3fn (fp32 or power-of-two scales). Not the library's
+    path; its codes are not checked here."""
+    import torch
+    import torch.nn.functional as F
+    if wl.op != "swiglu" or wl.out_fmt != "e4m3":
+        return None
+    T, H = wl.T, wl.H
+    g_sz = wl.group or H
+    n = len(xs)
+
+    def step(i):
+        x = xs[i % n]
+        g, u = x[:, :H].float(), x[:, H:].float()
+        if wl.clamp is not None:
+            g = g.clamp(max=wl.clamp)
+            u = u.clamp(-wl.clamp, wl.clamp)
+        y = F.silu(g) * u
+        if ws[i % n] is not None:
+            y = y * ws[i % n][:, None]
+        y = y.view(T, H // g_sz, g_sz)
+        amax = y.abs().amax(-1, keepdim=True)
+        if wl.scale_fmt == "fp32":
+            s = amax / 448.0
+            s = torch.where(s == 0, torch.ones_like(s), s)
+        else:
+            s = torch.exp2(torch.ceil(torch.log2(torch.clamp(amax, min=1e-38) / 448.0)))
+        return (y / s).to(torch.float8_e4m3fn), s
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i)
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            step(i)
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"ms_per_step": ms, "value": T / (ms / 1e3), "unit": "tokens/s", "steps": steps,
+            "path": "PyTorch eager, unfused (silu, multiply, amax, divide, float8 cast), same inputs"}
 
 
 def time_graph(args, dist, stream, launch, n_sets, dev):
