@@ -41,7 +41,7 @@ def _both(op, x, w):
 @pytest.mark.parametrize("scale_fmt", ["fp32", "ue8m0"])
 @pytest.mark.parametrize("group", [32, 64, 128])
 @pytest.mark.parametrize("H,T", [(128, 1), (256, 15), (256, 16), (512, 17), (2048, 63), (2048, 64),
-                                 (2048, 65), (1024, 1000), (7168, 129)])
+                                 (2048, 65), (1024, 1000), (7168, 129), (16384, 33)])
 def test_transposed_matches_row_major_and_oracle(H, T, group, scale_fmt):
     x, w = _inputs(T, H, seed=H + 7 * T + group)
     op = tk.SwigluQuant(H, group, scale_fmt, "e4m3", True)
@@ -138,3 +138,11 @@ def test_transposed_refused_where_unsupported():
         _abi.tk_swiglu_quant_run_transposed(op.plan, 10, x, torch.ones(10, device="cuda"), qt.data_ptr() + 8, s,
                                             None, None)
     assert e.value.status == 3
+
+
+def test_transposed_zero_rows_is_a_noop():
+    op = tk.SwigluQuant(256, 128, "fp32", "e4m3", True)
+    n, ld = tk.tk_swiglu_quant_transposed_size(op.plan, 0)
+    assert n == 0 and ld == 0
+    tk.tk_swiglu_quant_run_transposed(op.plan, 0, None, None, None, None, None, None)
+    torch.cuda.synchronize()
