@@ -66,7 +66,7 @@ SIGNATURES = {
     "tk_swiglu_quant_output_sizes": (ctypes.c_int, [ctypes.POINTER(SwigluQuantDesc), ctypes.c_int64,
                                                     _PSZ, _PSZ]),
     "tk_swiglu_quant_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP]),
-    "tk_swiglu_quant_launch_info": (ctypes.c_int, [_VP, ctypes.c_int64, _PINT, _PINT, _PINT, _PINT]),
+    "tk_swiglu_quant_launch_info": (ctypes.c_int, [_VP, ctypes.c_int64, _PINT, _PINT, _PINT, _PINT, _PINT]),
     "tk_swiglu_quant_run_mapped": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP]),
     "tk_swiglu_quant_transposed_size": (ctypes.c_int, [_VP, ctypes.c_int64, _PSZ,
                                                        ctypes.POINTER(ctypes.c_int64)]),
@@ -188,11 +188,15 @@ def tk_swiglu_quant_run_transposed(plan: int, num_tokens: int, x, topk_weights, 
                                                _ptr(scales), _ptr(clamped_count), stream))
 
 
+KERNEL_NAMES = {0: "row_quant_kernel", 1: "warp_stream_kernel", 2: "block_stream_kernel"}
+
+
 def tk_swiglu_quant_launch_info(plan: int, num_tokens: int) -> dict:
-    g, b, r, n = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    g, b, r, n, k = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     check(lib().tk_swiglu_quant_launch_info(plan, num_tokens, ctypes.byref(g), ctypes.byref(b),
-                                            ctypes.byref(r), ctypes.byref(n)))
-    return {"grid": g.value, "block": b.value, "rows_per_cta": r.value, "num_sms": n.value}
+                                            ctypes.byref(r), ctypes.byref(n), ctypes.byref(k)))
+    return {"grid": g.value, "block": b.value, "rows_per_cta": r.value, "num_sms": n.value,
+            "kernel": KERNEL_NAMES[k.value]}
 
 
 def tk_swiglu_quant_host_pipe_create(plan: int, chunk_rows: int) -> int:

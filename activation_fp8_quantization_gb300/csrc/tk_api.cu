@@ -119,14 +119,17 @@ struct DeviceScope {
     }
 };
 
+// The kernels a plan can launch.
+enum Kind { kRows = TK_KERNEL_ROWS, kWarpStream = TK_KERNEL_WARP_STREAM, kBlockStream = TK_KERNEL_BLOCK_RING };
+
 // Everything a launch needs, fixed when the plan is made.
 struct Launch {
     const void *fn;
-    bool stream;       // warp_stream_kernel (else row_quant_kernel)
+    int kind;          // row_quant_kernel, warp_stream_kernel or block_stream_kernel
     int block;         // threads per CTA
-    int rpc;           // row kernel: rows per CTA per iteration
+    int rpc;           // row kernel: rows per CTA per iteration; block kernel: rows per ring slot
     int tpr, tpg_log2, groups;
-    int wpr, stages;   // stream kernel: warps per row, ring slots per warp
+    int wpr, stages;   // stream kernels: 512-column slices per row, ring slots (per warp or per CTA)
     size_t smem;       // dynamic shared memory per CTA
     int max_grid;      // resident CTAs on all SMs
     int num_sms;
@@ -135,7 +138,8 @@ struct Launch {
 
 int grid_for(const Launch &L, int64_t T)
 {
-    const int64_t units = L.stream ? (T * L.wpr + (L.block / 32) - 1) / (L.block / 32) : (T + L.rpc - 1) / L.rpc;
+    const int64_t units =
+        L.kind == kWarpStream ? (T * L.wpr + (L.block / 32) - 1) / (L.block / 32) : (T + L.rpc - 1) / L.rpc;
     return (int)(units < L.max_grid ? units : L.max_grid);
 }
 
@@ -232,6 +236,50 @@ tk_status choose_stream_ring(Launch *L, int slot_bytes, int optin)
     return TK_OK;
 }
 
+// Ring of the block-ring kernel. Rows per slot: the fewest that give a block
+// at least one slice per consumer warp, times the multiple nearest below
+// TK_BLOCK_SLOT_KB (default 32) KB; then the ring depth with the most bytes
+// in flight per SM while at least 24 consumer warps per SM stay resident
+// (ties: the shallower ring). TK_BLOCK_STAGES=<n> (2..16) forces the depth.
+// Measured on GB300 at width 2048: 32 KB slots (four rows, two slots, three
+// CTAs per SM) are 3% faster than 16 KB slots four deep; six 16 KB slots
+// (two CTAs per SM) are 9% slower.
+tk_status choose_block_ring(Launch *L, int64_t row_bytes, int optin)
+{
+    const int rb_min = (tk::kBlockConsumerWarps + L->wpr - 1) / L->wpr;
+    const int64_t target = (int64_t)env_int("TK_BLOCK_SLOT_KB", 32) * 1024;
+    int64_t mult = target / (rb_min * row_bytes);
+    if (mult < 1)
+        mult = 1;
+    L->rpc = (int)(rb_min * mult);
+    const int64_t slot = (int64_t)L->rpc * row_bytes;
+    const int forced = env_int("TK_BLOCK_STAGES", 0);
+    long best = -1;
+    for (int S = 2; S <= 16; ++S) {
+        const int64_t smem = (int64_t)S * (slot + 16);   // the slots, then full[S] and empty[S]
+        if (smem > optin)
+            break;
+        int occ = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, L->fn, L->block, (size_t)smem);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (occ < 1)
+            continue;
+        const long inflight = (long)occ * S * slot;
+        const bool pick =
+            forced ? S == forced : ((long)occ * tk::kBlockConsumerWarps >= 24 || best < 0) && inflight > best;
+        if (pick) {
+            best = inflight;
+            L->stages = S;
+            L->smem = (size_t)smem;
+            L->max_grid = occ;
+        }
+    }
+    if (best < 0)
+        return fail(TK_ERR_UNSUPPORTED, "no block ring fits in shared memory");
+    return TK_OK;
+}
+
 }  // namespace
 
 // Set by a stream kernel that gave up waiting on one of its own copies.
@@ -239,34 +287,55 @@ __device__ unsigned int g_tk_fault_word;
 
 namespace {
 
-// Both kernels of a plan: the row kernel always, the stream kernel where it
-// applies. TK_KERNEL=rows or =stream (read when the plan is made) forces one.
+// The kernels of a plan: the row kernel always, the two stream kernels where
+// they apply. TK_KERNEL=rows, =stream or =block (read when the plan is made)
+// forces one; otherwise the block-ring kernel runs batches of the fused op
+// that give every resident CTA at least block_min row blocks, and the row
+// kernel everything else (block_min = 0: never).
 struct Launches {
     Launch rows;
     Launch stream;
+    Launch block;
     bool has_stream;
-    int forced;   // 0: by size, 1: rows, 2: stream
+    bool has_block;
+    int64_t block_min;
+    int forced;   // 0: by size, 1: rows, 2: warp stream, 3: block ring
 };
 
-// The stream kernel pays off once every resident warp has several slices to
-// stream (its ring stays full); smaller batches go to the row kernel, whose
-// register prefetch starts up faster.
-constexpr int64_t kStreamMinTasksPerWarp = 16;
+// Where the block-ring kernel overtakes the row kernel, whose register
+// prefetch starts up faster but which spends more instructions per element.
+// Measured on GB300 at width 2048 (4 rows per block, 456 CTAs), µs row kernel
+// / block kernel:
+//   fp32 scales, no clamp:  8192 rows 15.3/18.1, 16384 28.6/29.3, 24576 42.1/41.1
+//   UE8M0, clamp 7:         8192 rows 19.7/18.8, 16384 35.4/31.5, 32768 68.4/58.1
+//   FP4 1x32, clamp 7:      16384 rows 34.1/30.5
+// so about 12 blocks per CTA without the clamp and 4 with it (its extra
+// arithmetic is what the row kernel cannot hide). The standalone cast, with a
+// third of the fused op's arithmetic per byte, was faster on the row kernel at
+// every size tried (8192 x 4096 and 16384 x 7168), so its plans never pick the
+// block kernel.
+constexpr int64_t kBlockMinPerCtaPlain = 12;
+constexpr int64_t kBlockMinPerCtaClamp = 4;
 
 const Launch &pick(const Launches &Ls, int64_t T)
 {
-    if (!Ls.has_stream || Ls.forced == 1)
+    if (Ls.forced == 1)
         return Ls.rows;
     if (Ls.forced == 2)
-        return Ls.stream;
-    const int64_t warps = (int64_t)Ls.stream.max_grid * (Ls.stream.block / 32);
-    return T * Ls.stream.wpr >= kStreamMinTasksPerWarp * warps ? Ls.stream : Ls.rows;
+        return Ls.has_stream ? Ls.stream : Ls.rows;
+    if (Ls.forced == 3)
+        return Ls.has_block ? Ls.block : Ls.rows;
+    if (!Ls.has_block || Ls.block_min <= 0)
+        return Ls.rows;
+    const int64_t nblk = (T + Ls.block.rpc - 1) / Ls.block.rpc;
+    return nblk >= Ls.block_min * Ls.block.max_grid ? Ls.block : Ls.rows;
 }
 
-// Validate the device and size one kernel's launch: the stream kernel when
-// `want_stream` (the caller checked that it applies), else the row kernel.
-tk_status make_launch(int device, int64_t hidden, int32_t group, const void *row_fn, const void *stream_fn,
-                      int slot_bytes, bool want_stream, Launch *L)
+// Validate the device and size one kernel's launch of `kind` (the caller
+// checked that it applies): fn is that kernel's entry; slot_bytes the warp
+// stream kernel's slot, row_bytes one input row (block kernel).
+tk_status make_launch(int device, int64_t hidden, int32_t group, const void *fn, int kind, int slot_bytes,
+                      int64_t row_bytes, Launch *L)
 {
     int count = 0;
     cudaError_t e = cudaGetDeviceCount(&count);
@@ -293,9 +362,21 @@ tk_status make_launch(int device, int64_t hidden, int32_t group, const void *row
     L->tpr = geo.tpr;
     L->tpg_log2 = geo.tpg_log2;
     L->groups = geo.groups;
-    L->stream = want_stream;
-    if (L->stream) {
-        L->fn = stream_fn;
+    L->kind = kind;
+    L->fn = fn;
+    if (kind == kBlockStream) {
+        L->block = tk::kBlockThreads;
+        L->wpr = (int)(hidden / 512);
+        e = cudaFuncSetAttribute(L->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(L->fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "configuring the block kernel's shared memory");
+        tk_status st = choose_block_ring(L, row_bytes, optin);
+        if (st != TK_OK)
+            return st;
+    } else if (kind == kWarpStream) {
         L->block = tk::kStreamThreads;
         L->rpc = 1;
         L->wpr = (int)(hidden / 512);
@@ -309,7 +390,6 @@ tk_status make_launch(int device, int64_t hidden, int32_t group, const void *row
         if (st != TK_OK)
             return st;
     } else {
-        L->fn = row_fn;
         L->block = geo.block;
         L->rpc = geo.rpc;
         L->stages = 0;
@@ -328,18 +408,28 @@ tk_status make_launch(int device, int64_t hidden, int32_t group, const void *row
 }
 
 tk_status make_launches(int device, int64_t hidden, int32_t group, const void *row_fn, const void *stream_fn,
-                        int slot_bytes, Launches *Ls)
+                        const void *block_fn, int slot_bytes, int row_bytes_per_col, Launches *Ls)
 {
     *Ls = Launches{};
     const char *force = getenv("TK_KERNEL");
-    Ls->forced = !force ? 0 : (strcmp(force, "rows") == 0 ? 1 : (strcmp(force, "stream") == 0 ? 2 : 0));
-    tk_status st = make_launch(device, hidden, group, row_fn, stream_fn, slot_bytes, false, &Ls->rows);
+    Ls->forced = !force                       ? 0
+                 : strcmp(force, "rows") == 0   ? 1
+                 : strcmp(force, "stream") == 0 ? 2
+                 : strcmp(force, "block") == 0  ? 3
+                                                : 0;
+    tk_status st = make_launch(device, hidden, group, row_fn, kRows, 0, 0, &Ls->rows);
     if (st != TK_OK)
         return st;
     const Geometry geo = geometry(hidden, group);
     Ls->has_stream = stream_fn && hidden % 512 == 0 && !geo.cta_reduce;
     if (Ls->has_stream)
-        st = make_launch(device, hidden, group, row_fn, stream_fn, slot_bytes, true, &Ls->stream);
+        st = make_launch(device, hidden, group, stream_fn, kWarpStream, slot_bytes, 0, &Ls->stream);
+    if (st != TK_OK)
+        return st;
+    Ls->has_block = Ls->has_stream && block_fn;
+    if (Ls->has_block)
+        st = make_launch(device, hidden, group, block_fn, kBlockStream, 0, (int64_t)row_bytes_per_col * hidden,
+                         &Ls->block);
     return st;
 }
 
@@ -402,12 +492,15 @@ TK_API tk_status tk_swiglu_quant_plan(const tk_swiglu_quant_desc *d, int device,
     const bool clamp = d->use_clamp != 0;
     const void *row_fn = tk::swiglu_kernel_fn(d->out_fmt, d->scale_fmt, clamp, geo.cta_reduce);
     const void *stream_fn = tk::swiglu_stream_fn(d->out_fmt, d->scale_fmt, clamp);
+    const void *block_fn = tk::swiglu_block_fn(d->out_fmt, d->scale_fmt, clamp);
     if (!row_fn)
         return fail(TK_ERR_UNSUPPORTED, "no kernel for this combination");
     Launches Ls{};
-    st = make_launches(device, d->hidden, d->group_size, row_fn, stream_fn, tk::kSwigluSlotBytes, &Ls);
+    st = make_launches(device, d->hidden, d->group_size, row_fn, stream_fn, block_fn, tk::kSwigluSlotBytes,
+                       tk::kSwigluRowBytesPerCol, &Ls);
     if (st != TK_OK)
         return st;
+    Ls.block_min = clamp ? kBlockMinPerCtaClamp : kBlockMinPerCtaPlain;
     // The transposed-codes kernel: E4M3, groups of 32, 64 or 128 columns
     // inside its 128-column tiles.
     const void *tfn = nullptr;
@@ -619,7 +712,7 @@ TK_API tk_status tk_swiglu_quant_run_transposed(tk_swiglu_quant_plan_t plan, int
 }
 
 TK_API tk_status tk_swiglu_quant_launch_info(tk_swiglu_quant_plan_t plan, int64_t T, int *grid, int *block,
-                                             int *rows_per_cta, int *num_sms)
+                                             int *rows_per_cta, int *num_sms, int *kernel)
 {
     if (!plan || T < 0)
         return fail(TK_ERR_INVALID_ARG, "plan is NULL or num_tokens < 0");
@@ -629,9 +722,11 @@ TK_API tk_status tk_swiglu_quant_launch_info(tk_swiglu_quant_plan_t plan, int64_
     if (block)
         *block = L.block;
     if (rows_per_cta)
-        *rows_per_cta = L.stream ? 0 : L.rpc;
+        *rows_per_cta = L.kind == kWarpStream ? 0 : L.rpc;
     if (num_sms)
         *num_sms = L.num_sms;
+    if (kernel)
+        *kernel = L.kind;
     return ok();
 }
 
@@ -920,11 +1015,14 @@ TK_API tk_status tk_quant_cast_plan(const tk_quant_cast_desc *d, int device, tk_
     const Geometry geo = geometry(d->hidden, d->group_size);
     const void *row_fn = tk::cast_kernel_fn(d->in_dtype, d->out_fmt, d->scale_fmt, geo.cta_reduce);
     const void *stream_fn = tk::cast_stream_fn(d->in_dtype, d->out_fmt, d->scale_fmt);
+    const void *block_fn = tk::cast_block_fn(d->in_dtype, d->out_fmt, d->scale_fmt);
     if (!row_fn)
         return fail(TK_ERR_UNSUPPORTED, "no kernel for this combination");
     Launches Ls{};
-    st = make_launches(device, d->hidden, d->group_size, row_fn, stream_fn,
-                       d->in_dtype == TK_IN_BF16 ? tk::kCastBf16SlotBytes : tk::kCastF32SlotBytes, &Ls);
+    const bool bf16 = d->in_dtype == TK_IN_BF16;
+    st = make_launches(device, d->hidden, d->group_size, row_fn, stream_fn, block_fn,
+                       bf16 ? tk::kCastBf16SlotBytes : tk::kCastF32SlotBytes,
+                       bf16 ? tk::kCastBf16RowBytesPerCol : tk::kCastF32RowBytesPerCol, &Ls);
     if (st != TK_OK)
         return st;
     auto *p = new (std::nothrow) tk_quant_cast_plan_s{*d, device, Ls};

@@ -38,7 +38,27 @@ const void *stream_pick(int out_fmt, int scale_fmt)
                                       : reinterpret_cast<const void *>(&warp_stream_kernel<Src, kOutE2M1, kScaleUE8M0>);
     return nullptr;
 }
+template <class Src>
+const void *block_pick(int out_fmt, int scale_fmt)
+{
+    if (out_fmt == kOutE4M3)
+        return scale_fmt == kScaleF32 ? reinterpret_cast<const void *>(&block_stream_kernel<Src, kOutE4M3, kScaleF32>)
+                                      : reinterpret_cast<const void *>(&block_stream_kernel<Src, kOutE4M3, kScaleUE8M0>);
+    if (out_fmt == kOutE2M1)
+        return scale_fmt == kScaleF32 ? reinterpret_cast<const void *>(&block_stream_kernel<Src, kOutE2M1, kScaleF32>)
+                                      : reinterpret_cast<const void *>(&block_stream_kernel<Src, kOutE2M1, kScaleUE8M0>);
+    return nullptr;
+}
 }  // namespace
+
+const void *cast_block_fn(int in_dtype, int out_fmt, int scale_fmt)
+{
+    if (in_dtype == 0)
+        return block_pick<CastBf16Src>(out_fmt, scale_fmt);
+    if (in_dtype == 1)
+        return block_pick<CastF32Src>(out_fmt, scale_fmt);
+    return nullptr;
+}
 
 const void *cast_stream_fn(int in_dtype, int out_fmt, int scale_fmt)
 {

@@ -8,17 +8,19 @@
 
 namespace tk {
 
-// Entry of the fused op's row-block kernel (any width) or of its warp-stream
-// kernel (width a multiple of 512) for a format / scale / clamp combination;
-// nullptr if there is none.
+// Entry of the fused op's row-block kernel (any width), of its warp-stream
+// kernel or of its block-ring kernel (widths a multiple of 512) for a format /
+// scale / clamp combination; nullptr if there is none.
 const void *swiglu_kernel_fn(int out_fmt, int scale_fmt, bool clamp, bool cta_reduce);
 const void *swiglu_stream_fn(int out_fmt, int scale_fmt, bool clamp);
+const void *swiglu_block_fn(int out_fmt, int scale_fmt, bool clamp);   // block_stream_kernel
 cudaError_t launch_swiglu(const void *fn, int grid, int block, size_t smem, const SwigluArgs &a,
                           const OutArgs &o, const RowShape &sh, cudaStream_t stream);
 
 // Same for the standalone cast (in_dtype: 0 bf16, 1 fp32).
 const void *cast_kernel_fn(int in_dtype, int out_fmt, int scale_fmt, bool cta_reduce);
 const void *cast_stream_fn(int in_dtype, int out_fmt, int scale_fmt);
+const void *cast_block_fn(int in_dtype, int out_fmt, int scale_fmt);
 cudaError_t launch_cast(const void *fn, int grid, int block, size_t smem, const CastArgs &a,
                         const OutArgs &o, const RowShape &sh, cudaStream_t stream);
 
@@ -96,6 +98,11 @@ const void *moe_reduce_kernel_fn(int in_fmt);
 const void *moe_reduce_bulk_kernel_fn(int in_fmt);
 cudaError_t launch_moe_reduce(const void *fn, int grid, int block, int smem, const ReduceArgs &a,
                               cudaStream_t stream);
+
+// Bytes of one input row per column of H, for the block-ring kernel.
+constexpr int kSwigluRowBytesPerCol = SwigluSrc<false>::kRowBytesPerCol;
+constexpr int kCastBf16RowBytesPerCol = CastBf16Src::kRowBytesPerCol;
+constexpr int kCastF32RowBytesPerCol = CastF32Src::kRowBytesPerCol;
 
 // Bytes of one warp-ring slot of the stream kernels.
 constexpr int kSwigluSlotBytes = SwigluSrc<false>::kSpans * SwigluSrc<false>::kSpanBytes;

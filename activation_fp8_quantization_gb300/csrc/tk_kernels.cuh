@@ -650,6 +650,139 @@ warp_stream_kernel(typename Src::Args a, OutArgs o, RowShape sh)
     src.finish(a);
 }
 
+// ---------------------------------------------------- block_stream_kernel
+
+constexpr int kBlockConsumerWarps = 8;
+constexpr int kBlockThreads = 32 * (kBlockConsumerWarps + 1);   // + 1 producer warp
+
+// Src additionally supplies kRowBytesPerCol (bytes of one input row per
+// column of H) and fetch_block(row, H, s, lane, regs): the lane's bytes of
+// the row's 512-column slice s from a whole row held in shared memory.
+//
+// The CTA's kBlockConsumerWarps consumer warps share one ring of `stages`
+// slots; a slot holds sh.rpc consecutive whole rows of the input, which lie
+// contiguously in memory, so one TMA bulk copy by the producer warp (the
+// last warp, one lane) fills it. CTA b takes row blocks b, b + grid, ...;
+// a block's rpc * wpr tasks (a task: one 512-column slice of one row) go to
+// the consumer warps in turn, and the count runs on across blocks (task t of
+// the CTA -> warp t % kBlockConsumerWarps). full[s] completes when the copy
+// has landed; empty[s] takes one arrival per task, so it completes once every
+// task of the block has been read out of the slot. The plan keeps
+// rpc * wpr >= kBlockConsumerWarps: every warp then has a task in every full
+// block, so no warp can get a whole ring ahead of a barrier's phase.
+// Against warp_stream_kernel this moves the copies off the consumer warps
+// and makes them one per block instead of two per slice.
+template <class Src, int OUT, int SCALE>
+__global__ void __launch_bounds__(kBlockThreads, 3)
+block_stream_kernel(typename Src::Args a, OutArgs o, RowShape sh)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = sh.stages;
+    const int RB = sh.rpc;
+    const uint32_t row_bytes = (uint32_t)Src::kRowBytesPerCol * (uint32_t)sh.H;
+    const uint32_t slot_bytes = (uint32_t)RB * row_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * slot_bytes);
+    uint64_t *empty = full + S;
+    const int64_t nblk = (sh.T + RB - 1) / RB;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, (uint32_t)(RB * sh.wpr));
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_launch_dependents();
+
+    if (warp == kBlockConsumerWarps) {
+        // ------------------------------------------------------ producer
+        if (lane != 0)
+            return;
+        int slot = 0;
+        uint32_t par = 0;   // parity of the slot's current use
+        int64_t issued = 0;
+        for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+            // the slot's previous block must have been read out entirely
+            if (issued >= S && !mbar_wait_bounded(empty + slot, par ^ 1u)) {
+                atomicOr(sh.fault, 1u);
+                break;
+            }
+            const int64_t row0 = blk * RB;
+            const int64_t left = sh.T - row0;
+            const uint32_t bytes = (uint32_t)(left < RB ? left : RB) * row_bytes;
+            mbar_arrive_expect_tx(full + slot, bytes);
+            bulk_g2s(smem + (size_t)slot * slot_bytes, Src::span(a, row0, 0, 0), bytes, full + slot);
+            ++issued;
+            if (++slot == S) {
+                slot = 0;
+                par ^= 1u;
+            }
+        }
+        // every copy this CTA issued lands before its shared memory goes away
+        for (int s = 0; s < S && s < issued; ++s) {
+            const int64_t last_use = (issued - 1 - s) / S;
+            if (!mbar_wait_bounded(full + s, (uint32_t)(last_use & 1)))
+                atomicOr(sh.fault, 1u);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    Src src;
+    const int wpr = sh.wpr;
+    const int tpg_mask = (1 << sh.tpg_log2) - 1;
+    const int d_rl = kBlockConsumerWarps / wpr;   // the step of kBlockConsumerWarps tasks
+    const int d_s = kBlockConsumerWarps - d_rl * wpr;
+    int rl = warp / wpr;   // row within the block
+    int s = warp - rl * wpr;   // slice within the row
+    int slot = 0;
+    uint32_t par = 0;
+    int64_t row0 = (int64_t)blockIdx.x * RB;
+    const int64_t row_step = (int64_t)gridDim.x * RB;
+    while (row0 + rl < sh.T) {
+        const int64_t row = row0 + rl;
+        const float *wp = Src::scalar(a, row);
+        const float w = wp ? __ldg(wp) : 1.0f;
+        if (!mbar_wait_bounded(full + slot, par)) {
+            if (lane == 0)
+                atomicOr(sh.fault, 1u);
+            return;
+        }
+        typename Src::Regs regs;
+        Src::fetch_block(smem + (size_t)slot * slot_bytes + (size_t)rl * row_bytes, sh.H, s, lane, regs);
+        Src::set_scalar(regs, w);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(empty + slot);
+
+        uint64_t ny[kEPT / 2];
+        float amax = 0.0f;
+        src.produce(a, regs, true, ny, amax);
+        amax = group_max(amax, tpg_mask);
+        const int lr = s * 32 + lane;   // the lane's 16-column unit within the row
+        quantize_store<OUT, SCALE>(ny, amax, row, lr * kEPT, lr >> sh.tpg_log2, (lr & tpg_mask) == 0, sh, o);
+
+        s += d_s;
+        if (s >= wpr) {
+            s -= wpr;
+            ++rl;
+        }
+        rl += d_rl;
+        if (rl >= RB) {   // at most one block further: rpc * wpr >= kBlockConsumerWarps
+            rl -= RB;
+            row0 += row_step;
+            if (++slot == S) {
+                slot = 0;
+                par ^= 1u;
+            }
+        }
+    }
+    src.finish(a);
+}
+
 // ------------------------------------------------------------ sources
 
 struct SwigluArgs {
@@ -731,8 +864,19 @@ struct SwigluSrc {
     }
     __device__ __forceinline__ static void fetch_span(const uint8_t *slot, int lane, Regs &r)
     {
-        const uint4 *g = reinterpret_cast<const uint4 *>(slot + lane * 32);
-        const uint4 *u = reinterpret_cast<const uint4 *>(slot + 1024 + lane * 32);
+        fetch_pair(slot + lane * 32, slot + 1024 + lane * 32, r);
+    }
+    // block_stream_kernel: a whole row (H gate columns, then H up columns)
+    // sits in shared memory; the lane's 16 columns of its 512-column slice s
+    static constexpr int kRowBytesPerCol = 4;
+    __device__ __forceinline__ static void fetch_block(const uint8_t *row, int H, int s, int lane, Regs &r)
+    {
+        fetch_pair(row + s * 1024 + lane * 32, row + 2 * H + s * 1024 + lane * 32, r);
+    }
+    __device__ __forceinline__ static void fetch_pair(const uint8_t *gp, const uint8_t *up, Regs &r)
+    {
+        const uint4 *g = reinterpret_cast<const uint4 *>(gp);
+        const uint4 *u = reinterpret_cast<const uint4 *>(up);
         const uint4 g0 = g[0], g1 = g[1], u0 = u[0], u1 = u[1];
         r.g[0] = g0.x; r.g[1] = g0.y; r.g[2] = g0.z; r.g[3] = g0.w;
         r.g[4] = g1.x; r.g[5] = g1.y; r.g[6] = g1.z; r.g[7] = g1.w;
@@ -828,6 +972,11 @@ struct CastBf16Src {
         return static_cast<const uint16_t *>(a.x) + row * (int64_t)a.H + cbase;
     }
     __device__ __forceinline__ static const float *scalar(const Args &, int64_t) { return nullptr; }
+    static constexpr int kRowBytesPerCol = 2;
+    __device__ __forceinline__ static void fetch_block(const uint8_t *row, int, int s, int lane, Regs &r)
+    {
+        fetch_span(row + s * kSpanBytes, lane, r);
+    }
     __device__ __forceinline__ static void fetch_span(const uint8_t *slot, int lane, Regs &r)
     {
         const uint4 *p = reinterpret_cast<const uint4 *>(slot + lane * 32);
@@ -876,6 +1025,11 @@ struct CastF32Src {
         return static_cast<const float *>(a.x) + row * (int64_t)a.H + cbase;
     }
     __device__ __forceinline__ static const float *scalar(const Args &, int64_t) { return nullptr; }
+    static constexpr int kRowBytesPerCol = 4;
+    __device__ __forceinline__ static void fetch_block(const uint8_t *row, int, int s, int lane, Regs &r)
+    {
+        fetch_span(row + s * kSpanBytes, lane, r);
+    }
     __device__ __forceinline__ static void fetch_span(const uint8_t *slot, int lane, Regs &r)
     {
         const uint4 *p = reinterpret_cast<const uint4 *>(slot + lane * 64);

@@ -23,7 +23,22 @@ const void *stream_fn(bool clamp)
     return clamp ? reinterpret_cast<const void *>(&warp_stream_kernel<SwigluSrc<true>, OUT, SCALE>)
                  : reinterpret_cast<const void *>(&warp_stream_kernel<SwigluSrc<false>, OUT, SCALE>);
 }
+template <int OUT, int SCALE>
+const void *block_fn(bool clamp)
+{
+    return clamp ? reinterpret_cast<const void *>(&block_stream_kernel<SwigluSrc<true>, OUT, SCALE>)
+                 : reinterpret_cast<const void *>(&block_stream_kernel<SwigluSrc<false>, OUT, SCALE>);
+}
 }  // namespace
+
+const void *swiglu_block_fn(int out_fmt, int scale_fmt, bool clamp)
+{
+    if (out_fmt == kOutE4M3)
+        return scale_fmt == kScaleF32 ? block_fn<kOutE4M3, kScaleF32>(clamp) : block_fn<kOutE4M3, kScaleUE8M0>(clamp);
+    if (out_fmt == kOutE2M1)
+        return scale_fmt == kScaleF32 ? block_fn<kOutE2M1, kScaleF32>(clamp) : block_fn<kOutE2M1, kScaleUE8M0>(clamp);
+    return nullptr;
+}
 
 const void *swiglu_stream_fn(int out_fmt, int scale_fmt, bool clamp)
 {

@@ -467,7 +467,7 @@ def run_ours(args, dist: Dist):
     if transposed:
         kernel = "transpose_quant_kernel"
     elif wl.op == "swiglu":
-        kernel = "warp_stream_kernel" if op.launch_info(T)["rows_per_cta"] == 0 else "row_quant_kernel"
+        kernel = op.launch_info(T)["kernel"]
     line = {
         "metric": metric_of(wl), "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

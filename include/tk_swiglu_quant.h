@@ -175,12 +175,22 @@ tk_status tk_swiglu_quant_run_transposed(tk_swiglu_quant_plan_t plan, int64_t nu
                                          int64_t *clamped_count, void *stream);
 
 /* Launch shape a run of num_tokens rows would use (host only): CTAs in the
- * persistent grid, threads per CTA, rows one CTA processes per iteration (0
- * when the warp-stream kernel runs: each warp then streams 512-column
- * slices), and the SM count. A plan holds two kernels where the width is a
- * multiple of 512 and picks one per run by num_tokens. */
+ * persistent grid, threads per CTA, rows one CTA takes per iteration (the
+ * rows of one ring slot for the block-ring kernel; 0 for the warp-stream
+ * kernel, whose warps each stream 512-column slices), the SM count, and which
+ * kernel (TK_KERNEL_ROWS, TK_KERNEL_WARP_STREAM or TK_KERNEL_BLOCK_RING). Any
+ * output pointer may be NULL. Where the width is a multiple of 512 a plan
+ * holds the stream kernels too and picks per run by num_tokens: the block-ring
+ * kernel once every resident CTA has at least 12 row blocks to stream (4 with
+ * the clamp, whose extra arithmetic the row kernel hides less well), the row
+ * kernel below that. */
+typedef enum tk_kernel_kind {
+    TK_KERNEL_ROWS = 0,         /* row_quant_kernel: register-prefetch row blocks, any width */
+    TK_KERNEL_WARP_STREAM = 1,  /* warp_stream_kernel: a TMA ring per warp */
+    TK_KERNEL_BLOCK_RING = 2    /* block_stream_kernel: one TMA ring per CTA, whole rows per slot */
+} tk_kernel_kind;
 tk_status tk_swiglu_quant_launch_info(tk_swiglu_quant_plan_t plan, int64_t num_tokens,
-                                      int *grid, int *block, int *rows_per_cta, int *num_sms);
+                                      int *grid, int *block, int *rows_per_cta, int *num_sms, int *kernel);
 
 /* ------------------------------------------------------------------------
  * Host-buffer variant of the fused call

@@ -26,7 +26,7 @@ def _rows_near(row_bytes, T):
     return np.array(sorted(rows))
 
 
-@pytest.mark.parametrize("kernel", ["rows", "stream"])
+@pytest.mark.parametrize("kernel", ["rows", "stream", "block"])
 def test_fused_op_past_4_gib(kernel, monkeypatch):
     monkeypatch.setenv("TK_KERNEL", kernel)
     wl = wls.WORKLOADS["moe_T8192_H2048_g128"].with_rows(540_000)   # x: 4.42 GB

@@ -36,8 +36,9 @@ def _oracle(wl, x_cpu, w_cpu):
 
 
 def _rows_for_two_passes(op):
-    """Rows that make every CTA (row kernel) or every warp (stream kernel) of
-    the full grid take two steps, plus a ragged tail."""
+    """Rows that make every CTA (row kernel: rows per iteration; block-ring
+    kernel: rows per ring slot) or every warp (warp-stream kernel) of the full
+    grid take two steps, plus a ragged tail."""
     info = op.launch_info(1 << 30)
     if info["rows_per_cta"]:
         return 2 * info["grid"] * info["rows_per_cta"] + 37
@@ -45,7 +46,7 @@ def _rows_for_two_passes(op):
     return 2 * info["grid"] * (info["block"] // 32) // wpr + 37
 
 
-@pytest.mark.parametrize("kernel", ["rows", "stream"])
+@pytest.mark.parametrize("kernel", ["rows", "stream", "block"])
 @pytest.mark.parametrize("name", wls.ORDER)
 def test_workload_small_parity(name, kernel, monkeypatch):
     monkeypatch.setenv("TK_KERNEL", kernel)
@@ -115,7 +116,7 @@ GEOMS = [  # (H, group) incl. the CTA-reduction path (one scale per row, wide or
 ]
 
 
-@pytest.mark.parametrize("kernel", ["rows", "stream"])
+@pytest.mark.parametrize("kernel", ["rows", "stream", "block"])
 @pytest.mark.parametrize("H,group", GEOMS)
 @pytest.mark.parametrize("scale_fmt,out_fmt", [("fp32", "e4m3"), ("ue8m0", "e4m3"),
                                                ("ue8m0", "e2m1"), ("fp32", "e2m1")])
@@ -140,7 +141,7 @@ def _bf16(a):
     return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("kernel", ["rows", "stream"])
+@pytest.mark.parametrize("kernel", ["rows", "stream", "block"])
 def test_special_rows(kernel, monkeypatch):
     monkeypatch.setenv("TK_KERNEL", kernel)
     H, g = 512, 128
@@ -253,7 +254,7 @@ def test_host_side_errors():
 
 # ----------------------------------------------------- standalone cast
 
-@pytest.mark.parametrize("kernel", ["rows", "stream"])
+@pytest.mark.parametrize("kernel", ["rows", "stream", "block"])
 @pytest.mark.parametrize("in_dtype", ["fp32", "bf16"])
 @pytest.mark.parametrize("H,group", [(2048, 128), (512, 0), (7168, 0), (1024, 32), (48, 16)])
 @pytest.mark.parametrize("scale_fmt,out_fmt", [("fp32", "e4m3"), ("ue8m0", "e4m3"),
@@ -363,16 +364,32 @@ def test_host_pipe_errors():
 
 # ------------------------------------------- both kernels on the same shapes
 
-def test_plan_picks_the_kernel_by_batch_size():
-    # rows_per_cta == 0 marks the warp-stream kernel. It applies to widths
-    # that are multiples of 512 whose scale groups fit in a warp's 512
-    # columns, and runs once every resident warp has >= 16 slices to stream.
+def test_plan_picks_the_kernel_by_batch_size(monkeypatch):
+    # The block-ring kernel applies to widths that are multiples of 512 whose
+    # scale groups fit in 512 columns, and runs once every resident CTA has
+    # >= 12 row blocks to stream (>= 4 with the clamp); the row kernel runs
+    # everything else.
     op = tk.SwigluQuant(2048, 128)
-    assert op.launch_info(1024)["rows_per_cta"] > 0
-    assert op.launch_info(65536)["rows_per_cta"] == 0
-    assert tk.SwigluQuant(512, 0).launch_info(1 << 20)["rows_per_cta"] == 0
-    assert tk.SwigluQuant(4096, 0).launch_info(1 << 20)["rows_per_cta"] == 1    # CTA reduction
-    assert tk.SwigluQuant(1040, 16).launch_info(1 << 20)["rows_per_cta"] > 0
+    small, big = op.launch_info(1024), op.launch_info(65536)
+    assert op.launch_info(8192)["kernel"] == "row_quant_kernel"
+    clamped = tk.SwigluQuant(2048, 128, "ue8m0", "e4m3", True, 7.0)
+    assert clamped.launch_info(8192)["kernel"] == "block_stream_kernel"
+    assert clamped.launch_info(1024)["kernel"] == "row_quant_kernel"
+    assert small["kernel"] == "row_quant_kernel" and small["rows_per_cta"] > 0
+    assert big["kernel"] == "block_stream_kernel" and big["block"] == 288
+    assert big["rows_per_cta"] * 4 >= 8          # at least one slice per consumer warp in a block
+    assert big["grid"] % big["num_sms"] == 0
+    assert tk.SwigluQuant(512, 0).launch_info(1 << 20)["kernel"] == "block_stream_kernel"
+    info = tk.SwigluQuant(4096, 0).launch_info(1 << 20)    # per-token scales: a CTA-wide reduction
+    assert info["kernel"] == "row_quant_kernel" and info["rows_per_cta"] == 1
+    assert tk.SwigluQuant(1040, 16).launch_info(1 << 20)["kernel"] == "row_quant_kernel"
+    # forcing a kernel (read when the plan is made)
+    monkeypatch.setenv("TK_KERNEL", "stream")
+    info = tk.SwigluQuant(2048, 128).launch_info(1024)
+    assert info["kernel"] == "warp_stream_kernel" and info["rows_per_cta"] == 0
+    monkeypatch.setenv("TK_KERNEL", "block")
+    assert tk.SwigluQuant(2048, 128).launch_info(1024)["kernel"] == "block_stream_kernel"
+    assert tk.SwigluQuant(1040, 16).launch_info(1024)["kernel"] == "row_quant_kernel"   # does not apply
 
 
 def test_back_to_back_launches_see_the_previous_output():
@@ -423,7 +440,7 @@ def test_fault_word_clear_after_runs():
 
 # ------------------------------------------------------------ scale layouts
 
-@pytest.mark.parametrize("kernel", ["rows", "stream"])
+@pytest.mark.parametrize("kernel", ["rows", "stream", "block"])
 @pytest.mark.parametrize("layout,scale_fmt,group,out_fmt", [
     ("col", "fp32", 128, "e4m3"), ("col", "ue8m0", 128, "e4m3"), ("col_packed", "ue8m0", 128, "e4m3"),
     ("col_packed", "ue8m0", 32, "e2m1"), ("col", "fp32", 0, "e4m3")])
