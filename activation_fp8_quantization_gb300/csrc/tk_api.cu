@@ -303,19 +303,26 @@ struct Launches {
 };
 
 // Where the block-ring kernel overtakes the row kernel, whose register
-// prefetch starts up faster but which spends more instructions per element.
-// Measured on GB300 at width 2048 (4 rows per block, 456 CTAs), µs row kernel
-// / block kernel:
-//   fp32 scales, no clamp:  8192 rows 15.3/18.1, 16384 28.6/29.3, 24576 42.1/41.1
-//   UE8M0, clamp 7:         8192 rows 19.7/18.8, 16384 35.4/31.5, 32768 68.4/58.1
-//   FP4 1x32, clamp 7:      16384 rows 34.1/30.5
-// so about 12 blocks per CTA without the clamp and 4 with it (its extra
-// arithmetic is what the row kernel cannot hide). The standalone cast, with a
+// prefetch starts up faster: the row blocks per resident CTA from which the
+// block kernel runs. Measured on GB300 (µs, row kernel / block kernel):
+//   width 2048 (two rows per row-kernel CTA; 4 rows per block, 456 CTAs):
+//     fp32 scales, no clamp: 16384 rows 27.5/29.4, 32768 52.6/53.6, 65536 102.3/102.2
+//     UE8M0, clamp 7:        16384 rows 30.7/31.6, 32768 58.8/58.3, 65536 114.1/111.3
+//     FP4 1x32, clamp 7:     16384 rows 29.6/30.6, 65536 109.5/107.0
+//   width 3072 (one row per row-kernel CTA; 2 rows per block):
+//     fp32 scales, no clamp: 25000 rows 62.5/60.4, 100003 240.5/223.9
+// so about 32 blocks per CTA without the clamp and 16 with it where the row
+// kernel packs two or more rows per CTA, and 8 where it holds one row per CTA
+// (wide rows, which it runs less efficiently). The standalone cast, with a
 // third of the fused op's arithmetic per byte, was faster on the row kernel at
 // every size tried (8192 x 4096 and 16384 x 7168), so its plans never pick the
 // block kernel.
-constexpr int64_t kBlockMinPerCtaPlain = 12;
-constexpr int64_t kBlockMinPerCtaClamp = 4;
+int64_t block_min_per_cta(const Launch &rows, bool clamp)
+{
+    if (rows.rpc < 2)
+        return 8;
+    return clamp ? 16 : 32;
+}
 
 const Launch &pick(const Launches &Ls, int64_t T)
 {
@@ -500,7 +507,7 @@ TK_API tk_status tk_swiglu_quant_plan(const tk_swiglu_quant_desc *d, int device,
                        tk::kSwigluRowBytesPerCol, &Ls);
     if (st != TK_OK)
         return st;
-    Ls.block_min = clamp ? kBlockMinPerCtaClamp : kBlockMinPerCtaPlain;
+    Ls.block_min = block_min_per_cta(Ls.rows, clamp);
     // The transposed-codes kernel: E4M3, groups of 32, 64 or 128 columns
     // inside its 128-column tiles.
     const void *tfn = nullptr;

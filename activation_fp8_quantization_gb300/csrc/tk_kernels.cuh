@@ -481,20 +481,25 @@ row_quant_kernel(typename Src::Args a, OutArgs o, RowShape sh)
     const bool first_of_group = CTA_REDUCE ? (tid == 0) : ((lr & tpg_mask) == 0);
     pdl_wait();
     pdl_launch_dependents();
-    typename Src::Regs cur, nxt;
-    int64_t rb = blockIdx.x;
-    int64_t row = rb * sh.rpc + slot;
-    bool ok = slot_ok && rb < nrb && row < sh.T;
-    if (ok) Src::load(a, row, col0, cur); else Src::zero(cur);
+    // Two register sets in turn: while one row block is computed, the next
+    // one's loads land in the other set (no register copies between them).
+    typename Src::Regs ra, rb_regs;
+    const int64_t step = gridDim.x;
+    auto row_of = [&](int64_t b) { return b * sh.rpc + slot; };
+    auto valid = [&](int64_t b) { return slot_ok && b < nrb && row_of(b) < sh.T; };
+    auto fetch = [&](int64_t b, typename Src::Regs &r) {
+        if (valid(b))
+            Src::load(a, row_of(b), col0, r);
+        else
+            Src::zero(r);
+    };
     int it = 0;
-    for (; rb < nrb; rb += gridDim.x, ++it) {
-        const int64_t nrow = (rb + gridDim.x) * sh.rpc + slot;
-        const bool nok = slot_ok && (rb + gridDim.x) < nrb && nrow < sh.T;
-        if (nok) Src::load(a, nrow, col0, nxt); else Src::zero(nxt);
+    auto compute = [&](int64_t b, const typename Src::Regs &r) {
+        const int64_t row = row_of(b);
+        const bool ok = valid(b);
         uint64_t ny[kEPT / 2];
         float amax = 0.0f;
-        src.produce(a, cur, ok, ny, amax);
-
+        src.produce(a, r, ok, ny, amax);
         if (CTA_REDUCE) {
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1)
@@ -512,7 +517,19 @@ row_quant_kernel(typename Src::Args a, OutArgs o, RowShape sh)
         }
         if (ok)
             quantize_store<OUT, SCALE>(ny, amax, row, col0, group_idx, first_of_group, sh, o);
-        cur = nxt; row = nrow; ok = nok;
+        ++it;
+    };
+    int64_t b = blockIdx.x;
+    fetch(b, ra);
+    while (b < nrb) {
+        fetch(b + step, rb_regs);
+        compute(b, ra);
+        b += step;
+        if (b >= nrb)
+            break;
+        fetch(b + step, ra);
+        compute(b, rb_regs);
+        b += step;
     }
     src.finish(a);
 }

@@ -181,9 +181,9 @@ tk_status tk_swiglu_quant_run_transposed(tk_swiglu_quant_plan_t plan, int64_t nu
  * kernel (TK_KERNEL_ROWS, TK_KERNEL_WARP_STREAM or TK_KERNEL_BLOCK_RING). Any
  * output pointer may be NULL. Where the width is a multiple of 512 a plan
  * holds the stream kernels too and picks per run by num_tokens: the block-ring
- * kernel once every resident CTA has at least 12 row blocks to stream (4 with
- * the clamp, whose extra arithmetic the row kernel hides less well), the row
- * kernel below that. */
+ * kernel once every resident CTA has enough row blocks to stream (32, or 16
+ * with the clamp, where the row kernel packs two or more rows per CTA; 8 for
+ * wider rows), the row kernel below that. */
 typedef enum tk_kernel_kind {
     TK_KERNEL_ROWS = 0,         /* row_quant_kernel: register-prefetch row blocks, any width */
     TK_KERNEL_WARP_STREAM = 1,  /* warp_stream_kernel: a TMA ring per warp */

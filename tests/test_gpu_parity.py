@@ -367,14 +367,15 @@ def test_host_pipe_errors():
 def test_plan_picks_the_kernel_by_batch_size(monkeypatch):
     # The block-ring kernel applies to widths that are multiples of 512 whose
     # scale groups fit in 512 columns, and runs once every resident CTA has
-    # >= 12 row blocks to stream (>= 4 with the clamp); the row kernel runs
-    # everything else.
+    # enough row blocks to stream (at width 2048: 32, or 16 with the clamp;
+    # 8 at width 3072); the row kernel runs everything else.
     op = tk.SwigluQuant(2048, 128)
     small, big = op.launch_info(1024), op.launch_info(65536)
-    assert op.launch_info(8192)["kernel"] == "row_quant_kernel"
+    assert op.launch_info(32768)["kernel"] == "row_quant_kernel"
     clamped = tk.SwigluQuant(2048, 128, "ue8m0", "e4m3", True, 7.0)
-    assert clamped.launch_info(8192)["kernel"] == "block_stream_kernel"
-    assert clamped.launch_info(1024)["kernel"] == "row_quant_kernel"
+    assert clamped.launch_info(32768)["kernel"] == "block_stream_kernel"
+    assert clamped.launch_info(16384)["kernel"] == "row_quant_kernel"
+    assert tk.SwigluQuant(3072, 128).launch_info(25000)["kernel"] == "block_stream_kernel"
     assert small["kernel"] == "row_quant_kernel" and small["rows_per_cta"] > 0
     assert big["kernel"] == "block_stream_kernel" and big["block"] == 288
     assert big["rows_per_cta"] * 4 >= 8          # at least one slice per consumer warp in a block
