@@ -21,7 +21,7 @@ from ._abi import (IN_DTYPES, OUT_FMTS, REDUCE_IN_FMTS, SCALE_FMTS, SCALE_LAYOUT
                    QuantCastDesc, SwigluBackwardDesc, SwigluQuantDesc, tk_swiglu_backward_plan,
                    tk_swiglu_backward_plan_destroy, tk_swiglu_backward_run, tk_swiglu_backward_validate, tk_moe_reduce_plan, tk_moe_reduce_plan_destroy,
                    tk_moe_reduce_launch_info, tk_moe_reduce_run, tk_moe_reduce_validate,
-                   TkError, tk_fault_word, tk_last_error_message, tk_quant_cast_output_sizes,
+                   TkError, tk_diag_unanswered_wait, tk_fault_word, tk_last_error_message, tk_quant_cast_output_sizes,
                    tk_quant_cast_plan, tk_quant_cast_plan_destroy,
                    tk_quant_cast_run, tk_quant_cast_validate, tk_status_string,
                    tk_swiglu_quant_host_pipe_create, tk_swiglu_quant_host_pipe_destroy,
@@ -46,7 +46,7 @@ __all__ = [
     "tk_swiglu_quant_run_mapped",
     "tk_quant_cast_validate", "tk_quant_cast_plan",
     "tk_quant_cast_plan_destroy", "tk_quant_cast_output_sizes", "tk_quant_cast_run", "tk_status_string",
-    "tk_last_error_message", "tk_fault_word",
+    "tk_last_error_message", "tk_fault_word", "tk_diag_unanswered_wait",
 ]
 
 

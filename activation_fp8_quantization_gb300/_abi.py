@@ -98,6 +98,7 @@ SIGNATURES = {
     "tk_swiglu_backward_plan_destroy": (ctypes.c_int, [_VP]),
     "tk_swiglu_backward_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "tk_fault_word": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
+    "tk_diag_unanswered_wait": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint32, _VP]),
     "tk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tk_last_error_message": (ctypes.c_char_p, []),
 }
@@ -312,6 +313,10 @@ def tk_fault_word(device: int, clear: bool = False) -> int:
     v = ctypes.c_uint32()
     check(lib().tk_fault_word(device, ctypes.byref(v), int(clear)))
     return v.value
+
+
+def tk_diag_unanswered_wait(device: int, tries: int, stream=None) -> None:
+    check(lib().tk_diag_unanswered_wait(device, tries, stream))
 
 
 def tk_status_string(status: int) -> str:

@@ -1522,6 +1522,22 @@ TK_API tk_status tk_fault_word(int device, uint32_t *value, int clear)
 }
 
 
+TK_API tk_status tk_diag_unanswered_wait(int device, uint32_t tries, void *stream)
+{
+    if (tries == 0 || tries > (1u << 22))
+        return fail(TK_ERR_INVALID_ARG, "tries must be in [1, 2^22] (got %u)", tries);
+    tk_status st = check_current_device(device);
+    if (st != TK_OK)
+        return st;
+    void *fault = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&fault, g_tk_fault_word);
+    if (e == cudaSuccess)
+        e = tk::launch_unanswered_wait(static_cast<unsigned *>(fault), tries, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launch of the unanswered-wait kernel");
+    return ok();
+}
+
 TK_API const char *tk_status_string(tk_status s)
 {
     switch (s) {

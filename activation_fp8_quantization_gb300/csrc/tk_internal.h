@@ -94,6 +94,10 @@ const void *backward_kernel_fn(bool clamp, bool recompute, int out_fmt, int scal
 cudaError_t launch_backward(const void *fn, int grid, int block, const BackwardArgs &a, const OutArgs &o,
                             const RowShape &sh, cudaStream_t stream);
 
+// One thread waits on an mbarrier nothing arrives at for `tries` tries, then
+// sets bit 0 of *fault (the bounded waits' failure path, for tests).
+cudaError_t launch_unanswered_wait(unsigned *fault, uint32_t tries, cudaStream_t stream);
+
 const void *moe_reduce_kernel_fn(int in_fmt);
 const void *moe_reduce_bulk_kernel_fn(int in_fmt);
 cudaError_t launch_moe_reduce(const void *fn, int grid, int block, int smem, const ReduceArgs &a,

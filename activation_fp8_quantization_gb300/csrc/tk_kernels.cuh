@@ -177,17 +177,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return done != 0;
 }
 
-// Each try_wait suspends for a hardware-chosen interval; this many tries is
-// far beyond any legitimate copy (well over a second), after which the
-// kernel gives up on the barrier instead of spinning forever.
-constexpr uint32_t kSpinLimit = 1u << 22;
+// Each try_wait on a phase that does not complete suspends the thread for a
+// hardware-chosen interval (3.5 us on GB300, measured with
+// tk_diag_unanswered_wait), so this many tries take about 1.8 s: far beyond
+// any legitimate copy, after which the kernel gives up on the barrier instead
+// of waiting forever.
+constexpr uint32_t kSpinLimit = 1u << 19;
 
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+__device__ __forceinline__ bool mbar_wait_tries(uint64_t *bar, uint32_t parity, uint32_t tries)
 {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
+    for (uint32_t i = 0; i < tries; ++i)
         if (mbar_try_wait(bar, parity))
             return true;
     return false;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+{
+    return mbar_wait_tries(bar, parity, kSpinLimit);
 }
 
 // ---------------------------------------------------------------- arithmetic

@@ -7,7 +7,8 @@
  *   tk_quant_cast_*       the standalone per-token / per-block cast
  *   tk_moe_reduce_*       the weighted top-k combine after the expert GEMMs
  *   tk_swiglu_backward_*  the SwiGLU backward, optionally recomputing the codes
- *   tk_fault_word, tk_status_string, tk_last_error_message   diagnostics
+ *   tk_fault_word, tk_diag_unanswered_wait, tk_status_string,
+ *   tk_last_error_message                                     diagnostics
  *
  * The operation ("TileKernels从入门到精通" / "TileKernels from Beginner to
  * Master", zhichai.net/topic/177618752 and zhichai.net/en/topic/177618752,
@@ -446,6 +447,16 @@ tk_status tk_swiglu_backward_run(tk_swiglu_backward_plan_t plan, int64_t num_tok
  * shared by every call on the device; the read is ordered after all work
  * already submitted to the device (it synchronises with it). */
 tk_status tk_fault_word(int device, uint32_t *value, int clear);
+
+/* Exercise the failure path of the kernels' bounded waits (not part of the
+ * pages' method): one thread of one CTA waits on a shared-memory mbarrier that
+ * nothing arrives at, gives up after `tries` (1 ... 2^22) tries of
+ * mbarrier.try_wait exactly as the library's kernels do, sets bit 0 of the
+ * fault word and returns, with nothing left in flight. Stream-ordered on
+ * `stream`; `device` must be the current device (TK_ERR_DEVICE otherwise).
+ * The library's kernels give up after 2^19 tries (about 1.8 s on GB300, where
+ * an unanswered try takes 3.5 us). */
+tk_status tk_diag_unanswered_wait(int device, uint32_t tries, void *stream);
 
 /* Static name of a status ("TK_OK", ...). Never NULL. */
 const char *tk_status_string(tk_status status);

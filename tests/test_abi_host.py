@@ -164,3 +164,11 @@ def test_backward_validate():
     assert v(B(16384, 1, 0, 0.0, 0, 0, 0, 0, 0)) == 2      # above 8192
     assert v(B(2048, 1, 0, 0.0, 1, 0, 0, 0, 0)) == 2       # recompute needs a group size
     assert v(B(2048, 1, 0, 0.0, 1, 128, 0, 0, 2)) == 2     # packed layout needs UE8M0
+
+
+def test_unanswered_wait_rejects_tries_out_of_range():
+    # checked on the host before any device is touched
+    for tries in (0, (1 << 22) + 1):
+        with pytest.raises(tk.TkError) as e:
+            tk.tk_diag_unanswered_wait(0, tries, None)
+        assert e.value.status == 1
