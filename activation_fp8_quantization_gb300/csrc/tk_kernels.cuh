@@ -59,11 +59,11 @@ struct RowShape {
     int32_t H;          // columns of the activation
     int32_t tpr;        // threads per row = H / 16
     int32_t tpg_log2;   // log2(threads per group); unused by the CTA-reduction variant
-    int32_t rpc;        // rows per CTA per iteration
+    int32_t rpc;        // rows per CTA per iteration (block_stream_kernel: rows per ring slot)
     int32_t groups;     // scales per row
-    int32_t stages;     // warp_stream_kernel: slots per warp ring (>= 2)
-    int32_t wpr;        // warp_stream_kernel: warps (512-column slices) per row
-    unsigned *fault;    // warp_stream_kernel: device word, bit 0 set if a wait gave up
+    int32_t stages;     // stream kernels: ring slots per warp (warp_stream) or per CTA (block_stream), >= 2
+    int32_t wpr;        // stream kernels: 512-column slices per row
+    unsigned *fault;    // device word: bit 0 set by a kernel whose bounded wait gave up
     int32_t scale_layout;  // 0 row-major [T, G]; 1 column-major [G, ld]; 2 packed UE8M0 words [G/4, ld]
     int64_t scale_ld;      // column-major layouts: padded rows per column (elements or words)
 };

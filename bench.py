@@ -703,17 +703,43 @@ def run_backward(args, dist, wl, dev, n_sets):
     return 0
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments, whitespace runs collapsed to one
+    space (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
-    """sha256 over the device-code sources (the kernel files and the headers
-    they include; not the host-side API in tk_api.cu), to tell whether a
-    committed ncu summary still describes the kernel that runs."""
+    """sha256 over the device code (the kernel files and the headers they
+    include, comments and layout left out; not the host-side API in
+    tk_api.cu), to tell whether a committed ncu summary still describes the
+    kernel that runs."""
     import hashlib
     csrc = os.path.join(ROOT, "activation_fp8_quantization_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")) and name != "tk_api.cu":
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()
 
 
