@@ -1,0 +1,25 @@
+"""Host-side helpers of bench.py that need no GPU: the device-code hash that
+decides whether a committed ncu summary still describes the running kernels."""
+import bench
+
+
+def test_code_only_drops_comments_and_layout_but_keeps_literals():
+    src = 'int a = 1;   // note\n/* block\n comment */  asm("x // y"); char c = \'/\';\nint  b;'
+    assert bench._code_only(src) == 'int a = 1; asm("x // y"); char c = \'/\'; int b;'
+    # an escaped quote does not end a string literal
+    assert bench._code_only('s = "a\\" // b"; // c') == 's = "a\\" // b";'
+
+
+def test_hash_is_stable_under_comment_edits(tmp_path, monkeypatch):
+    csrc = tmp_path / "activation_fp8_quantization_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("__global__ void k() { int a = 1; }\n")
+    (csrc / "tk_api.cu").write_text("int host_side = 0;\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    (csrc / "k.cu").write_text("// a kernel\n__global__ void k() {\n    int a = 1;   /* one */\n}\n")
+    assert bench.kernel_source_hash() == h0
+    (csrc / "tk_api.cu").write_text("int host_side = 1;\n")        # host code is not hashed
+    assert bench.kernel_source_hash() == h0
+    (csrc / "k.cu").write_text("__global__ void k() { int a = 2; }\n")
+    assert bench.kernel_source_hash() != h0
