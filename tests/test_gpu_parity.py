@@ -489,3 +489,35 @@ def test_host_pipe_refuses_column_major_scales():
         pipe(torch.zeros(8, 4096, dtype=torch.bfloat16), torch.ones(8),
              q=torch.empty(8, 2048, dtype=torch.uint8), scales=torch.empty(op.output_shapes(8)[1]))
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("H,group,scale_fmt,out_fmt,clamp", [
+    (512, 128, "fp32", "e4m3", None), (2048, 128, "ue8m0", "e4m3", 7.0), (3072, 128, "fp32", "e4m3", None),
+    (2048, 32, "ue8m0", "e2m1", 7.0), (7168, 128, "ue8m0", "e4m3", None)])
+def test_block_ring_equals_row_kernel_at_block_boundaries(H, group, scale_fmt, out_fmt, clamp, monkeypatch):
+    """The block-ring kernel runs the row kernel's arithmetic, so codes, scales
+    and clamp counters agree bit for bit; row counts around whole blocks and
+    around one block per CTA exercise ragged last blocks and grids smaller
+    than the resident maximum."""
+    ops = {}
+    for kernel in ("rows", "block"):
+        monkeypatch.setenv("TK_KERNEL", kernel)
+        ops[kernel] = tk.SwigluQuant(H, group, scale_fmt, out_fmt, True, clamp, clamp is not None)
+    info = ops["block"].launch_info(1 << 30)
+    assert info["kernel"] == "block_stream_kernel"
+    rb, grid = info["rows_per_cta"], info["grid"]
+    rng = np.random.default_rng(H + group)
+    for T in sorted({1, rb - 1, rb, rb + 1, grid * rb - 1, grid * rb, grid * rb + 1, 2 * grid * rb + 3} - {0}):
+        x = torch.from_numpy(rng.standard_normal((T, 2 * H)).astype(np.float32) * 3).to(torch.bfloat16).cuda()
+        w = torch.from_numpy(rng.uniform(0.0, 1.0, T).astype(np.float32)).cuda()
+        out = {}
+        for kernel, op in ops.items():
+            counts = torch.zeros(2, dtype=torch.int64, device="cuda") if clamp is not None else None
+            q, s = _run(op, x, w, counts)
+            out[kernel] = (q, s, counts)
+        torch.cuda.synchronize()
+        (q0, s0, c0), (q1, s1, c1) = out["rows"], out["block"]
+        assert torch.equal(q0, q1) and torch.equal(s0.view(torch.uint8), s1.view(torch.uint8)), (H, T)
+        if clamp is not None:
+            assert torch.equal(c0, c1), (H, T)
+    assert tk.tk_fault_word(torch.cuda.current_device()) == 0
