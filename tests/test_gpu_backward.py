@@ -198,3 +198,27 @@ def test_backward_host_side_errors():
     with pytest.raises(tk.TkError) as e:
         tk.SwigluBackward(96, True)
     assert e.value.status == 2
+
+
+def test_backward_guard_bands_untouched():
+    """dx, dw, the codes and the scales live inside larger buffers filled with
+    a sentinel; only their bytes may change."""
+    H, T, pad = 2048, 97, 512
+    x, w, dy = _case(T, H, seed=5, clamp=7.0)
+    op = tk.SwigluBackward(H, True, 7.0, recompute=dict(group_size=128, scale_fmt="ue8m0", out_fmt="e4m3"))
+    bufs = {
+        "dx": torch.full((T * 2 * H + 2 * pad,), 0x5A5A, dtype=torch.int16, device="cuda"),
+        "dw": torch.full((T + 2 * pad,), -3.0, dtype=torch.float32, device="cuda"),
+        "q": torch.full((T * H + 2 * pad,), 0xA5, dtype=torch.uint8, device="cuda"),
+        "s": torch.full((T * (H // 128) + 2 * pad,), 0xA5, dtype=torch.uint8, device="cuda"),
+    }
+    dx = bufs["dx"][pad:pad + T * 2 * H].view(torch.bfloat16).view(T, 2 * H)
+    dw = bufs["dw"][pad:pad + T]
+    q = bufs["q"][pad:pad + T * H].view(T, H)
+    s = bufs["s"][pad:pad + T * (H // 128)].view(T, H // 128)
+    op(x.cuda(), dy.cuda(), w.cuda(), dx=dx, dw=dw, q=q, scales=s)
+    torch.cuda.synchronize()
+    for name, b in bufs.items():
+        fill = b[0].item()
+        n = b.numel() - 2 * pad
+        assert bool((b[:pad] == fill).all()) and bool((b[pad + n:] == fill).all()), name

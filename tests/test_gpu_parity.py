@@ -182,9 +182,11 @@ def test_zero_rows_is_noop_and_tails():
         compare(q.cpu().numpy(), s.cpu().numpy(), ref, 128, "fp32", "e4m3").check("T=%d" % T)
 
 
-def test_guard_bands_untouched():
+@pytest.mark.parametrize("kernel", ["rows", "stream", "block"])
+def test_guard_bands_untouched(kernel, monkeypatch):
     """Outputs live inside larger buffers filled with a sentinel; only the
     output bytes may change."""
+    monkeypatch.setenv("TK_KERNEL", kernel)
     H, T, g = 1024, 301, 32
     for scale_fmt, out_fmt in (("fp32", "e4m3"), ("ue8m0", "e2m1")):
         op = tk.SwigluQuant(H, g, scale_fmt, out_fmt, True, 7.0, False)

@@ -284,3 +284,21 @@ def test_reduce_host_side_errors():
     with pytest.raises(tk.TkError) as e:     # a width that is not a multiple of 16
         tk.tk_moe_reduce_plan(tk.MoeReduceDesc(200, 2, 0), 0)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("name", list(wls.REDUCE_WORKLOADS))
+def test_reduce_guard_bands_untouched(name, kernel, monkeypatch):
+    """The output lives inside a larger buffer filled with a sentinel; only
+    its bytes may change."""
+    rw = wls.REDUCE_WORKLOADS[name].with_rows(97)
+    d = wls.make_reduce_inputs(rw, "cuda")
+    monkeypatch.setenv("TK_REDUCE_KERNEL", kernel)
+    op = tk.MoeReduce(rw.H, rw.topk, rw.in_dtype)
+    pad, n = 512, rw.T * rw.H
+    buf = torch.full((n + 2 * pad,), 0x5A5A, dtype=torch.int16, device="cuda")
+    out = buf[pad:pad + n].view(torch.bfloat16).view(rw.T, rw.H)
+    op(d["y"], d["pos"], d["w"], d["gs"], y_scale=d["y_scale"], out=out)
+    torch.cuda.synchronize()
+    assert bool((buf[:pad] == 0x5A5A).all()) and bool((buf[pad + n:] == 0x5A5A).all())
+    assert not bool((buf[pad:pad + n] == 0x5A5A).all())
