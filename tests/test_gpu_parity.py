@@ -523,3 +523,24 @@ def test_block_ring_equals_row_kernel_at_block_boundaries(H, group, scale_fmt, o
         if clamp is not None:
             assert torch.equal(c0, c1), (H, T)
     assert tk.tk_fault_word(torch.cuda.current_device()) == 0
+
+
+@pytest.mark.parametrize("kernel", ["rows", "block"])
+def test_every_row_count_up_to_257(kernel, monkeypatch):
+    """Every batch size from 1 to 257 rows against the oracle, clamp counters
+    included: every ragged tail of the row blocks and of the block ring's
+    slots (16 rows at this width)."""
+    monkeypatch.setenv("TK_KERNEL", kernel)
+    H, g, L = 512, 128, 7.0
+    op = tk.SwigluQuant(H, g, "ue8m0", "e4m3", True, L, True)
+    rng = np.random.default_rng(257)
+    xr = _bf16(rng.standard_normal((257, 2 * H)) * 3)
+    wr = torch.from_numpy(rng.uniform(0.0, 1.0, 257).astype(np.float32))
+    xc, wc = xr.cuda(), wr.cuda()
+    for T in range(1, 258):
+        counts = torch.zeros(2, dtype=torch.int64, device="cuda")
+        q, s = _run(op, xc[:T], wc[:T], counts)
+        ref = oracle.swiglu_quant(wls.bf16_bits(xr[:T]), wr[:T].numpy(), g, "ue8m0", "e4m3", clamp=L, want_y=True)
+        compare(q.cpu().numpy(), s.cpu().numpy(), ref, g, "ue8m0", "e4m3").check("%s T=%d" % (kernel, T))
+        assert counts.cpu().tolist() == ref["counts"].tolist(), T
+    assert tk.tk_fault_word(torch.cuda.current_device()) == 0
