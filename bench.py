@@ -185,6 +185,28 @@ def measured_peaks() -> dict:
 
 # ------------------------------------------------------------- CPU oracle
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it ("model name" on x86; the
+    implementer and part numbers on Arm), with the logical core count."""
+    import platform
+    name = ""
+    parts = set()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                key, val = key.strip().lower(), val.strip()
+                if key == "model name" and not name:
+                    name = val
+                elif key in ("cpu implementer", "cpu part"):
+                    parts.add("%s %s" % (key.replace("cpu ", ""), val))
+    except OSError:
+        pass
+    if not name:
+        name = "%s (%s)" % (platform.machine(), ", ".join(sorted(parts))) if parts else platform.machine()
+    return "%s, %d logical cores" % (name, os.cpu_count() or 1)
+
+
 def time_oracle(wl, seconds: float, seed_rows: int = 8) -> dict:
     """Time the CPU oracle on a bounded row sample of the workload: a short
     calibration, then a sample sized to about `seconds` of single-core work."""
@@ -309,7 +331,7 @@ def run_reference(args, dist):
         "vs_baseline": None, "dtype": "f64/f32", "data": "synthetic",
         "config": config_of(wl, args.gpus),
         "hbm_gbs": wl.algo_bytes(rows) * args.steps / dt / 1e9,
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "cpu": cpu_model(),
                          "sample": "%d of %d rows per step, single-threaded C oracle" % (rows, wl.T)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -453,7 +475,7 @@ def run_ours(args, dist: Dist):
     cpu = None
     if dist.rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
         r = time_oracle(wl, args.cpu_seconds)
-        cpu = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle", "cpu": cpu_model(),
                "sample": "%d of %d rows of the same workload, single-threaded C oracle, %.1f s"
                          % (r["rows"], wl.T, r["seconds"])}
         ra = time_oracle_all_cores(wl, args.cpu_seconds)
@@ -612,7 +634,7 @@ def run_reduce(args, dist, wl, dev, n_sets):
     cpu = None
     if dist.rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
         r = time_oracle(wl, args.cpu_seconds)
-        cpu = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle", "cpu": cpu_model(),
                "sample": "%d of %d tokens of the same workload, single-threaded C oracle, %.1f s"
                          % (r["rows"], wl.T, r["seconds"])}
     if dist.rank != 0:
@@ -679,7 +701,7 @@ def run_backward(args, dist, wl, dev, n_sets):
     cpu = None
     if dist.rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
         r = time_oracle(wl, args.cpu_seconds)
-        cpu = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": 1, "kind": "oracle", "cpu": cpu_model(),
                "sample": "%d of %d rows of the same workload (backward and recomputed forward), "
                          "single-threaded C oracle, %.1f s" % (r["rows"], T, r["seconds"])}
     if dist.rank != 0:
