@@ -314,8 +314,13 @@ def test_cast_workload_full_size(name):
 
 # ------------------------------------------------------ host-buffer pipe
 
+@pytest.mark.parametrize("kernel", ["auto", "block"])
 @pytest.mark.parametrize("chunk_rows", [1, 7, 1000, 4096, 100000])
-def test_host_pipe_matches_device_call(chunk_rows):
+def test_host_pipe_matches_device_call(chunk_rows, kernel, monkeypatch):
+    """The pipe's chunks run the plan's kernel for their size (the block-ring
+    kernel too when forced) and must give the device call's bytes."""
+    if kernel == "block":
+        monkeypatch.setenv("TK_KERNEL", "block")
     wl = wls.WORKLOADS["moe_T32768_H2048_g128_ue8m0_clamp7"].with_rows(3001)
     x, w = wls.make_inputs(wl, "cpu")
     op = _op(wl, count=True)
