@@ -2,8 +2,9 @@
 """Benchmark of the fused SwiGLU + MoE top-k weight + FP8 cast on GB300.
 
 One step = one launch of the fused kernel over one batch of the workload
-(default: T=8192 expanded rows, H=2048, 1x128 fp32 scales, E4M3 codes, top-k
-weights; synthetic inputs from workloads.py). Prints ONE JSON line on rank 0.
+(default: the largest configuration, T=100003 expanded rows with a ragged
+tail, H=3072, 1x128 fp32 scales, E4M3 codes, top-k weights; synthetic inputs
+from workloads.py). Prints ONE JSON line on rank 0.
 
   value     tokens/s over all ranks, device-timed with CUDA events around K
             back-to-back launches (replayed from a CUDA graph) on the
@@ -12,7 +13,11 @@ weights; synthetic inputs from workloads.py). Prints ONE JSON line on rank 0.
             every launch reads cold inputs and also evicts the previous
             launch's dirty outputs (steady state).
   roofline  algorithmic bytes per launch / average launch time vs the
-            measured HBM copy bandwidth.
+            measured HBM copy bandwidth; `steady` repeats the launches for at
+            least 0.3 s of device time, as a check on the K-step figure.
+  per_config  the other large fused workloads (the clamp / UE8M0 one, the
+            FP4 one and the 8192-row one), each timed over at least 0.3 s of
+            device time with its own clock record (default workload only).
   e2e       the same metric through the host-buffer C-ABI call with pinned
             host buffers: every step copies its inputs host->device and its
             codes and scales back, chunked so the copies overlap the kernel.
@@ -40,7 +45,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "tokens/s and achieved HBM GB/s (fraction of GB300 peak) for fused SwiGLU+FP8 cast"
-DEFAULT_WORKLOAD = "moe_T8192_H2048_g128"
+DEFAULT_WORKLOAD = "ragged_T100003_H3072_g128"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 
@@ -63,6 +68,10 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-context", action="store_true", help="skip the unfused PyTorch context timing")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-steady", action="store_true",
+                   help="skip the >= 0.3 s steady-state timing reported beside the K-step figure")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="skip the other large fused workloads reported under per_config")
     p.add_argument("--jsonl", default=None, help="also append the JSON line to this file")
     return p.parse_args(argv)
 
@@ -369,10 +378,127 @@ def emit(line: dict, args):
 
 # ------------------------------------------------------------- GPU timing
 
+# The large fused workloads reported beside the headline on the same line
+# (each timed over at least PER_CONFIG_MIN_MS of device time).
+PER_CONFIG = ["moe_T32768_H2048_g128_ue8m0_clamp7", "fp4_T65536_H2048_g32_ue8m0_clamp7", "moe_T8192_H2048_g128"]
+PER_CONFIG_MIN_MS = 300.0
+
+
+def n_sets_for(per_set: int) -> int:
+    """Input/output sets to rotate so that the sets not in use hold > 3x L2."""
+    return max(2, -(-3 * L2_BYTES // per_set) + 1)
+
+
+class FusedBench:
+    """The fused op or the standalone cast of one workload on one device:
+    the plan, `n_sets` rotating input/output sets and a launch(i) that
+    enqueues one launch on set i % n_sets through the C ABI."""
+
+    def __init__(self, wl, dev: int, scale_layout: str = "row", transposed: bool = False):
+        import torch
+        import activation_fp8_quantization_gb300 as tk
+        from activation_fp8_quantization_gb300 import _abi
+        from activation_fp8_quantization_gb300 import workloads as wls
+
+        self.wl, self.dev = wl, dev
+        T = wl.T
+        if wl.op == "cast":
+            op = tk.QuantCast(wl.H, wl.group, wl.scale_fmt, wl.out_fmt, wl.in_dtype, dev, scale_layout)
+            op.count_clamped = False
+        else:
+            op = tk.SwigluQuant(wl.H, wl.group, wl.scale_fmt, wl.out_fmt, wl.w_dist is not None, wl.clamp,
+                                wl.clamp is not None, dev, scale_layout)
+        self.op = op
+        self.transposed = transposed and wl.op == "swiglu"
+        self.algo = wl.algo_bytes()
+        self.n_sets = n_sets_for(self.algo)
+        x0, w0 = wls.make_inputs(wl, "cuda")
+        self.x0, self.w0 = x0, w0
+        q_shape, s_shape, s_dtype = op.output_shapes(T)
+        if self.transposed:
+            q_shape = (wl.H, tk.tk_swiglu_quant_transposed_size(op.plan, T)[1])
+        self.xs, self.ws, qs, ss = [], [], [], []
+        for i in range(self.n_sets):
+            self.xs.append(x0 if i == 0 else x0.clone())
+            self.ws.append(None if w0 is None else (w0 if i == 0 else w0.clone()))
+            qs.append(torch.empty(q_shape, dtype=torch.uint8, device=dev))
+            ss.append(torch.empty(s_shape, dtype=s_dtype, device=dev))
+        self.qs, self.ss = qs, ss
+        self.counts = torch.zeros(2, dtype=torch.int64, device=dev) if op.count_clamped else None
+        self.lib = _abi.lib()
+        self.stream = torch.cuda.Stream(device=dev)
+        self.sh = self.stream.cuda_stream
+        self.ptrs = [(self.xs[i].data_ptr(), None if self.ws[i] is None else self.ws[i].data_ptr(),
+                      qs[i].data_ptr(), ss[i].data_ptr()) for i in range(self.n_sets)]
+        self.cp = None if self.counts is None else self.counts.data_ptr()
+        self._tk, self._abi = tk, _abi
+
+    def launch(self, i: int):
+        wl, lib, T = self.wl, self.lib, self.wl.T
+        xp, wp, qp, spp = self.ptrs[i % self.n_sets]
+        if wl.op == "cast":
+            st = lib.tk_quant_cast_run(self.op.plan, T, xp, qp, spp, self.sh)
+        elif self.transposed:
+            st = lib.tk_swiglu_quant_run_transposed(self.op.plan, T, xp, wp, qp, spp, self.cp, self.sh)
+        else:
+            st = lib.tk_swiglu_quant_run(self.op.plan, T, xp, wp, qp, spp, self.cp, self.sh)
+        if st != 0:
+            raise self._tk.TkError(st, self._abi.tk_last_error_message())
+
+    def kernel_name(self) -> str | None:
+        if self.transposed:
+            return "transpose_quant_kernel"
+        if self.wl.op == "swiglu":
+            return self.op.launch_info(self.wl.T)["kernel"]
+        return "row_quant_kernel"
+
+    def launches_per_step(self) -> int:
+        return 1
+
+
+def time_steady(fb: FusedBench, min_ms: float, sample_clocks: bool) -> dict:
+    """Per-launch device time over back-to-back graph replays totalling at
+    least min_ms of device time (after a warm-up), with clocks sampled
+    meanwhile. For context beside the K-step headline, and for the per-config
+    rows."""
+    import torch
+    stream, n = fb.stream, fb.n_sets
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            fb.launch(i)
+    stream.synchronize()
+    chunk = n * max(1, 120 // n)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(chunk):
+            fb.launch(i)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        graph.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    per = ev0.elapsed_time(ev1) / chunk
+    reps = max(1, int(min_ms / max(per * chunk, 1e-3)) + 1)
+    clocks = ClockSampler(torch.cuda.current_device()) if sample_clocks else None
+    if clocks:
+        clocks.start()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    launches = reps * chunk
+    us = 1e3 * ms / launches
+    gbs = fb.algo / (us / 1e6) / 1e9
+    return {"us_per_launch": us, "gbs": gbs, "launches": launches, "device_ms": ms,
+            "clocks": clocks.stop() if clocks else None}
+
+
 def run_ours(args, dist: Dist):
     import torch
-    import activation_fp8_quantization_gb300 as tk
-    from activation_fp8_quantization_gb300 import _abi
     from activation_fp8_quantization_gb300 import workloads as wls
 
     if not torch.cuda.is_available():
@@ -380,97 +506,54 @@ def run_ours(args, dist: Dist):
     dev = dist.local_rank
     torch.cuda.set_device(dev)
     wl = wls.ALL_WORKLOADS[args.workload]
-    T, H = wl.T, wl.H
+    T = wl.T
     algo = wl.algo_bytes()
-    per_set = algo
-    n_sets = max(2, -(-3 * L2_BYTES // per_set) + 1)   # sets beyond the current one hold > 3x L2
     if wl.op == "reduce":
-        return run_reduce(args, dist, wl, dev, n_sets)
+        return run_reduce(args, dist, wl, dev, n_sets_for(algo))
     if wl.op == "backward":
-        return run_backward(args, dist, wl, dev, n_sets)
-    if wl.op == "cast":
-        op = tk.QuantCast(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.in_dtype, dev, args.scale_layout)
-        op.count_clamped = False
-    else:
-        op = tk.SwigluQuant(H, wl.group, wl.scale_fmt, wl.out_fmt, wl.w_dist is not None, wl.clamp,
-                            wl.clamp is not None, dev, args.scale_layout)
+        return run_backward(args, dist, wl, dev, n_sets_for(algo))
 
-    x0, w0 = wls.make_inputs(wl, "cuda")
-    q_shape, s_shape, s_dtype = op.output_shapes(T)
-    transposed = args.transposed and wl.op == "swiglu"
-    if transposed:
-        q_shape = (wl.H, tk.tk_swiglu_quant_transposed_size(op.plan, T)[1])
-    xs, ws, qs, ss = [], [], [], []
-    for i in range(n_sets):
-        xs.append(x0 if i == 0 else x0.clone())
-        ws.append(None if w0 is None else (w0 if i == 0 else w0.clone()))
-        qs.append(torch.empty(q_shape, dtype=torch.uint8, device=dev))
-        ss.append(torch.empty(s_shape, dtype=s_dtype, device=dev))
-    counts = torch.zeros(2, dtype=torch.int64, device=dev) if op.count_clamped else None
-    lib = _abi.lib()
-    stream = torch.cuda.Stream(device=dev)
-    sh = stream.cuda_stream
-    cp = None if counts is None else counts.data_ptr()
-    ptrs = [(xs[i].data_ptr(), None if ws[i] is None else ws[i].data_ptr(), qs[i].data_ptr(),
-             ss[i].data_ptr()) for i in range(n_sets)]
-
-    def launch(i):
-        xp, wp, qp, spp = ptrs[i % n_sets]
-        if wl.op == "cast":
-            st = lib.tk_quant_cast_run(op.plan, T, xp, qp, spp, sh)
-        elif transposed:
-            st = lib.tk_swiglu_quant_run_transposed(op.plan, T, xp, wp, qp, spp, cp, sh)
-        else:
-            st = lib.tk_swiglu_quant_run(op.plan, T, xp, wp, qp, spp, cp, sh)
-        if st != 0:
-            raise tk.TkError(st, _abi.tk_last_error_message())
-
-    # warm-up, then a CUDA graph holding `chunk` back-to-back launches
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            launch(i)
-    stream.synchronize()
-    chunk = min(args.steps, n_sets * max(1, 600 // n_sets))
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(chunk):
-            launch(i)
-    reps, rem = divmod(args.steps, chunk)
-    with torch.cuda.stream(stream):
-        graph.replay()      # one untimed replay: graph upload and clocks up
-    stream.synchronize()
-
-    clocks = ClockSampler(torch.cuda.current_device()) if dist.local_rank == 0 else None
-    if clocks:
-        clocks.start()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    dist.barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(reps):
-            graph.replay()
-        for i in range(rem):
-            launch(i)
-        ev1.record(stream)
-    torch.cuda.synchronize()
-    dist.barrier()
-    ms = ev0.elapsed_time(ev1)
-    clk = clocks.stop() if clocks else None
+    fb = FusedBench(wl, dev, args.scale_layout, args.transposed)
+    transposed = fb.transposed
+    n_sets = fb.n_sets
+    ms, clk = time_graph(args, dist, fb.stream, fb.launch, n_sets, dev)
     ms_max = dist.max(ms, device=dev)
     ms_per_step = ms_max / args.steps
     rows_total = dist.sum(float(T * args.steps), device=dev)
     value = rows_total / (ms_max / 1e3)
     achieved = algo / (ms_per_step / 1e3) / 1e9
     peaks = measured_peaks()
+    steady = None
+    if not args.no_steady:
+        steady = time_steady(fb, PER_CONFIG_MIN_MS, False)
+        steady["frac"] = steady["gbs"] / peaks["hbm_gbs"]
 
     e2e = None
     if not args.no_e2e and wl.op == "swiglu" and args.scale_layout == "row" and not transposed:
-        e2e = measure_e2e(op, wl, x0, w0, dev, args, dist)
+        e2e = measure_e2e(fb.op, wl, fb.x0, fb.w0, dev, args, dist)
     context = None
     if dist.rank == 0 and not transposed and not args.no_context:
-        context = torch_unfused_context(wl, xs, ws, stream)
+        context = torch_unfused_context(wl, fb.xs, fb.ws, fb.stream)
+    kernel = fb.kernel_name()
+    launches = args.steps * fb.launches_per_step()
+    del fb
+    torch.cuda.empty_cache()
+
+    per_config = None
+    if dist.rank == 0 and not args.no_per_config and args.workload == DEFAULT_WORKLOAD and not transposed:
+        per_config = {}
+        for name in PER_CONFIG:
+            pw = wls.ALL_WORKLOADS[name]
+            pfb = FusedBench(pw, dev, args.scale_layout)
+            r = time_steady(pfb, PER_CONFIG_MIN_MS, True)
+            per_config[name] = {"us_per_launch": r["us_per_launch"], "gbs": r["gbs"],
+                                "frac": r["gbs"] / peaks["hbm_gbs"], "kernel": pfb.kernel_name(),
+                                "tokens_per_s": pw.T / (r["us_per_launch"] / 1e6),
+                                "algo_bytes_per_launch": pfb.algo, "launches": r["launches"],
+                                "device_ms": r["device_ms"], "clocks": r["clocks"],
+                                "traffic": load_traffic(name, PROFILE_FAMILY[pw.op])}
+            del pfb
+            torch.cuda.empty_cache()
 
     cpu = None
     if dist.rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
@@ -485,11 +568,6 @@ def run_ours(args, dist: Dist):
     if dist.rank != 0:
         return 0
     traffic = load_traffic(wl.name, PROFILE_FAMILY["transposed" if transposed else wl.op])
-    kernel = None
-    if transposed:
-        kernel = "transpose_quant_kernel"
-    elif wl.op == "swiglu":
-        kernel = op.launch_info(T)["kernel"]
     line = {
         "metric": metric_of(wl), "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -498,15 +576,17 @@ def run_ours(args, dist: Dist):
         "config": {**config_of(wl, args.gpus), "scale_layout": args.scale_layout,
                    "codes": "transposed [H, ld]" if transposed else "row-major [T, H]",
                    "l2": "inputs larger than L2: %d rotating input/output sets, %.0f MB" % (
-                       n_sets, n_sets * per_set / 1e6)},
+                       n_sets, n_sets * algo / 1e6)},
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": kernel,
-                     "peak_source": peaks["source"], "algo_bytes_per_launch": algo},
+                     "peak_source": peaks["source"], "algo_bytes_per_launch": algo,
+                     "steady": steady},
+        "per_config": per_config,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "context_torch_unfused": context,
-        "gpu_launches": args.steps,
+        "gpu_launches": launches,
         "clocks": clk,
     }
     emit(line, args)
@@ -803,7 +883,9 @@ def measure_e2e(op, wl, x0, w0, dev, args, dist: Dist):
     from activation_fp8_quantization_gb300 import _abi
 
     T = wl.T
-    n_sets = 4
+    # sets rotated so that the host's last-level cache never holds a step's
+    # inputs (two suffice once a set is several hundred MB)
+    n_sets = 4 if wl.algo_bytes() < (512 << 20) else 2
     q_shape, s_shape, s_dtype = op.output_shapes(T)
     xs = [x0.cpu().pin_memory() for _ in range(n_sets)]
     ws = [None if w0 is None else w0.cpu().pin_memory() for _ in range(n_sets)]

@@ -70,6 +70,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.tko_quant_rows_f32.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_int64,
                                        c.c_int, c.c_int, c.c_void_p, c.c_void_p]
     lib.tko_quant_rows_f32.restype = c.c_int
+    lib.tko_quant_cols_f32.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_int, c.c_int, c.c_void_p,
+                                       c.c_void_p]
+    lib.tko_quant_cols_f32.restype = c.c_int
     lib.tko_swiglu_quant.argtypes = [c.c_void_p, c.c_int64, c.c_int64, c.c_void_p,
                                      c.c_int64, c.c_int, c.c_int, c.c_int, c.c_float,
                                      c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p]
@@ -141,6 +144,21 @@ def quant_rows_f32(y: np.ndarray, group: int, scale_fmt: str, out_fmt: str,
     scales = np.zeros(s_shape, s_dtype)
     rc = lib.tko_quant_rows_f32(_ptr(y), rows, hidden, group, SCALE_FMTS[scale_fmt],
                                 OUT_FMTS[out_fmt], _ptr(q), _ptr(scales))
+    if rc != 0:
+        raise ValueError("oracle rejected the sizes")
+    return q, scales
+
+
+def quant_cols_f32(y: np.ndarray, scale_fmt: str, out_fmt: str, lib: ctypes.CDLL | None = None):
+    """Per-channel quantization of fp32 y [rows, H]: one scale per column;
+    returns (codes [rows, H] or packed [rows, H/2], scales [H])."""
+    lib = lib or load()
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    rows, hidden = y.shape
+    q = np.zeros((rows, hidden if out_fmt == "e4m3" else hidden // 2), np.uint8)
+    scales = np.zeros(hidden, np.float32 if scale_fmt == "fp32" else np.uint8)
+    rc = lib.tko_quant_cols_f32(_ptr(y), rows, hidden, SCALE_FMTS[scale_fmt], OUT_FMTS[out_fmt],
+                                _ptr(q), _ptr(scales))
     if rc != 0:
         raise ValueError("oracle rejected the sizes")
     return q, scales

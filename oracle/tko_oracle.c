@@ -40,6 +40,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define TKO_SCALE_FP32 0
@@ -233,6 +234,58 @@ int tko_quant_rows_f32(const float *y, int64_t rows, int64_t hidden, int64_t gro
             }
         }
     }
+    return 0;
+}
+
+/* Per-channel quantization of y [rows, hidden] (the per-channel granularity
+ * of FP8 E4M3 in "TileLang + TileKernels：DeepSeek 的 GPU 内核开发新范式",
+ * zhichai.net/topic/177618740, section "3. Quantization", format table): one
+ * scale per column j, from the absolute maximum of that column over all rows;
+ * every value of the column is scaled by it and encoded exactly as a group is
+ * above. Here a column is gathered into a buffer and quantized as one group.
+ * Codes [rows, hidden] (E4M3) or [rows, hidden/2] (E2M1, column 2k in the low
+ * nibble of byte k, as for rows); scales [hidden]: float (fp32 mode) or byte
+ * (UE8M0 mode). Returns 0, or -1 on bad sizes or when out of memory. */
+int tko_quant_cols_f32(const float *y, int64_t rows, int64_t hidden, int scale_fmt, int out_fmt,
+                       uint8_t *q, void *scales)
+{
+    if (rows < 0 || hidden <= 0)
+        return -1;
+    if (out_fmt == TKO_OUT_E2M1 && (hidden % 2) != 0)
+        return -1;
+    if (rows == 0)
+        return 0;
+    float *col = malloc((size_t)rows * sizeof(float));
+    uint8_t *codes = malloc((size_t)rows);
+    if (!col || !codes) {
+        free(col);
+        free(codes);
+        return -1;
+    }
+    for (int64_t j = 0; j < hidden; ++j) {
+        for (int64_t r = 0; r < rows; ++r)
+            col[r] = y[r * hidden + j];
+        float sf = 0.0f;
+        uint8_t sb = 0;
+        quantize_group(col, rows, scale_fmt, out_fmt, codes, &sf, &sb);
+        if (scale_fmt == TKO_SCALE_FP32)
+            ((float *)scales)[j] = sf;
+        else
+            ((uint8_t *)scales)[j] = sb;
+        for (int64_t r = 0; r < rows; ++r) {
+            if (out_fmt == TKO_OUT_E4M3) {
+                q[r * hidden + j] = codes[r];
+            } else {
+                uint8_t *byte = q + r * (hidden / 2) + j / 2;
+                if (j % 2 == 0)
+                    *byte = (uint8_t)((*byte & 0xF0) | (codes[r] & 0xF));
+                else
+                    *byte = (uint8_t)((*byte & 0x0F) | ((codes[r] & 0xF) << 4));
+            }
+        }
+    }
+    free(col);
+    free(codes);
     return 0;
 }
 

@@ -155,6 +155,60 @@ def pin_ue8m0(lib):
         assert lib.tko_ue8m0_value(b) == np.float32(2.0 ** (b - 127))
 
 
+def pin_ue8m0_lower_clamp(lib):
+    # UE8M0's smallest finite scale is 2^-127 (byte 0). An amax that a
+    # smaller power of two would cover still gets byte 0; the first amax above
+    # Qmax * 2^-127 needs 2^-126 (byte 1). Subnormal amax included.
+    for qmax in (448.0, 6.0):
+        edge = np.float32(qmax * 2.0 ** -127)          # exact: 7 * 2^-121, 3 * 2^-126
+        assert float(edge) == qmax * 2.0 ** -127
+        assert lib.tko_ue8m0_byte(float(edge), qmax) == 0, qmax
+        above = np.nextafter(edge, np.float32(np.inf))
+        assert lib.tko_ue8m0_byte(float(above), qmax) == 1, qmax
+        tiny = [np.nextafter(edge, np.float32(0)), edge / np.float32(2), np.float32(qmax * 2.0 ** -130),
+                np.float32(2.0 ** -126), np.float32(2.0 ** -130), np.float32(2.0 ** -140),
+                np.float32(3 * 2.0 ** -149), np.float32(2.0 ** -149)]
+        for a in tiny:
+            assert a > 0 and lib.tko_ue8m0_byte(float(a), qmax) == 0, (qmax, float(a))
+    # through a whole row: a group whose amax is 2^-130 gets byte 0, so the
+    # codes are the E4M3 encoding (torch's cast) of y * 2^127, exact in fp32
+    y = np.array([[2.0 ** -130, -2.0 ** -131, 3 * 2.0 ** -133, 0.0]], np.float32)
+    q, s = oracle.quant_rows_f32(y, 0, "ue8m0", "e4m3", lib=lib)
+    assert int(s[0, 0]) == 0
+    want = torch.from_numpy(y * np.float32(2.0 ** 127)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(q, want), (q, want)
+
+
+def _random_positive_f32(rng, n):
+    """Positive fp32 values spread over every binade, subnormals included."""
+    bits = rng.integers(1, 0x7F7FFFFF, n, dtype=np.int64).astype(np.uint32)
+    sub = rng.integers(1, 0x007FFFFF, n // 8, dtype=np.int64).astype(np.uint32)
+    return np.concatenate([bits, sub]).view(np.float32)
+
+
+def pin_fp32_scale_ieee(lib):
+    # The fp32 scale is the IEEE single-precision quotient amax / Qmax,
+    # correctly rounded (numpy's float32 division), replaced by 1 only when
+    # it is zero. Non-power-of-two amax, normal and subnormal, and quotients
+    # that come out subnormal.
+    rng = np.random.default_rng(17)
+    a = _random_positive_f32(rng, 4000)
+    for qmax in (448.0, 6.0):
+        want = a / np.float32(qmax)
+        want = np.where(want == 0, np.float32(1.0), want)
+        got = np.array([lib.tko_fp32_scale(float(v), qmax) for v in a], np.float32)
+        bad = np.nonzero(got.view(np.uint32) != want.view(np.uint32))[0]
+        assert bad.size == 0, (qmax, a[bad[:3]], got[bad[:3]], want[bad[:3]])
+    # through whole rows: every group's scale is fl32(max|y| / Qmax) bit for bit
+    y = (rng.standard_normal((6, 256)) * np.exp2(rng.uniform(-140, 100, (6, 1)))).astype(np.float32)
+    for out_fmt, qmax in (("e4m3", 448.0), ("e2m1", 6.0)):
+        _, sc = oracle.quant_rows_f32(y, 32, "fp32", out_fmt, lib=lib)
+        amax = np.abs(y).reshape(6, 8, 32).max(axis=2)
+        want = amax / np.float32(qmax)
+        want = np.where(want == 0, np.float32(1.0), want)
+        assert np.array_equal(sc.view(np.uint32), want.view(np.uint32)), out_fmt
+
+
 # ---------------------------------------------------------------- full rows
 
 def _fmt_codes(q: np.ndarray):
@@ -338,6 +392,60 @@ def pin_quant_rows_indexing(lib):
             assert tops == [c], (out_fmt, r, j, tops)
 
 
+GOLDEN_COLS = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "hand_cols.json")
+
+
+def pin_quant_cols_hand(lib):
+    # tests/golden/hand_cols.json: a 3 x 4 input worked by hand in three modes
+    d = json.load(open(GOLDEN_COLS))
+    x = np.array(d["x"], np.float32)
+    for c in d["cases"]:
+        q, s = oracle.quant_cols_f32(x, c["scale_fmt"], c["out_fmt"], lib=lib)
+        assert [["%02X" % int(v) for v in r] for r in q] == c["q"], (c["name"], q)
+        if c["scale_fmt"] == "ue8m0":
+            assert s.tolist() == c["scales"], (c["name"], s)
+        else:
+            assert np.allclose(s, c["scales_approx"], rtol=1e-6), (c["name"], s)
+
+
+def pin_quant_cols_is_rows_of_transpose(lib):
+    # Per-channel quantization of y is per-token quantization of y's
+    # transpose (one group per row of y.T = one column of y), transposed back.
+    rng = np.random.default_rng(23)
+    rows, H = 10, 12
+    y = (rng.standard_normal((rows, H)) * np.exp2(rng.uniform(-8, 8, (1, H)))).astype(np.float32)
+    y[:, 5] = 0.0                           # an all-zero column
+    y[3, 7] = -np.abs(y[:, 7]).max() * 1.5     # a negative column peak
+    for scale_fmt in ("fp32", "ue8m0"):
+        for out_fmt in ("e4m3", "e2m1"):
+            q, s = oracle.quant_cols_f32(y, scale_fmt, out_fmt, lib=lib)
+            qt, st = oracle.quant_rows_f32(np.ascontiguousarray(y.T), 0, scale_fmt, out_fmt, lib=lib)
+            if out_fmt == "e2m1":
+                q, qt = oracle.unpack_e2m1(q), oracle.unpack_e2m1(qt)
+            assert np.array_equal(q, qt.T), (scale_fmt, out_fmt)
+            assert np.array_equal(s, st.reshape(-1)), (scale_fmt, out_fmt)
+
+
+def pin_quant_cols_planted_peaks(lib):
+    # Column j holds one peak among small values; its scale is exactly
+    # fl32(peak / Qmax) and the only saturated code of the column is the
+    # peak's row.
+    rows, H = 9, 16
+    y = np.full((rows, H), 0.01, np.float32)
+    peaks = {}
+    for j in range(H):
+        r = (5 * j + 2) % rows
+        y[r, j] = np.float32((-1.0) ** j * 1.3 * 2.0 ** (j % 7 - 3))
+        peaks[j] = r
+    for out_fmt, qmax, top in (("e4m3", 448.0, 0x7E), ("e2m1", 6.0, 0x7)):
+        q, s = oracle.quant_cols_f32(y, "fp32", out_fmt, lib=lib)
+        q = q if out_fmt == "e4m3" else oracle.unpack_e2m1(q)
+        mag = q & (0x7F if out_fmt == "e4m3" else 0x7)
+        for j, r in peaks.items():
+            assert s[j] == np.float32(abs(y[r, j])) / np.float32(qmax), (out_fmt, j)
+            assert np.nonzero(mag[:, j] == top)[0].tolist() == [r], (out_fmt, j, mag[:, j])
+
+
 def pin_scale_layouts(lib):
     # column-major = numpy's transpose into a padded [G, ld] array; packed =
     # little-endian words of four consecutive group exponents (hand example)
@@ -503,6 +611,8 @@ ALL_PINS = [
     pin_e2m1_ties,
     pin_e2m1_encode_bruteforce,
     pin_ue8m0,
+    pin_ue8m0_lower_clamp,
+    pin_fp32_scale_ieee,
     pin_hand_rows,
     pin_clamp_limit_strict,
     pin_swiglu_textbook,
@@ -511,6 +621,9 @@ ALL_PINS = [
     pin_zero_and_signed_zero,
     pin_e2m1_packing,
     pin_quant_rows_indexing,
+    pin_quant_cols_hand,
+    pin_quant_cols_is_rows_of_transpose,
+    pin_quant_cols_planted_peaks,
     pin_scale_layouts,
     pin_codes_transposed,
     pin_swiglu_backward,

@@ -7,7 +7,8 @@ Acceptance (per output tensor):
     4 fp32 ulp of a power-of-two boundary Qmax * 2^k, where the kernel's fp32
     activation (a few ulp from the oracle's) may land on the other side; those
     are counted, either exponent is accepted, and the group's oracle codes are
-    recomputed with the kernel's scale;
+    recomputed with the kernel's scale and must then equal the kernel's codes
+    exactly;
   * at least 99.9% of codes identical and every code within one step of the
     oracle's (signed ordinal distance <= 1, +0 and -0 both ordinal 0).
 Integer outputs (clamp counters) must match exactly.
@@ -44,6 +45,7 @@ class Report:
     n_groups: int = 0
     n_boundary_groups: int = 0
     n_boundary_flips: int = 0
+    n_flip_code_mismatch: int = 0
     max_scale_rel: float = 0.0
     notes: list = field(default_factory=list)
 
@@ -56,6 +58,8 @@ class Report:
         assert self.identical_frac >= 0.999, "%s: only %.5f%% codes identical (%d of %d differ)" % (
             what, 100 * self.identical_frac, self.n_code_mismatch, self.n_codes)
         assert self.max_scale_rel <= 1e-6, "%s: fp32 scale off by %.3g relative" % (what, self.max_scale_rel)
+        assert self.n_flip_code_mismatch == 0, "%s: %d codes of boundary groups differ from the oracle's " \
+            "recomputed with the kernel's scale" % (what, self.n_flip_code_mismatch)
         assert not self.notes, "%s: %s" % (what, "; ".join(self.notes[:5]))
 
 
@@ -108,6 +112,7 @@ def compare(gpu_q: np.ndarray, gpu_s: np.ndarray, ref: dict, group: int, scale_f
                 s = np.float32(2.0 ** (int(gs[r, j]) - 127))
                 yy = y[r, j * g:(j + 1) * g]
                 oq[r, j] = [enc(float(np.float32(v) / s)) for v in yy]
+                rep.n_flip_code_mismatch += int((gq[r, j] != oq[r, j]).sum())
     go, oo = ordinal(gq, out_fmt), ordinal(oq, out_fmt)
     rep.n_codes = go.size
     rep.n_code_mismatch = int((gq != oq).sum())

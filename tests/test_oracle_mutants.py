@@ -21,6 +21,9 @@ MUTANTS = {
     "up_reads_gate": ("xr[hidden + i]", "xr[i]"),
     "weight_dropped": ("silu * u * w", "silu * u"),
     "ties_to_odd": ("(c & 1) == 0", "(c & 1) == 1"),
+    "ue8m0_clamp_lo": ("if (k < -127)\n        k = -127;", "if (k < -126)\n        k = -126;"),
+    "ue8m0_clamp_dropped": ("if (k < -127)\n        k = -127;", ""),
+    "fp32_scale_by_reciprocal": ("float s = amax / qmax;", "float s = amax * (1.0f / qmax);"),
     "ue8m0_off_by_one": ("qmax * ldexp(1.0, k) < (double)amax", "qmax * ldexp(1.0, k) <= (double)amax"),
     "scale_inverted": ("float s = amax / qmax;", "float s = qmax / amax;"),
     "up_clamp_one_sided": ("} else if (u < -lim) {", "} else if (u < -2 * lim) {"),
@@ -48,6 +51,11 @@ MUTANTS = {
     "backward_up_mask_ignored": ("pass_u ? d * wr * silu : 0.0", "d * wr * silu"),
     "backward_dw_drops_up": ("acc += d * silu * u;", "acc += d * silu;"),
     "backward_weight_dropped": ("pass_g ? d * wr * u * dsilu : 0.0", "pass_g ? d * u * dsilu : 0.0"),
+    "cols_gather_transposed": ("col[r] = y[r * hidden + j];", "col[r] = y[j * rows + r];"),
+    "cols_store_transposed": ("q[r * hidden + j] = codes[r];", "q[j * rows + r] = codes[r];"),
+    "cols_nibbles_swapped": ("if (j % 2 == 0)\n                    *byte", "if (j % 2 == 1)\n                    *byte"),
+    "cols_last_row_dropped": ("quantize_group(col, rows, scale_fmt", "quantize_group(col, rows - 1, scale_fmt"),
+    "cols_scale_index": ("((float *)scales)[j] = sf;", "((float *)scales)[j / 2] = sf;"),
     "reduce_weight_dropped": ("acc += (double)w[t * K + k] * v;", "acc += v;"),
     "reduce_empty_slot_kept": ("if (r < 0)\n                    continue;", "if (r < 0)\n                    r = 0;"),
     "reduce_global_scale_dropped": ("bf16_rne_from_double((double)gs * acc)", "bf16_rne_from_double(acc)"),
