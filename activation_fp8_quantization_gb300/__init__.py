@@ -17,13 +17,14 @@ from __future__ import annotations
 import threading
 
 from . import _abi
-from ._abi import (IN_DTYPES, OUT_FMTS, REDUCE_IN_FMTS, SCALE_FMTS, SCALE_LAYOUTS, MoeReduceDesc,
+from ._abi import (GRANULARITIES, IN_DTYPES, OUT_FMTS, REDUCE_IN_FMTS, SCALE_FMTS, SCALE_LAYOUTS, MoeReduceDesc,
                    QuantCastDesc, SwigluBackwardDesc, SwigluQuantDesc, tk_swiglu_backward_plan,
                    tk_swiglu_backward_plan_destroy, tk_swiglu_backward_run, tk_swiglu_backward_validate, tk_moe_reduce_plan, tk_moe_reduce_plan_destroy,
                    tk_moe_reduce_launch_info, tk_moe_reduce_run, tk_moe_reduce_validate,
                    TkError, tk_diag_unanswered_wait, tk_fault_word, tk_last_error_message, tk_quant_cast_output_sizes,
                    tk_quant_cast_plan, tk_quant_cast_plan_destroy,
-                   tk_quant_cast_run, tk_quant_cast_validate, tk_status_string,
+                   tk_quant_cast_run, tk_quant_cast_run_ws, tk_quant_cast_validate,
+                   tk_quant_cast_workspace_size, tk_status_string,
                    tk_swiglu_quant_host_pipe_create, tk_swiglu_quant_host_pipe_destroy,
                    tk_swiglu_quant_host_workspace_size, tk_swiglu_quant_launch_info,
                    tk_swiglu_quant_output_sizes, tk_swiglu_quant_plan, tk_swiglu_quant_plan_destroy,
@@ -45,7 +46,8 @@ __all__ = [
     "tk_swiglu_quant_launch_info", "tk_swiglu_quant_run_transposed", "tk_swiglu_quant_transposed_size",
     "tk_swiglu_quant_run_mapped",
     "tk_quant_cast_validate", "tk_quant_cast_plan",
-    "tk_quant_cast_plan_destroy", "tk_quant_cast_output_sizes", "tk_quant_cast_run", "tk_status_string",
+    "tk_quant_cast_plan_destroy", "tk_quant_cast_output_sizes", "tk_quant_cast_run", "tk_quant_cast_run_ws",
+    "tk_quant_cast_workspace_size", "tk_status_string",
     "tk_last_error_message", "tk_fault_word", "tk_diag_unanswered_wait",
 ]
 
@@ -259,17 +261,20 @@ class HostPipe:
 
 
 class QuantCast:
-    """A plan for the standalone per-token / per-block cast (tk_quant_cast_plan)."""
+    """A plan for the standalone cast (tk_quant_cast_plan): per token
+    (group_size 0), per 1 x group_size block, or per channel
+    (granularity="channel": one scale per column, scales [H])."""
 
     def __init__(self, hidden: int, group_size: int = 128, scale_fmt: str = "fp32",
                  out_fmt: str = "e4m3", in_dtype: str = "bf16", device: int | None = None,
-                 scale_layout: str = "row"):
+                 scale_layout: str = "row", granularity: str = "groups"):
         torch = _torch()
         self.hidden, self.group_size = int(hidden), int(group_size)
         self.scale_fmt, self.out_fmt, self.in_dtype = scale_fmt, out_fmt, in_dtype
-        self.scale_layout = scale_layout
+        self.scale_layout, self.granularity = scale_layout, granularity
         self.desc = QuantCastDesc(self.hidden, self.group_size, SCALE_FMTS[scale_fmt],
-                                  OUT_FMTS[out_fmt], IN_DTYPES[in_dtype], SCALE_LAYOUTS[scale_layout])
+                                  OUT_FMTS[out_fmt], IN_DTYPES[in_dtype], SCALE_LAYOUTS[scale_layout],
+                                  GRANULARITIES[granularity])
         self.device = torch.cuda.current_device() if device is None else int(device)
         self.plan = tk_quant_cast_plan(self.desc, self.device)
 
@@ -283,10 +288,21 @@ class QuantCast:
             self.plan = None
 
     def output_shapes(self, T: int):
+        if self.granularity == "channel":
+            torch = _torch()
+            q_shape = (T, self.hidden if self.out_fmt == "e4m3" else self.hidden // 2)
+            return q_shape, (self.hidden,), torch.float32 if self.scale_fmt == "fp32" else torch.uint8
         return _out_shapes(T, self.hidden, self.group_size, self.scale_fmt, self.out_fmt,
                            self.scale_layout)
 
-    def __call__(self, x, *, q=None, scales=None, stream=None):
+    def workspace_bytes(self, T: int) -> int:
+        return tk_quant_cast_workspace_size(self.plan, T)
+
+    def launches_per_run(self) -> int:
+        """Kernel launches one run enqueues (the per-channel cast: three)."""
+        return 3 if self.granularity == "channel" else 1
+
+    def __call__(self, x, *, q=None, scales=None, workspace=None, stream=None):
         torch = _torch()
         T = x.shape[0]
         dt = torch.bfloat16 if self.in_dtype == "bf16" else torch.float32
@@ -298,10 +314,14 @@ class QuantCast:
         if scales is None:
             scales = torch.empty(s_shape, dtype=s_dtype, device=x.device)
         _check_cuda(scales, "scales", s_dtype, s_shape)
+        nb = self.workspace_bytes(T)
+        if nb and workspace is None:
+            workspace = torch.empty(nb, dtype=torch.uint8, device=x.device)
         if stream is None:
             stream = torch.cuda.current_stream(x.device)
         with torch.cuda.device(x.device):
-            tk_quant_cast_run(self.plan, T, x, q, scales, stream.cuda_stream)
+            tk_quant_cast_run_ws(self.plan, T, x, q, scales, workspace if nb else None,
+                                 workspace.numel() if nb else 0, stream.cuda_stream)
         return q, scales
 
 
@@ -451,11 +471,15 @@ def swiglu_quant(x, topk_weights=None, *, group_size: int = 128, scale_fmt: str 
     return op(x, topk_weights, clamped_count=clamped_count)
 
 
-def quant_cast(x, *, group_size: int = 128, scale_fmt: str = "fp32", out_fmt: str = "e4m3"):
-    """Functional form of the standalone cast (bf16 or fp32 input)."""
+def quant_cast(x, *, group_size: int = 128, scale_fmt: str = "fp32", out_fmt: str = "e4m3",
+               granularity: str = "groups"):
+    """Functional form of the standalone cast (bf16 or fp32 input); with
+    granularity="channel" one scale per column (group_size is then 0)."""
     torch = _torch()
     in_dtype = "bf16" if x.dtype == torch.bfloat16 else "fp32"
-    key = (x.shape[1], group_size, scale_fmt, out_fmt, in_dtype, x.device.index)
+    if granularity == "channel":
+        group_size = 0
+    key = (x.shape[1], group_size, scale_fmt, out_fmt, in_dtype, granularity, x.device.index)
     op = _cached("cast", key, lambda: QuantCast(x.shape[1], group_size, scale_fmt, out_fmt,
-                                                in_dtype, x.device.index))
+                                                in_dtype, x.device.index, granularity=granularity))
     return op(x)

@@ -36,7 +36,11 @@ class SwigluQuantDesc(ctypes.Structure):
 class QuantCastDesc(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int64), ("group_size", ctypes.c_int32),
                 ("scale_fmt", ctypes.c_int32), ("out_fmt", ctypes.c_int32),
-                ("in_dtype", ctypes.c_int32), ("scale_layout", ctypes.c_int32)]
+                ("in_dtype", ctypes.c_int32), ("scale_layout", ctypes.c_int32),
+                ("granularity", ctypes.c_int32)]
+
+
+GRANULARITIES = {"groups": 0, "channel": 1}
 
 
 class SwigluBackwardDesc(ctypes.Structure):
@@ -85,6 +89,8 @@ SIGNATURES = {
     "tk_quant_cast_output_sizes": (ctypes.c_int, [ctypes.POINTER(QuantCastDesc), ctypes.c_int64,
                                                   _PSZ, _PSZ]),
     "tk_quant_cast_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP]),
+    "tk_quant_cast_workspace_size": (ctypes.c_int, [_VP, ctypes.c_int64, _PSZ]),
+    "tk_quant_cast_run_ws": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
     "tk_moe_reduce_validate": (ctypes.c_int, [ctypes.POINTER(MoeReduceDesc)]),
     "tk_moe_reduce_plan": (ctypes.c_int, [ctypes.POINTER(MoeReduceDesc), ctypes.c_int, ctypes.POINTER(_VP)]),
     "tk_moe_reduce_plan_destroy": (ctypes.c_int, [_VP]),
@@ -258,6 +264,18 @@ def tk_quant_cast_output_sizes(desc: QuantCastDesc, num_tokens: int) -> tuple[in
 
 def tk_quant_cast_run(plan: int, num_tokens: int, x, q, scales, stream: int | None) -> None:
     check(lib().tk_quant_cast_run(plan, num_tokens, _ptr(x), _ptr(q), _ptr(scales), stream))
+
+
+def tk_quant_cast_workspace_size(plan: int, num_tokens: int) -> int:
+    b = ctypes.c_size_t()
+    check(lib().tk_quant_cast_workspace_size(plan, num_tokens, ctypes.byref(b)))
+    return b.value
+
+
+def tk_quant_cast_run_ws(plan: int, num_tokens: int, x, q, scales, workspace, workspace_bytes: int,
+                         stream: int | None) -> None:
+    check(lib().tk_quant_cast_run_ws(plan, num_tokens, _ptr(x), _ptr(q), _ptr(scales), _ptr(workspace),
+                                     workspace_bytes, stream))
 
 
 def tk_moe_reduce_validate(desc: MoeReduceDesc) -> int:

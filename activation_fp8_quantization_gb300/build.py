@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtk_swiglu_quant.so")
 
 SOURCES = ["tk_api.cu", "tk_swiglu_kernels.cu", "tk_cast_kernels.cu", "tk_reduce_kernels.cu",
-           "tk_transpose_kernels.cu", "tk_backward_kernels.cu", "tk_diag_kernels.cu"]
+           "tk_transpose_kernels.cu", "tk_backward_kernels.cu", "tk_diag_kernels.cu", "tk_channel_kernels.cu"]
 HEADERS = ["tk_kernels.cuh", "tk_internal.h"]
 
 # No --use_fast_math; -fmad=false keeps every multiply and add a separately

@@ -466,7 +466,12 @@ struct tk_swiglu_quant_plan_s {
 struct tk_quant_cast_plan_s {
     tk_quant_cast_desc desc;
     int device;
-    Launches Ls;
+    Launches Ls;       // per-token / per-block plans
+    // per-channel plans: the three kernels, the quantize pass's launch shape
+    // and the CTAs the amax pass aims at
+    tk::ChannelFns cfn;
+    Launch cq;
+    int amax_ctas;
 };
 
 // ------------------------------------------------------------------ fused op
@@ -1008,8 +1013,82 @@ TK_API tk_status tk_quant_cast_validate(const tk_quant_cast_desc *d)
         return st;
     if (d->in_dtype != TK_IN_BF16 && d->in_dtype != TK_IN_FP32)
         return fail(TK_ERR_INVALID_ARG, "unknown in_dtype %d", d->in_dtype);
+    if (d->granularity != TK_GRAN_GROUPS && d->granularity != TK_GRAN_PER_CHANNEL)
+        return fail(TK_ERR_INVALID_ARG, "unknown granularity %d", d->granularity);
+    if (d->granularity == TK_GRAN_PER_CHANNEL) {
+        if (d->group_size != 0)
+            return fail(TK_ERR_INVALID_ARG, "a per-channel cast takes group_size 0 (got %d)", d->group_size);
+        if (d->scale_layout != TK_SCALE_ROW_MAJOR && d->scale_layout != TK_SCALE_COL_MAJOR &&
+            d->scale_layout != TK_SCALE_COL_MAJOR_PACKED)
+            return fail(TK_ERR_INVALID_ARG, "unknown scale_layout %d", d->scale_layout);
+        if (d->scale_layout != TK_SCALE_ROW_MAJOR)
+            return fail(TK_ERR_UNSUPPORTED, "per-channel scales are one row [H]: row-major layout only");
+        return TK_OK;
+    }
     return check_scale_layout(d->scale_layout, d->scale_fmt, d->hidden, d->group_size);
 }
+
+namespace {
+
+// Plan the per-channel kernels: the quantize pass sized like the row kernel
+// (16 columns per thread, rows per CTA so that a CTA has about 256 threads),
+// the amax pass aiming at four CTAs per SM (each keeps 32 KB of loads in
+// flight), capped by its occupancy.
+tk_status plan_channel(const tk_quant_cast_desc *d, int device, tk_quant_cast_plan_s *p)
+{
+    p->cfn = tk::channel_fns(d->in_dtype, d->out_fmt, d->scale_fmt, d->hidden);
+    if (!p->cfn.amax || !p->cfn.scale || !p->cfn.quant)
+        return fail(TK_ERR_UNSUPPORTED, "no per-channel kernel for this combination");
+    tk_status st = make_launch(device, d->hidden, 16, p->cfn.quant, kRows, 0, 0, &p->cq);
+    if (st != TK_OK)
+        return st;
+    DeviceScope scope(device);
+    if (scope.err != cudaSuccess)
+        return cuda_fail(scope.err, "cudaSetDevice");
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, p->cfn.amax, tk::channel_amax_threads(), 0);
+    if (e == cudaSuccess) {
+        int occ2 = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, p->cfn.scale, tk::channel_scale_threads(), 0);
+        if (e == cudaSuccess && occ2 < 1)
+            return fail(TK_ERR_UNSUPPORTED, "the per-channel scale kernel cannot be resident");
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, "occupancy of the per-channel kernels");
+    if (occ < 1)
+        return fail(TK_ERR_UNSUPPORTED, "the per-channel amax kernel cannot be resident");
+    p->amax_ctas = (occ < 4 ? occ : 4) * p->cq.num_sms;
+    return TK_OK;
+}
+
+// Row slabs of the amax pass for T rows: about amax_ctas CTAs in all, at
+// least 32 rows per slab (four rows per warp), no empty slab.
+tk::ChannelLaunch channel_launch(const tk_quant_cast_plan_s *p, int64_t T)
+{
+    tk::ChannelLaunch L{};
+    L.chunks = (int)((p->desc.hidden + 511) / 512);
+    int64_t slabs = (p->amax_ctas + L.chunks - 1) / L.chunks;
+    const int64_t by_rows = (T + 31) / 32;
+    if (slabs > by_rows)
+        slabs = by_rows;
+    if (slabs < 1)
+        slabs = 1;
+    L.slab_rows = (T + slabs - 1) / slabs;
+    L.slabs = (int)((T + L.slab_rows - 1) / L.slab_rows);
+    L.quant_grid = grid_for(p->cq, T);
+    L.quant_block = p->cq.block;
+    return L;
+}
+
+size_t channel_workspace(const tk_quant_cast_plan_s *p, int64_t T)
+{
+    if (T <= 0)
+        return 0;
+    const tk::ChannelLaunch L = channel_launch(p, T);
+    return (size_t)L.slabs * (size_t)p->desc.hidden * sizeof(float);
+}
+
+}  // namespace
 
 TK_API tk_status tk_quant_cast_plan(const tk_quant_cast_desc *d, int device, tk_quant_cast_plan_t *plan)
 {
@@ -1019,6 +1098,20 @@ TK_API tk_status tk_quant_cast_plan(const tk_quant_cast_desc *d, int device, tk_
     tk_status st = tk_quant_cast_validate(d);
     if (st != TK_OK)
         return st;
+    if (d->granularity == TK_GRAN_PER_CHANNEL) {
+        auto *p = new (std::nothrow) tk_quant_cast_plan_s{};
+        if (!p)
+            return fail(TK_ERR_INVALID_ARG, "out of host memory");
+        p->desc = *d;
+        p->device = device;
+        st = plan_channel(d, device, p);
+        if (st != TK_OK) {
+            delete p;
+            return st;
+        }
+        *plan = p;
+        return ok();
+    }
     const Geometry geo = geometry(d->hidden, d->group_size);
     const void *row_fn = tk::cast_kernel_fn(d->in_dtype, d->out_fmt, d->scale_fmt, geo.cta_reduce);
     const void *stream_fn = tk::cast_stream_fn(d->in_dtype, d->out_fmt, d->scale_fmt);
@@ -1032,7 +1125,7 @@ TK_API tk_status tk_quant_cast_plan(const tk_quant_cast_desc *d, int device, tk_
                        bf16 ? tk::kCastBf16RowBytesPerCol : tk::kCastF32RowBytesPerCol, &Ls);
     if (st != TK_OK)
         return st;
-    auto *p = new (std::nothrow) tk_quant_cast_plan_s{*d, device, Ls};
+    auto *p = new (std::nothrow) tk_quant_cast_plan_s{*d, device, Ls, tk::ChannelFns{}, Launch{}, 0};
     if (!p)
         return fail(TK_ERR_INVALID_ARG, "out of host memory");
     *plan = p;
@@ -1049,7 +1142,10 @@ TK_API tk_status tk_quant_cast_output_sizes(const tk_quant_cast_desc *d, int64_t
         return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 and the outputs non-NULL");
     const int64_t groups = d->group_size ? d->hidden / d->group_size : 1;
     *q_bytes = (size_t)T * (size_t)(d->out_fmt == TK_OUT_E4M3 ? d->hidden : d->hidden / 2);
-    *scale_bytes_out = scale_bytes_for(d->scale_layout, d->scale_fmt, T, groups);
+    if (d->granularity == TK_GRAN_PER_CHANNEL)
+        *scale_bytes_out = (size_t)d->hidden * (d->scale_fmt == TK_SCALE_FP32 ? 4u : 1u);
+    else
+        *scale_bytes_out = scale_bytes_for(d->scale_layout, d->scale_fmt, T, groups);
     return ok();
 }
 
@@ -1059,15 +1155,11 @@ TK_API tk_status tk_quant_cast_plan_destroy(tk_quant_cast_plan_t plan)
     return ok();
 }
 
-TK_API tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t T, const void *x, void *q, void *scales,
-                                   void *stream)
+namespace {
+
+// Host checks shared by both cast calls (T > 0).
+tk_status check_cast_args(const tk_quant_cast_plan_s *plan, const void *x, const void *q, const void *scales)
 {
-    if (!plan)
-        return fail(TK_ERR_INVALID_ARG, "plan is NULL");
-    if (T < 0)
-        return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)T);
-    if (T == 0)
-        return ok();
     const tk_quant_cast_desc &d = plan->desc;
     if (!x || !q || !scales)
         return fail(TK_ERR_INVALID_ARG, "x, q and scales must be non-NULL");
@@ -1075,13 +1167,22 @@ TK_API tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t T, const v
         return fail(TK_ERR_MISALIGNED, "x must be 32-byte aligned");
     if (!aligned(q, 16))
         return fail(TK_ERR_MISALIGNED, "q must be 16-byte aligned");
-    if (d.scale_fmt == TK_SCALE_FP32 && !aligned(scales, 4))
-        return fail(TK_ERR_MISALIGNED, "fp32 scales must be 4-byte aligned");
-    if (d.scale_layout != TK_SCALE_ROW_MAJOR && !aligned(scales, 16))
-        return fail(TK_ERR_MISALIGNED, "column-major scales must be 16-byte aligned");
-    tk_status st = check_current_device(plan->device);
-    if (st != TK_OK)
-        return st;
+    if (d.granularity == TK_GRAN_PER_CHANNEL) {
+        if (!aligned(scales, 16))
+            return fail(TK_ERR_MISALIGNED, "per-channel scales must be 16-byte aligned");
+    } else {
+        if (d.scale_fmt == TK_SCALE_FP32 && !aligned(scales, 4))
+            return fail(TK_ERR_MISALIGNED, "fp32 scales must be 4-byte aligned");
+        if (d.scale_layout != TK_SCALE_ROW_MAJOR && !aligned(scales, 16))
+            return fail(TK_ERR_MISALIGNED, "column-major scales must be 16-byte aligned");
+    }
+    return check_current_device(plan->device);
+}
+
+tk_status launch_groups_cast(const tk_quant_cast_plan_s *plan, int64_t T, const void *x, void *q, void *scales,
+                             void *stream)
+{
+    const tk_quant_cast_desc &d = plan->desc;
     tk::CastArgs a{x, (int32_t)d.hidden};
     tk::OutArgs o{static_cast<uint8_t *>(q), scales};
     const Launch &L = pick(plan->Ls, T);
@@ -1090,6 +1191,65 @@ TK_API tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t T, const v
                                     static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the cast kernel");
+    return ok();
+}
+
+}  // namespace
+
+TK_API tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t T, const void *x, void *q, void *scales,
+                                   void *stream)
+{
+    if (!plan)
+        return fail(TK_ERR_INVALID_ARG, "plan is NULL");
+    if (T < 0)
+        return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)T);
+    if (plan->desc.granularity == TK_GRAN_PER_CHANNEL)
+        return fail(TK_ERR_INVALID_ARG, "a per-channel cast needs device workspace: call tk_quant_cast_run_ws");
+    if (T == 0)
+        return ok();
+    tk_status st = check_cast_args(plan, x, q, scales);
+    if (st != TK_OK)
+        return st;
+    return launch_groups_cast(plan, T, x, q, scales, stream);
+}
+
+TK_API tk_status tk_quant_cast_workspace_size(tk_quant_cast_plan_t plan, int64_t T, size_t *bytes)
+{
+    if (!plan || !bytes || T < 0)
+        return fail(TK_ERR_INVALID_ARG, "plan and bytes must be non-NULL and num_tokens >= 0");
+    *bytes = plan->desc.granularity == TK_GRAN_PER_CHANNEL ? channel_workspace(plan, T) : 0;
+    return ok();
+}
+
+TK_API tk_status tk_quant_cast_run_ws(tk_quant_cast_plan_t plan, int64_t T, const void *x, void *q, void *scales,
+                                      void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!plan)
+        return fail(TK_ERR_INVALID_ARG, "plan is NULL");
+    if (T < 0)
+        return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)T);
+    if (T == 0)
+        return ok();
+    tk_status st = check_cast_args(plan, x, q, scales);
+    if (st != TK_OK)
+        return st;
+    const tk_quant_cast_desc &d = plan->desc;
+    if (d.granularity != TK_GRAN_PER_CHANNEL)
+        return launch_groups_cast(plan, T, x, q, scales, stream);
+    const size_t need = channel_workspace(plan, T);
+    if (!workspace || workspace_bytes < need)
+        return fail(TK_ERR_INVALID_ARG, "workspace must hold %zu bytes for %lld rows (got %zu)", need,
+                    (long long)T, workspace ? workspace_bytes : (size_t)0);
+    if (!aligned(workspace, 16))
+        return fail(TK_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+    const tk::ChannelLaunch L = channel_launch(plan, T);
+    tk::CastArgs a{x, (int32_t)d.hidden};
+    tk::OutArgs o{static_cast<uint8_t *>(q), scales};
+    const tk::RowShape sh = shape_for(plan->cq, T, d.hidden, TK_SCALE_ROW_MAJOR, d.scale_fmt);
+    cudaError_t e = tk::launch_channel(plan->cfn, L, a, o, sh, static_cast<float *>(workspace),
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launch of the per-channel cast kernels");
     return ok();
 }
 

@@ -1,0 +1,377 @@
+// Per-channel cast, sm_103a: one scale per column j of x [T, H], from the
+// absolute maximum of column j over all T rows; every value of the column is
+// scaled by it and encoded ("TileLang + TileKernels：DeepSeek 的 GPU 内核开发新范式",
+// zhichai.net/topic/177618740, section "3. Quantization", format table: the
+// per-channel granularity of FP8 E4M3).
+//
+// A column's scale depends on every row, so no row can be encoded before the
+// whole input has been read once: the cast reads x twice. Three launches,
+// chained by programmatic dependent launch (each waits for the previous one
+// in griddepcontrol.wait before its first global access):
+//
+//  1. col_amax_kernel: CTA (c, s) takes the 512-column chunk c of the row
+//     slab s; its eight warps take the slab's rows in turn (warp w: rows
+//     w, w + 8, ...), a lane 16 columns of each (32-byte loads, four rows in
+//     flight), keeping the running |x| maximum in registers (bf16 pairs by
+//     packed max, exact). The warps' maxima meet in shared memory and the CTA
+//     writes one fp32 partial maximum per column: partial[s, col].
+//  2. col_scale_kernel: one CTA per 32 columns, 32 threads per column, each
+//     the maximum over a stride of the partials, then one shared-memory
+//     reduction: amax, then the scale by the same rules as the per-block
+//     cast (fp32 amax / Qmax correctly rounded, 1 for a zero column; UE8M0
+//     2^k, k the smallest with Qmax * 2^k >= amax).
+//  3. col_quant_kernel: the row kernel's mapping (16 columns per thread,
+//     H / 16 threads per row, a persistent grid over row blocks, the next
+//     block's loads in flight): each thread reads its 16 column scales once
+//     and keeps them, with their negated reciprocals, in registers; every
+//     value then costs one correctly rounded quotient (Markstein's
+//     correction, or an exact power-of-two multiply) and its share of a
+//     packed conversion.
+#include "tk_internal.h"
+
+namespace tk {
+
+namespace {
+
+constexpr int kAmaxWarps = 8;
+constexpr int kAmaxThreads = 32 * kAmaxWarps;
+constexpr int kAmaxUnroll = 4;   // rows in flight per warp
+
+// Running |x| maximum of a lane's 16 columns.
+template <bool BF16> struct AbsMax;
+
+template <> struct AbsMax<true> {
+    uint32_t m[8];   // bf16 pairs; |x| of a bf16 is its bits without the sign
+    __device__ __forceinline__ void init()
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            m[i] = 0u;
+    }
+    __device__ __forceinline__ void add(const CastBf16Src::Regs &r)
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            m[i] = bf16x2_max(m[i], r.v[i] & 0x7fff7fffu);
+    }
+    __device__ __forceinline__ void out(float (&f)[kEPT]) const
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            f[2 * i] = bf16_lo(m[i]);
+            f[2 * i + 1] = bf16_hi(m[i]);
+        }
+    }
+};
+
+template <> struct AbsMax<false> {
+    float m[kEPT];
+    __device__ __forceinline__ void init()
+    {
+#pragma unroll
+        for (int i = 0; i < kEPT; ++i)
+            m[i] = 0.0f;
+    }
+    __device__ __forceinline__ void add(const CastF32Src::Regs &r)
+    {
+#pragma unroll
+        for (int i = 0; i < kEPT; ++i)
+            m[i] = fmaxf(m[i], fabsf(__uint_as_float(r.v[i])));
+    }
+    __device__ __forceinline__ void out(float (&f)[kEPT]) const
+    {
+#pragma unroll
+        for (int i = 0; i < kEPT; ++i)
+            f[i] = m[i];
+    }
+};
+
+template <class Src, bool BF16>
+__global__ void __launch_bounds__(kAmaxThreads, 1) col_amax_kernel(CastArgs a, int64_t T, int64_t slab_rows,
+                                                               float *partial)
+{
+    __shared__ __align__(16) float red[kAmaxWarps][512];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int chunk0 = (int)blockIdx.x * 512;
+    const int col0 = chunk0 + lane * kEPT;
+    const bool col_ok = col0 < a.H;
+    const int64_t r0 = (int64_t)blockIdx.y * slab_rows;
+    const int64_t r1 = (T - r0) < slab_rows ? T : r0 + slab_rows;
+    pdl_wait();
+    pdl_launch_dependents();
+    AbsMax<BF16> acc;
+    acc.init();
+    for (int64_t r = r0 + warp; r < r1; r += kAmaxUnroll * kAmaxWarps) {
+        typename Src::Regs v[kAmaxUnroll];
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; ++u) {
+            const int64_t row = r + (int64_t)u * kAmaxWarps;
+            if (col_ok && row < r1)
+                Src::load(a, row, col0, v[u]);
+            else
+                Src::zero(v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; ++u)
+            acc.add(v[u]);
+    }
+    float f[kEPT];
+    acc.out(f);
+    float4 *dst = reinterpret_cast<float4 *>(&red[warp][lane * kEPT]);
+#pragma unroll
+    for (int k = 0; k < kEPT / 4; ++k)
+        dst[k] = make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+    __syncthreads();
+    for (int c = threadIdx.x; c < 512; c += kAmaxThreads) {
+        float m = red[0][c];
+#pragma unroll
+        for (int w = 1; w < kAmaxWarps; ++w)
+            m = fmaxf(m, red[w][c]);
+        if (chunk0 + c < a.H)
+            partial[(int64_t)blockIdx.y * a.H + chunk0 + c] = m;
+    }
+}
+
+constexpr int kScaleThreads = 1024;   // 32 columns x 32 partial strides
+
+template <int OUT, int SCALE>
+__global__ void __launch_bounds__(kScaleThreads) col_scale_kernel(const float *partial, int slabs, int H,
+                                                                   void *scales)
+{
+    __shared__ float red[32][33];
+    const int tx = threadIdx.x & 31;
+    const int ty = threadIdx.x >> 5;
+    const int c = (int)blockIdx.x * 32 + tx;
+    pdl_wait();
+    pdl_launch_dependents();
+    float m = 0.0f;
+    if (c < H)
+        for (int s = ty; s < slabs; s += 32)
+            m = fmaxf(m, partial[(int64_t)s * H + c]);
+    red[ty][tx] = m;
+    __syncthreads();
+    if (ty != 0 || c >= H)
+        return;
+#pragma unroll 8
+    for (int k = 1; k < 32; ++k)
+        m = fmaxf(m, red[k][tx]);
+    if (SCALE == kScaleUE8M0) {
+        static_cast<uint8_t *>(scales)[c] = (uint8_t)(ue8m0_exponent<OUT>(m) + 127);
+    } else {
+        // the per-block cast's rule: correctly rounded m / Qmax, 1 for zero
+        float s;
+        if (m >= 0x1p-64f) {
+            s = div_markstein1(m, Fmt<OUT>::kQmax, Fmt<OUT>::kRcpQmax);
+        } else {
+            s = __fdiv_rn(m, Fmt<OUT>::kQmax);
+            if (s == 0.0f)
+                s = 1.0f;
+        }
+        static_cast<float *>(scales)[c] = s;
+    }
+}
+
+// The 16 column scales of one thread as pair operands of the quotient:
+// s2 = (s_a, s_b) and nr2 = (-RN(1/s_a), -RN(1/s_b)) in fp32 mode, or
+// nr2 = (-2^-k_a, -2^-k_b) in UE8M0 mode. slow: some scale is below 2^-73,
+// where Markstein's remainder could underflow; such columns take the IEEE
+// division (never with ordinary data).
+template <int SCALE> struct ColScales {
+    uint64_t s2[kEPT / 2];
+    uint64_t nr2[kEPT / 2];
+    bool slow;
+
+    __device__ __forceinline__ void load(const void *scales, int col0)
+    {
+        slow = false;
+        if (SCALE == kScaleUE8M0) {
+            const uint4 b = *reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(scales) + col0);
+            const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int i = 0; i < kEPT / 2; ++i) {
+                const uint32_t byte_a = (w[i >> 1] >> (16 * (i & 1))) & 0xffu;
+                const uint32_t byte_b = (w[i >> 1] >> (16 * (i & 1) + 8)) & 0xffu;
+                // byte = k + 127, so 2^-k has the biased exponent 254 - byte
+                // (byte <= 253 for any finite amax)
+                nr2[i] = pk(-__uint_as_float((254u - byte_a) << 23), -__uint_as_float((254u - byte_b) << 23));
+                s2[i] = 0;
+            }
+        } else {
+            const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(scales) + col0);
+#pragma unroll
+            for (int k = 0; k < kEPT / 4; ++k) {
+                const float4 v = p[k];
+                s2[2 * k] = pk(v.x, v.y);
+                s2[2 * k + 1] = pk(v.z, v.w);
+                nr2[2 * k] = pk(-__frcp_rn(v.x), -__frcp_rn(v.y));
+                nr2[2 * k + 1] = pk(-__frcp_rn(v.z), -__frcp_rn(v.w));
+                slow |= fminf(fminf(v.x, v.y), fminf(v.z, v.w)) < 0x1p-73f;
+            }
+        }
+    }
+
+    // quotients y / s of the 16 values, given as -y pairs
+    __device__ __forceinline__ void divide(const uint64_t (&ny)[kEPT / 2], uint64_t (&v)[kEPT / 2]) const
+    {
+        if (SCALE == kScaleUE8M0) {
+#pragma unroll
+            for (int i = 0; i < kEPT / 2; ++i)
+                v[i] = mul2(ny[i], nr2[i]);
+        } else if (!slow) {
+#pragma unroll
+            for (int i = 0; i < kEPT / 2; ++i)
+                v[i] = div_markstein2(ny[i], s2[i], nr2[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < kEPT / 2; ++i)
+                v[i] = pk(__fdiv_rn(-plo(ny[i]), plo(s2[i])), __fdiv_rn(-phi(ny[i]), phi(s2[i])));
+        }
+    }
+};
+
+// MAXT: the CTA size the instantiation allows. Rows up to 8192 columns take
+// 512-thread CTAs, which lets each thread hold the 32 scale registers and two
+// row blocks of loads without spilling; wider rows take 1024-thread CTAs
+// (64 registers per thread).
+template <class Src, int OUT, int SCALE, int MAXT>
+__global__ void __launch_bounds__(MAXT) col_quant_kernel(CastArgs a, OutArgs o, RowShape sh)
+{
+    Src src;
+    const int tid = threadIdx.x;
+    const int slot = tid / sh.tpr;
+    const int lr = tid - slot * sh.tpr;
+    const bool slot_ok = slot < sh.rpc;
+    const int col0 = lr * kEPT;
+    const int64_t nrb = (sh.T + sh.rpc - 1) / sh.rpc;
+    pdl_wait();
+    pdl_launch_dependents();
+    ColScales<SCALE> cs;
+    cs.load(o.scales, slot_ok ? col0 : 0);
+    typename Src::Regs ra, rb_regs;
+    const int64_t step = gridDim.x;
+    auto row_of = [&](int64_t b) { return b * sh.rpc + slot; };
+    auto valid = [&](int64_t b) { return slot_ok && b < nrb && row_of(b) < sh.T; };
+    auto fetch = [&](int64_t b, typename Src::Regs &r) {
+        if (valid(b))
+            Src::load(a, row_of(b), col0, r);
+        else
+            Src::zero(r);
+    };
+    auto compute = [&](int64_t b, const typename Src::Regs &r) {
+        if (!valid(b))
+            return;
+        const int64_t row = row_of(b);
+        uint64_t ny[kEPT / 2];
+        float amax_unused = 0.0f;
+        src.produce(a, r, true, ny, amax_unused);
+        uint64_t v[kEPT / 2];
+        cs.divide(ny, v);
+        if (OUT == kOutE4M3) {
+            uint32_t w[4];
+            e4m3_words(v, w);
+            st_stream_128(o.q + row * (int64_t)sh.H + col0, w[0], w[1], w[2], w[3]);
+        } else {
+            const uint32_t w0 = cvt_e2m1x8(v[0], v[1], v[2], v[3]);
+            const uint32_t w1 = cvt_e2m1x8(v[4], v[5], v[6], v[7]);
+            st_stream_64(o.q + row * (int64_t)(sh.H / 2) + col0 / 2, w0, w1);
+        }
+    };
+    int64_t b = blockIdx.x;
+    fetch(b, ra);
+    while (b < nrb) {
+        fetch(b + step, rb_regs);
+        compute(b, ra);
+        b += step;
+        if (b >= nrb)
+            break;
+        fetch(b + step, ra);
+        compute(b, rb_regs);
+        b += step;
+    }
+}
+
+template <class Src, int OUT, int MAXT>
+const void *quant_pick(int scale_fmt)
+{
+    return scale_fmt == kScaleF32 ? reinterpret_cast<const void *>(&col_quant_kernel<Src, OUT, kScaleF32, MAXT>)
+                                  : reinterpret_cast<const void *>(&col_quant_kernel<Src, OUT, kScaleUE8M0, MAXT>);
+}
+
+template <class Src>
+const void *quant_pick_out(int out_fmt, int scale_fmt, bool wide)
+{
+    if (out_fmt == kOutE4M3)
+        return wide ? quant_pick<Src, kOutE4M3, kMaxThreads>(scale_fmt) : quant_pick<Src, kOutE4M3, 512>(scale_fmt);
+    return wide ? quant_pick<Src, kOutE2M1, kMaxThreads>(scale_fmt) : quant_pick<Src, kOutE2M1, 512>(scale_fmt);
+}
+
+template <int OUT>
+const void *scale_pick(int scale_fmt)
+{
+    return scale_fmt == kScaleF32 ? reinterpret_cast<const void *>(&col_scale_kernel<OUT, kScaleF32>)
+                                  : reinterpret_cast<const void *>(&col_scale_kernel<OUT, kScaleUE8M0>);
+}
+
+cudaError_t launch_grid(const void *fn, dim3 grid, int block, void **args, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace
+
+ChannelFns channel_fns(int in_dtype, int out_fmt, int scale_fmt, int64_t hidden)
+{
+    ChannelFns f{};
+    if (in_dtype != 0 && in_dtype != 1)
+        return f;
+    if (out_fmt != kOutE4M3 && out_fmt != kOutE2M1)
+        return f;
+    if (scale_fmt != kScaleF32 && scale_fmt != kScaleUE8M0)
+        return f;
+    f.amax = in_dtype == 0 ? reinterpret_cast<const void *>(&col_amax_kernel<CastBf16Src, true>)
+                           : reinterpret_cast<const void *>(&col_amax_kernel<CastF32Src, false>);
+    f.scale = out_fmt == kOutE4M3 ? scale_pick<kOutE4M3>(scale_fmt) : scale_pick<kOutE2M1>(scale_fmt);
+    const bool wide = hidden > 8192;   // more than 512 threads per row
+    f.quant = in_dtype == 0 ? quant_pick_out<CastBf16Src>(out_fmt, scale_fmt, wide)
+                            : quant_pick_out<CastF32Src>(out_fmt, scale_fmt, wide);
+    return f;
+}
+
+int channel_amax_threads() { return kAmaxThreads; }
+int channel_scale_threads() { return kScaleThreads; }
+
+cudaError_t launch_channel(const ChannelFns &f, const ChannelLaunch &L, const CastArgs &a, const OutArgs &o,
+                           const RowShape &sh, float *partial, cudaStream_t stream)
+{
+    CastArgs a_ = a;
+    int64_t T = sh.T, slab_rows = L.slab_rows;
+    float *part = partial;
+    void *args1[] = {&a_, &T, &slab_rows, &part};
+    cudaError_t e = launch_grid(f.amax, dim3(L.chunks, L.slabs), kAmaxThreads, args1, stream);
+    if (e != cudaSuccess)
+        return e;
+    const float *cpart = partial;
+    int slabs = L.slabs, H = a.H;
+    void *sc = o.scales;
+    void *args2[] = {&cpart, &slabs, &H, &sc};
+    e = launch_grid(f.scale, dim3((H + 31) / 32), kScaleThreads, args2, stream);
+    if (e != cudaSuccess)
+        return e;
+    OutArgs o_ = o;
+    RowShape sh_ = sh;
+    void *args3[] = {&a_, &o_, &sh_};
+    return launch_grid(f.quant, dim3(L.quant_grid), L.quant_block, args3, stream);
+}
+
+}  // namespace tk

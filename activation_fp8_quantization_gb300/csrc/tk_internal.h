@@ -24,6 +24,31 @@ const void *cast_block_fn(int in_dtype, int out_fmt, int scale_fmt);
 cudaError_t launch_cast(const void *fn, int grid, int block, size_t smem, const CastArgs &a,
                         const OutArgs &o, const RowShape &sh, cudaStream_t stream);
 
+// Per-channel cast (tk_channel_kernels.cu): the column-amax pass, the scale
+// kernel and the quantize pass for an input / code / scale format.
+struct ChannelFns {
+    const void *amax;
+    const void *scale;
+    const void *quant;
+};
+// One run's launch shape: the amax pass runs (chunks x slabs) CTAs, each over
+// slab_rows rows of a 512-column chunk; the quantize pass is a persistent
+// grid of quant_grid CTAs of quant_block threads (the row kernel's mapping,
+// sh.rpc rows per CTA per iteration).
+struct ChannelLaunch {
+    int chunks;
+    int slabs;
+    int64_t slab_rows;
+    int quant_grid;
+    int quant_block;
+};
+ChannelFns channel_fns(int in_dtype, int out_fmt, int scale_fmt, int64_t hidden);
+int channel_amax_threads();
+int channel_scale_threads();
+// partial: device fp32 [slabs, H], the caller's workspace.
+cudaError_t launch_channel(const ChannelFns &f, const ChannelLaunch &L, const CastArgs &a, const OutArgs &o,
+                           const RowShape &sh, float *partial, cudaStream_t stream);
+
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the previous kernel of the stream drains; it waits for that kernel
 // itself (griddepcontrol.wait) before touching global memory.

@@ -23,7 +23,7 @@ class Workload:
     group: int                  # 0 = one scale per row, else columns per scale
     scale_fmt: str              # "fp32" | "ue8m0"
     out_fmt: str                # "e4m3" | "e2m1"
-    x_dist: str                 # "normal" | "row_lognormal" | "outliers"
+    x_dist: str                 # "normal" | "row_lognormal" | "col_lognormal" | "outliers"
     x_sigma: float = 1.0
     w_dist: str | None = None   # None | "topk8_norm" | "uniform"
     clamp: float | None = None
@@ -32,10 +32,15 @@ class Workload:
     in_dtype: str = "bf16"      # cast input: "bf16" | "fp32"; reduce rows: "bf16" | "e4m3"
     topk: int = 8               # reduce: slots per token (T tokens, T * topk expert rows)
     empty_frac: float = 0.0     # reduce: share of empty slots
+    gran: str = "groups"        # cast: "groups" (per token / per block) | "channel" (one scale per column)
 
     @property
     def groups_per_row(self) -> int:
         return 1 if self.group == 0 else self.H // self.group
+
+    @property
+    def channel(self) -> bool:
+        return self.gran == "channel"
 
     @property
     def x_cols(self) -> int:
@@ -57,6 +62,10 @@ class Workload:
             return T * (4 * self.H + 2 * self.H + 4 * self.H + 4 + (4 if self.w_dist else 0)) + q + s
         x = T * self.x_cols * (4 if self.in_dtype == "fp32" else 2)
         q = T * self.H if self.out_fmt == "e4m3" else T * self.H // 2
+        if self.channel:
+            # a column's scale needs every row, so x is read twice (one pass
+            # for the column maxima, one to encode); one scale per column
+            return 2 * x + q + self.H * (4 if self.scale_fmt == "fp32" else 1)
         s = T * self.groups_per_row * (4 if self.scale_fmt == "fp32" else 1)
         w = 4 * T if self.w_dist else 0
         return x + q + s + w
@@ -97,6 +106,19 @@ CAST_WORKLOADS = {
                                                   "ue8m0", "e4m3", "normal", seed=2002, op="cast"),
     "cast_T8192_H4096_token_fp32": Workload("cast_T8192_H4096_token_fp32", 8192, 4096, 0, "fp32", "e4m3",
                                             "row_lognormal", seed=2003, op="cast", in_dtype="fp32"),
+    # per channel: one scale per column; "col_lognormal" gives every column
+    # its own LogNormal(0, 1) magnitude (outlier channels)
+    "cast_T8192_H4096_channel_bf16": Workload("cast_T8192_H4096_channel_bf16", 8192, 4096, 0, "fp32", "e4m3",
+                                              "col_lognormal", seed=2004, op="cast", gran="channel"),
+    "cast_T16384_H7168_channel_ue8m0_bf16": Workload("cast_T16384_H7168_channel_ue8m0_bf16", 16384, 7168, 0,
+                                                     "ue8m0", "e4m3", "col_lognormal", seed=2005, op="cast",
+                                                     gran="channel"),
+    "cast_T32768_H4096_channel_ue8m0_e2m1_bf16": Workload("cast_T32768_H4096_channel_ue8m0_e2m1_bf16", 32768,
+                                                          4096, 0, "ue8m0", "e2m1", "col_lognormal", seed=2006,
+                                                          op="cast", gran="channel"),
+    "cast_T8192_H4096_channel_fp32": Workload("cast_T8192_H4096_channel_fp32", 8192, 4096, 0, "fp32", "e4m3",
+                                              "col_lognormal", seed=2007, op="cast", in_dtype="fp32",
+                                              gran="channel"),
 }
 # The weighted top-k combine after the expert GEMMs: T tokens, each gathering
 # `topk` expert rows (a random permutation of the T * topk rows, as after a
@@ -134,6 +156,9 @@ def make_inputs(wl: Workload, device: str | torch.device = "cpu"):
     T, C = wl.T, wl.x_cols
     xdt = torch.float32 if wl.in_dtype == "fp32" else torch.bfloat16
     x = torch.empty((T, C), dtype=xdt, device=device)
+    col = None
+    if wl.x_dist == "col_lognormal":
+        col = torch.randn((1, C), generator=gen, device=device).exp_()
     for r0 in range(0, T, _CHUNK_ROWS):
         r1 = min(T, r0 + _CHUNK_ROWS)
         n = r1 - r0
@@ -142,6 +167,8 @@ def make_inputs(wl: Workload, device: str | torch.device = "cpu"):
             v.mul_(wl.x_sigma)
         if wl.x_dist == "row_lognormal":
             v.mul_(torch.randn((n, 1), generator=gen, device=device).exp_())
+        elif wl.x_dist == "col_lognormal":
+            v.mul_(col)
         elif wl.x_dist == "outliers":
             hit = torch.rand((n, C), generator=gen, device=device) < 1e-3
             v = torch.where(hit, v * 50.0, v)

@@ -303,6 +303,8 @@ def oracle_step(wl, x, w, lib):
         return lambda: oracle.moe_reduce(yc, pos, wt, d["gs"], y_scale=ys, lib=lib)
     if wl.op == "cast":
         y = x.float().numpy()
+        if wl.channel:
+            return lambda: oracle.quant_cols_f32(y, wl.scale_fmt, wl.out_fmt, lib=lib)
         return lambda: oracle.quant_rows_f32(y, wl.group, wl.scale_fmt, wl.out_fmt, lib=lib)
     xb = wls.bf16_bits(x)
     wn = None if w is None else w.numpy()
@@ -355,6 +357,9 @@ def config_of(wl, n: int) -> dict:
          "parallelism": "replicas x%d" % n}
     if wl.op != "swiglu":
         c.update({"op": wl.op, "in_dtype": wl.in_dtype})
+    if wl.op == "cast":
+        c["granularity"] = "per channel (scales [H]; x read twice)" if wl.channel else (
+            "per token" if wl.group == 0 else "per 1x%d block" % wl.group)
     return c
 
 
@@ -403,7 +408,8 @@ class FusedBench:
         self.wl, self.dev = wl, dev
         T = wl.T
         if wl.op == "cast":
-            op = tk.QuantCast(wl.H, wl.group, wl.scale_fmt, wl.out_fmt, wl.in_dtype, dev, scale_layout)
+            op = tk.QuantCast(wl.H, wl.group, wl.scale_fmt, wl.out_fmt, wl.in_dtype, dev, scale_layout,
+                              granularity=wl.gran)
             op.count_clamped = False
         else:
             op = tk.SwigluQuant(wl.H, wl.group, wl.scale_fmt, wl.out_fmt, wl.w_dist is not None, wl.clamp,
@@ -425,6 +431,10 @@ class FusedBench:
             ss.append(torch.empty(s_shape, dtype=s_dtype, device=dev))
         self.qs, self.ss = qs, ss
         self.counts = torch.zeros(2, dtype=torch.int64, device=dev) if op.count_clamped else None
+        self.workspace, self.ws_bytes = None, 0
+        if wl.op == "cast" and op.workspace_bytes(T):
+            self.ws_bytes = op.workspace_bytes(T)
+            self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.lib = _abi.lib()
         self.stream = torch.cuda.Stream(device=dev)
         self.sh = self.stream.cuda_stream
@@ -437,7 +447,9 @@ class FusedBench:
         wl, lib, T = self.wl, self.lib, self.wl.T
         xp, wp, qp, spp = self.ptrs[i % self.n_sets]
         if wl.op == "cast":
-            st = lib.tk_quant_cast_run(self.op.plan, T, xp, qp, spp, self.sh)
+            st = lib.tk_quant_cast_run_ws(self.op.plan, T, xp, qp, spp,
+                                          None if self.workspace is None else self.workspace.data_ptr(),
+                                          self.ws_bytes, self.sh)
         elif self.transposed:
             st = lib.tk_swiglu_quant_run_transposed(self.op.plan, T, xp, wp, qp, spp, self.cp, self.sh)
         else:
@@ -450,10 +462,12 @@ class FusedBench:
             return "transpose_quant_kernel"
         if self.wl.op == "swiglu":
             return self.op.launch_info(self.wl.T)["kernel"]
+        if self.wl.channel:
+            return "col_amax_kernel + col_scale_kernel + col_quant_kernel"
         return "row_quant_kernel"
 
     def launches_per_step(self) -> int:
-        return 1
+        return self.op.launches_per_run() if self.wl.op == "cast" else 1
 
 
 def time_steady(fb: FusedBench, min_ms: float, sample_clocks: bool) -> dict:

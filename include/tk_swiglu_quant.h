@@ -4,7 +4,7 @@
  *   tk_swiglu_quant_*     the fused op (device buffers; host buffers staged
  *                         through device memory, or read and written in place
  *                         by the kernel; codes row-major or transposed)
- *   tk_quant_cast_*       the standalone per-token / per-block cast
+ *   tk_quant_cast_*       the standalone per-token / per-block / per-channel cast
  *   tk_moe_reduce_*       the weighted top-k combine after the expert GEMMs
  *   tk_swiglu_backward_*  the SwiGLU backward, optionally recomputing the codes
  *   tk_fault_word, tk_diag_unanswered_wait, tk_status_string,
@@ -297,17 +297,26 @@ tk_status tk_swiglu_quant_run_mapped(tk_swiglu_quant_plan_t plan, int64_t num_to
                                      int64_t *clamped_count_host, void *stream);
 
 /* ------------------------------------------------------------------------
- * Standalone per-token / per-block cast: x [T, H] (bf16 or fp32) -> codes + scales,
- * with the same grouping, scale and code rules as the fused call.
+ * Standalone cast: x [T, H] (bf16 or fp32) -> codes + scales, per token, per
+ * 1 x group_size block, or per channel ("TileLang + TileKernels：DeepSeek 的
+ * GPU 内核开发新范式", zhichai.net/topic/177618740, section "3. Quantization",
+ * format table: per-token, per-block and per-channel FP8 E4M3, FP4 E2M1,
+ * UE8M0 scales), with the same scale and code rules as the fused call.
  * ---------------------------------------------------------------------- */
+
+typedef enum tk_granularity {
+    TK_GRAN_GROUPS = 0,       /* one scale per row (group_size 0) or per 1 x group_size block of a row */
+    TK_GRAN_PER_CHANNEL = 1   /* one scale per column j: amax over all T rows of column j; scales [H] */
+} tk_granularity;
 
 typedef struct tk_quant_cast_desc {
     int64_t hidden;      /* H: 16 <= H <= 16384, H % 16 == 0 */
-    int32_t group_size;  /* as in tk_swiglu_quant_desc */
+    int32_t group_size;  /* as in tk_swiglu_quant_desc; must be 0 with TK_GRAN_PER_CHANNEL */
     int32_t scale_fmt;   /* tk_scale_fmt */
     int32_t out_fmt;     /* tk_out_fmt */
     int32_t in_dtype;    /* tk_in_dtype */
-    int32_t scale_layout;  /* tk_scale_layout */
+    int32_t scale_layout;  /* tk_scale_layout; TK_SCALE_ROW_MAJOR with TK_GRAN_PER_CHANNEL */
+    int32_t granularity;   /* tk_granularity */
 } tk_quant_cast_desc;
 
 typedef struct tk_quant_cast_plan_s *tk_quant_cast_plan_t;
@@ -316,14 +325,41 @@ tk_status tk_quant_cast_validate(const tk_quant_cast_desc *desc);
 tk_status tk_quant_cast_plan(const tk_quant_cast_desc *desc, int device, tk_quant_cast_plan_t *plan);
 tk_status tk_quant_cast_plan_destroy(tk_quant_cast_plan_t plan);
 
-/* Bytes of the cast's outputs, as tk_swiglu_quant_output_sizes (host only). */
+/* Bytes of the cast's outputs (host only): as tk_swiglu_quant_output_sizes
+ * for per-token and per-block plans; per channel, q as there and scales
+ * H * 4 (fp32) or H (UE8M0) bytes. */
 tk_status tk_quant_cast_output_sizes(const tk_quant_cast_desc *desc, int64_t num_tokens,
                                      size_t *q_bytes, size_t *scale_bytes);
 
-/* Enqueue the cast. x [T, H] row-major, 32-byte aligned; q, scales as in
- * tk_swiglu_quant_run. num_tokens == 0 is a no-op. */
+/* Enqueue a per-token or per-block cast. x [T, H] row-major, 32-byte
+ * aligned; q, scales as in tk_swiglu_quant_run. num_tokens == 0 is a no-op.
+ * A per-channel plan needs device workspace: it returns TK_ERR_INVALID_ARG
+ * here; use tk_quant_cast_run_ws. */
 tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t num_tokens, const void *x,
                             void *q, void *scales, void *stream);
+
+/* Bytes of device workspace tk_quant_cast_run_ws needs for num_tokens rows
+ * (host only): 0 for per-token and per-block plans; for a per-channel plan
+ * one fp32 partial column maximum per row slab of the first pass and column,
+ * at most ceil(4 * SMs / ceil(H / 512)) * H * 4 bytes (4 MiB at H = 7168 on
+ * 152 SMs, independent of T beyond a few thousand rows). */
+tk_status tk_quant_cast_workspace_size(tk_quant_cast_plan_t plan, int64_t num_tokens, size_t *bytes);
+
+/* Enqueue the cast with a caller-owned workspace (any granularity).
+ *   x, q                as in tk_quant_cast_run
+ *   scales              per token / per block: as tk_quant_cast_run; per
+ *                       channel: [H] fp32 or UE8M0 bytes, 16-byte aligned
+ *   workspace           device memory of at least tk_quant_cast_workspace_size
+ *                       bytes for this num_tokens, 16-byte aligned, not used by
+ *                       anything else until `stream` passes this call (NULL
+ *                       when the size is 0). It need not be initialised and
+ *                       is left holding intermediate values.
+ * A per-channel column scale depends on every row, so the cast reads x
+ * twice: one launch takes column maxima over row slabs into the workspace,
+ * one reduces them to the scales, one encodes every row (three kernels,
+ * stream-ordered). num_tokens == 0 is a no-op (no scale is written). */
+tk_status tk_quant_cast_run_ws(tk_quant_cast_plan_t plan, int64_t num_tokens, const void *x, void *q,
+                               void *scales, void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
  * Weighted top-k combine after the expert GEMMs

@@ -84,6 +84,16 @@ def test_cast_validate():
     assert tk.tk_quant_cast_validate(C(100, 0, 0, 0, 0, 0)) == 2
     assert tk.tk_quant_cast_validate(C(4096, 128, 1, 0, 0, 2)) == 0
     assert tk.tk_quant_cast_validate(C(4096, 128, 0, 0, 0, 2)) == 2
+    # per channel: group_size 0, scales one row [H] (row-major), any formats
+    for sf in (0, 1):
+        for of in (0, 1):
+            for dt in (0, 1):
+                assert tk.tk_quant_cast_validate(C(4096, 0, sf, of, dt, 0, 1)) == 0
+    assert tk.tk_quant_cast_validate(C(4096, 128, 0, 0, 0, 0, 1)) == 1   # group_size must be 0
+    assert tk.tk_quant_cast_validate(C(4096, 0, 0, 0, 0, 1, 1)) == 2     # no column-major [H]
+    assert tk.tk_quant_cast_validate(C(4096, 0, 0, 0, 0, 7, 1)) == 1     # unknown layout
+    assert tk.tk_quant_cast_validate(C(4096, 0, 0, 0, 0, 0, 2)) == 1     # unknown granularity
+    assert tk.tk_quant_cast_validate(C(4112, 0, 0, 0, 0, 0, 1)) == 0     # any multiple of 16
 
 
 def test_output_sizes_of_scale_layouts():
@@ -97,6 +107,9 @@ def test_output_sizes_of_scale_layouts():
     C = tk.QuantCastDesc
     assert tk.tk_quant_cast_output_sizes(C(4096, 32, 1, 1, 0, 2), 7) == (7 * 2048, 32 * 8 * 4)
     assert tk.tk_quant_cast_output_sizes(C(4096, 0, 0, 0, 1, 0), 7) == (7 * 4096, 7 * 4)
+    # per channel: one scale per column, whatever the number of rows
+    assert tk.tk_quant_cast_output_sizes(C(4096, 0, 0, 0, 0, 0, 1), 7) == (7 * 4096, 4096 * 4)
+    assert tk.tk_quant_cast_output_sizes(C(4096, 0, 1, 1, 0, 0, 1), 100003) == (100003 * 2048, 4096)
 
 
 def test_output_sizes():
