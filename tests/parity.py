@@ -118,3 +118,25 @@ def compare(gpu_q: np.ndarray, gpu_s: np.ndarray, ref: dict, group: int, scale_f
     rep.n_code_mismatch = int((gq != oq).sum())
     rep.max_step = int(np.abs(go - oo).max()) if go.size else 0
     return rep
+
+
+def compare_chunked(gpu_q: np.ndarray, gpu_s: np.ndarray, ref: dict, group: int, scale_fmt: str,
+                    out_fmt: str, chunk_rows: int = 8192, lib=None) -> Report:
+    """compare() over consecutive row chunks (bounded memory for outputs of
+    hundreds of millions of codes), merged into one Report; row-major scales."""
+    total = Report()
+    rows = ref["y"].shape[0]
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        part = {"y": ref["y"][r0:r1], "q": ref["q"][r0:r1], "scales": ref["scales"][r0:r1]}
+        rep = compare(gpu_q[r0:r1], gpu_s[r0:r1], part, group, scale_fmt, out_fmt, lib=lib)
+        total.n_codes += rep.n_codes
+        total.n_code_mismatch += rep.n_code_mismatch
+        total.max_step = max(total.max_step, rep.max_step)
+        total.n_groups += rep.n_groups
+        total.n_boundary_groups += rep.n_boundary_groups
+        total.n_boundary_flips += rep.n_boundary_flips
+        total.n_flip_code_mismatch += rep.n_flip_code_mismatch
+        total.max_scale_rel = max(total.max_scale_rel, rep.max_scale_rel)
+        total.notes += ["rows %d..%d: %s" % (r0, r1, n) for n in rep.notes]
+    return total

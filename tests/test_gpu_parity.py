@@ -108,6 +108,40 @@ def test_workload_full_size(name):
     print(name, "full: %d sampled rows, identical %.6f" % (len(idx), rep.identical_frac))
 
 
+LARGE = ["moe_T32768_H2048_g128_ue8m0_clamp7", "ragged_T100003_H3072_g128", "fp4_T65536_H2048_g32_ue8m0_clamp7"]
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_workload_full_output(name):
+    """The three largest workloads at full size in the benchmark's launch
+    configuration, every row compared with the oracle (run over all host
+    cores): at least 99.9% of the codes identical, none more than one step
+    away, UE8M0 scales exact up to counted boundary groups (whose codes must
+    then follow the kernel's scale exactly), fp32 scales within 1e-6, and the
+    clamp counters exact."""
+    from oracle import parallel
+    from parity import compare_chunked
+    wl = wls.WORKLOADS[name]
+    op = _op(wl, count=True)
+    x_cpu, w_cpu = wls.make_inputs(wl, "cpu")
+    counts = torch.zeros(2, dtype=torch.int64, device="cuda")
+    q, s = _run(op, x_cpu.cuda(), None if w_cpu is None else w_cpu.cuda(),
+                counts if op.count_clamped else None)
+    kernel = op.launch_info(wl.T)["kernel"]
+    gq, gs = q.cpu().numpy(), s.cpu().numpy()
+    del q, s
+    ref = parallel.swiglu_quant(wls.bf16_bits(x_cpu), None if w_cpu is None else w_cpu.numpy(), wl.group,
+                                wl.scale_fmt, wl.out_fmt, clamp=wl.clamp, want_y=True)
+    rep = compare_chunked(gq, gs, ref, wl.group, wl.scale_fmt, wl.out_fmt)
+    print(name, kernel, "every row: %d codes, identical %.7f, max step %d, %d groups, boundary groups %d, "
+          "flips %d, max fp32 scale rel %.3g" % (rep.n_codes, rep.identical_frac, rep.max_step, rep.n_groups,
+                                                rep.n_boundary_groups, rep.n_boundary_flips, rep.max_scale_rel))
+    rep.check(name + " every row")
+    assert rep.n_codes == wl.T * wl.H
+    if op.count_clamped:
+        assert counts.cpu().tolist() == ref["counts"].tolist()
+
+
 # ------------------------------------------------------------- edge cases
 
 GEOMS = [  # (H, group) incl. the CTA-reduction path (one scale per row, wide or odd rows)

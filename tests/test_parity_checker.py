@@ -53,3 +53,19 @@ def test_flip_away_from_a_boundary_fails():
     gs[0, 1] += 1                     # group 1 is nowhere near a boundary
     rep = compare(q.copy(), gs, {"y": y, "q": q, "scales": s}, 32, "ue8m0", "e4m3")
     assert rep.notes
+
+
+def test_chunked_comparison_merges_like_one_comparison():
+    from parity import compare_chunked
+    rng = np.random.default_rng(8)
+    y = (rng.standard_normal((300, 256)) * np.exp(rng.standard_normal((300, 1)))).astype(np.float32)
+    q, s = oracle.quant_rows_f32(y, 128, "fp32", "e4m3")
+    ref = {"y": y, "q": q, "scales": s}
+    gq = q.copy()
+    gq[5, 7] ^= 1                      # one code a step away
+    gq[250, 3] ^= 1
+    one = compare(gq, s, ref, 128, "fp32", "e4m3")
+    many = compare_chunked(gq, s, ref, 128, "fp32", "e4m3", chunk_rows=64)
+    for k in ("n_codes", "n_code_mismatch", "max_step", "n_groups", "max_scale_rel"):
+        assert getattr(one, k) == getattr(many, k), k
+    assert many.n_code_mismatch == 2
