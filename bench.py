@@ -565,7 +565,8 @@ def run_ours(args, dist: Dist):
                                 "tokens_per_s": pw.T / (r["us_per_launch"] / 1e6),
                                 "algo_bytes_per_launch": pfb.algo, "launches": r["launches"],
                                 "device_ms": r["device_ms"], "clocks": r["clocks"],
-                                "traffic": load_traffic(name, PROFILE_FAMILY[pw.op])}
+                                "traffic": load_traffic(name, family_of(pw)),
+                                "l2_write_bytes": load_profile_field(name, family_of(pw), "l2_write_bytes_per_launch")}
             del pfb
             torch.cuda.empty_cache()
 
@@ -581,7 +582,8 @@ def run_ours(args, dist: Dist):
                                       % (ra["rows"] // ra["cores"], ra["seconds"])}
     if dist.rank != 0:
         return 0
-    traffic = load_traffic(wl.name, PROFILE_FAMILY["transposed" if transposed else wl.op])
+    fam = family_of(wl, transposed)
+    traffic = load_traffic(wl.name, fam)
     line = {
         "metric": metric_of(wl), "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -595,6 +597,7 @@ def run_ours(args, dist: Dist):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": kernel,
                      "peak_source": peaks["source"], "algo_bytes_per_launch": algo,
+                     "l2_write_bytes": load_profile_field(wl.name, fam, "l2_write_bytes_per_launch"),
                      "steady": steady},
         "per_config": per_config,
         "cpu_baseline": cpu,
@@ -844,23 +847,45 @@ def _code_only(text: str) -> str:
     return " ".join("".join(out).split())
 
 
-def kernel_source_hash() -> str:
-    """sha256 over the device code (the kernel files and the headers they
-    include, comments and layout left out; not the host-side API in
-    tk_api.cu), to tell whether a committed ncu summary still describes the
-    kernel that runs."""
+# The device-code files each profile family's kernels are built from.
+FAMILY_SOURCES = {
+    "swiglu_quant": ["tk_kernels.cuh", "tk_internal.h", "tk_swiglu_kernels.cu"],
+    "quant_cast": ["tk_kernels.cuh", "tk_internal.h", "tk_cast_kernels.cu"],
+    "channel_cast": ["tk_kernels.cuh", "tk_internal.h", "tk_channel_kernels.cu"],
+    "transposed_quant": ["tk_kernels.cuh", "tk_internal.h", "tk_transpose_kernels.cu"],
+    "moe_reduce": ["tk_kernels.cuh", "tk_internal.h", "tk_reduce_kernels.cu"],
+    "swiglu_backward": ["tk_kernels.cuh", "tk_internal.h", "tk_backward_kernels.cu"],
+}
+
+
+def kernel_source_hash(family: str | None = None) -> str:
+    """sha256 over the device code a profile family's kernels are built from
+    (every kernel file and header but the host-side tk_api.cu when family is
+    None), comments and layout left out, to tell whether a committed ncu
+    summary still describes the kernel that runs."""
     import hashlib
     csrc = os.path.join(ROOT, "activation_fp8_quantization_gb300", "csrc")
+    if family is None:
+        names = [n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")) and n != "tk_api.cu"]
+    else:
+        names = FAMILY_SOURCES[family]
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")) and name != "tk_api.cu":
-            with open(os.path.join(csrc, name), encoding="utf-8") as f:
-                h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
+    for name in sorted(names):
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()
 
 
-PROFILE_FAMILY = {"swiglu": "swiglu_quant", "cast": "quant_cast", "reduce": "moe_reduce",
+PROFILE_FAMILY = {"swiglu": "swiglu_quant", "cast": "quant_cast", "channel": "channel_cast", "reduce": "moe_reduce",
                   "backward": "swiglu_backward", "transposed": "transposed_quant"}
+
+
+def family_of(wl, transposed: bool = False) -> str:
+    if transposed:
+        return PROFILE_FAMILY["transposed"]
+    if wl.op == "cast" and wl.channel:
+        return PROFILE_FAMILY["channel"]
+    return PROFILE_FAMILY[wl.op]
 
 
 def load_traffic(workload: str, family: str):
@@ -877,10 +902,30 @@ def load_traffic(workload: str, family: str):
                     fields[k.strip("`")] = v.strip().strip("`")
     except OSError:
         return None
-    if fields.get("source_sha256") != kernel_source_hash():
+    if fields.get("source_sha256") != kernel_source_hash(family):
         return None
     try:
         return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def load_profile_field(workload: str, family: str, key: str):
+    """Another integer field of the same summary (None if absent or stale)."""
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (family, workload))
+    fields = {}
+    try:
+        with open(path) as f:
+            for line in f:
+                if line.startswith("- ") and ": " in line:
+                    k, v = line[2:].strip().split(": ", 1)
+                    fields[k.strip("`")] = v.strip().strip("`")
+    except OSError:
+        return None
+    if fields.get("source_sha256") != kernel_source_hash(family):
+        return None
+    try:
+        return int(fields[key])
     except (KeyError, ValueError):
         return None
 

@@ -97,10 +97,10 @@ def compare(gpu_q: np.ndarray, gpu_s: np.ndarray, ref: dict, group: int, scale_f
     else:
         gs, os_ = gpu_s.astype(np.int32), ref["scales"].astype(np.int32)
         diff = gs != os_
+        amax = np.abs(y.reshape(rows, G, g)).max(axis=2)
+        nb = _near_boundary(amax, QMAX[out_fmt])
+        rep.n_boundary_groups = int(nb.sum())
         if diff.any():
-            amax = np.abs(y.reshape(rows, G, g)).max(axis=2)
-            nb = _near_boundary(amax, QMAX[out_fmt])
-            rep.n_boundary_groups = int(nb.sum())
             bad = diff & ~(nb & (np.abs(gs - os_) == 1))
             if bad.any():
                 r, j = np.argwhere(bad)[0]

@@ -23,3 +23,16 @@ def test_hash_is_stable_under_comment_edits(tmp_path, monkeypatch):
     assert bench.kernel_source_hash() == h0
     (csrc / "k.cu").write_text("__global__ void k() { int a = 2; }\n")
     assert bench.kernel_source_hash() != h0
+
+
+def test_family_hash_covers_only_its_sources(tmp_path, monkeypatch):
+    csrc = tmp_path / "activation_fp8_quantization_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in ("tk_kernels.cuh", "tk_internal.h", "tk_swiglu_kernels.cu", "tk_channel_kernels.cu"):
+        (csrc / name).write_text("int %s = 0;\n" % name.split(".")[0])
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.kernel_source_hash("swiglu_quant")
+    (csrc / "tk_channel_kernels.cu").write_text("int changed = 1;\n")   # another family's file
+    assert bench.kernel_source_hash("swiglu_quant") == h
+    (csrc / "tk_kernels.cuh").write_text("int changed = 2;\n")          # a shared header
+    assert bench.kernel_source_hash("swiglu_quant") != h
