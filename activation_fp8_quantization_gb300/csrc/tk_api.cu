@@ -963,7 +963,11 @@ static __device__ __align__(256) unsigned char g_tk_static_scratch[TK_STATIC_SCR
 namespace {
 constexpr int kMaxDevices = 256;
 std::mutex g_static_mu;
-void *g_static_addr[kMaxDevices] = {};   // device address of the array, looked up once per device
+// Device address of the array, looked up once per device ordinal. The
+// address belongs to the context current at the lookup, the device's primary
+// context for a runtime-API caller; the cache assumes that context for the
+// life of the process.
+void *g_static_addr[kMaxDevices] = {};
 }  // namespace
 
 TK_API tk_status tk_swiglu_quant_run_host_static(tk_swiglu_quant_host_pipe_t pipe, int64_t T, const void *x_host,
@@ -972,6 +976,11 @@ TK_API tk_status tk_swiglu_quant_run_host_static(tk_swiglu_quant_host_pipe_t pip
 {
     if (!pipe)
         return fail(TK_ERR_INVALID_ARG, "pipe is NULL");
+    // the same statuses as tk_swiglu_quant_run_host for the row count
+    if (T < 0)
+        return fail(TK_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)T);
+    if (T == 0)
+        return ok();
     if (pipe->total_bytes > TK_STATIC_SCRATCH_BYTES)
         return fail(TK_ERR_UNSUPPORTED,
                     "the pipe needs %zu bytes of workspace but the built-in array holds %zu: "

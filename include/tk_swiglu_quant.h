@@ -271,7 +271,10 @@ tk_status tk_swiglu_quant_run_host(tk_swiglu_quant_host_pipe_t pipe, int64_t num
  *     fit for hidden 2048; about 300 for hidden 7168).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current, once; make that first
- *     call before any stream capture.
+ *     call before any stream capture. The address is kept per device ordinal
+ *     for the rest of the process, so the call assumes the device's primary
+ *     context (the runtime API's) throughout: not a driver-API context of the
+ *     caller's own, and not across cudaDeviceReset.
  *   - Every call on a device shares the one array, and it keeps the last
  *     call's contents; nothing in it needs clearing, since each call writes
  *     every byte before reading it. Calls whose work overlaps on the GPU race

@@ -62,3 +62,22 @@ def test_static_workspace_refuses_a_pipe_that_does_not_fit():
         tk.tk_swiglu_quant_run_host_static(pipe.pipe, 16, x, w, q, s, None, None)
     assert e.value.status == 2
     assert "chunk_rows" in str(e.value)
+
+
+def test_static_workspace_row_count_statuses_match_the_workspace_call():
+    """T < 0 and T == 0 answer as tk_swiglu_quant_run_host does, before the
+    size check: INVALID_ARG, and OK with nothing enqueued, even on a pipe too
+    large for the built-in array."""
+    op = tk.SwigluQuant(2048, 128, "fp32", "e4m3", True)
+    big = tk.HostPipe(op, 8192)
+    assert big.ws_bytes > _abi.STATIC_SCRATCH_BYTES
+    x = torch.zeros(16, 4096, dtype=torch.bfloat16).pin_memory()
+    w = torch.ones(16).pin_memory()
+    q = torch.full((16, 2048), 0x33, dtype=torch.uint8).pin_memory()
+    s = torch.full((16, 16), 5.0).pin_memory()
+    with pytest.raises(tk.TkError) as e:
+        tk.tk_swiglu_quant_run_host_static(big.pipe, -1, x, w, q, s, None, None)
+    assert e.value.status == 1
+    tk.tk_swiglu_quant_run_host_static(big.pipe, 0, x, w, q, s, None, None)
+    torch.cuda.synchronize()
+    assert bool((q == 0x33).all()) and bool((s == 5.0).all())
