@@ -35,7 +35,9 @@ namespace {
 
 constexpr int kAmaxWarps = 8;
 constexpr int kAmaxThreads = 32 * kAmaxWarps;
-constexpr int kAmaxUnroll = 4;   // rows in flight per warp
+// rows per load set (two sets in flight per warp): 32 bytes of a bf16 row,
+// 64 of an fp32 row per lane
+template <bool BF16> constexpr int kAmaxUnroll = BF16 ? 4 : 2;
 
 // Running |x| maximum of a lane's 16 columns.
 template <bool BF16> struct AbsMax;
@@ -87,7 +89,7 @@ template <> struct AbsMax<false> {
 };
 
 template <class Src, bool BF16>
-__global__ void __launch_bounds__(kAmaxThreads, 1) col_amax_kernel(CastArgs a, int64_t T, int64_t slab_rows,
+__global__ void __launch_bounds__(kAmaxThreads, 2) col_amax_kernel(CastArgs a, int64_t T, int64_t slab_rows,
                                                                float *partial)
 {
     __shared__ __align__(16) float red[kAmaxWarps][512];
@@ -102,19 +104,37 @@ __global__ void __launch_bounds__(kAmaxThreads, 1) col_amax_kernel(CastArgs a, i
     pdl_launch_dependents();
     AbsMax<BF16> acc;
     acc.init();
-    for (int64_t r = r0 + warp; r < r1; r += kAmaxUnroll * kAmaxWarps) {
-        typename Src::Regs v[kAmaxUnroll];
+    // Two sets of U rows in turn: the next set's loads are issued before the
+    // current set is reduced, so 2U rows stay in flight per warp.
+    constexpr int U = kAmaxUnroll<BF16>;
+    constexpr int64_t kStep = U * kAmaxWarps;
+    typename Src::Regs va[U], vb[U];
+    auto fetch = [&](int64_t r, typename Src::Regs (&v)[U]) {
 #pragma unroll
-        for (int u = 0; u < kAmaxUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t row = r + (int64_t)u * kAmaxWarps;
             if (col_ok && row < r1)
                 Src::load(a, row, col0, v[u]);
             else
                 Src::zero(v[u]);
         }
+    };
+    auto reduce = [&](const typename Src::Regs (&v)[U]) {
 #pragma unroll
-        for (int u = 0; u < kAmaxUnroll; ++u)
+        for (int u = 0; u < U; ++u)
             acc.add(v[u]);
+    };
+    int64_t r = r0 + warp;
+    fetch(r, va);
+    while (r < r1) {
+        fetch(r + kStep, vb);
+        reduce(va);
+        r += kStep;
+        if (r >= r1)
+            break;
+        fetch(r + kStep, va);
+        reduce(vb);
+        r += kStep;
     }
     float f[kEPT];
     acc.out(f);
@@ -145,10 +165,22 @@ __global__ void __launch_bounds__(kScaleThreads) col_scale_kernel(const float *p
     const int c = (int)blockIdx.x * 32 + tx;
     pdl_wait();
     pdl_launch_dependents();
+    // independent loads, four at a time, so their latencies overlap
     float m = 0.0f;
-    if (c < H)
-        for (int s = ty; s < slabs; s += 32)
+    if (c < H) {
+        float m1 = 0.0f, m2 = 0.0f, m3 = 0.0f;
+        int s = ty;
+        for (; s + 96 < slabs; s += 128) {
+            const float *p = partial + (int64_t)s * H + c;
+            m = fmaxf(m, p[0]);
+            m1 = fmaxf(m1, p[32 * (int64_t)H]);
+            m2 = fmaxf(m2, p[64 * (int64_t)H]);
+            m3 = fmaxf(m3, p[96 * (int64_t)H]);
+        }
+        for (; s < slabs; s += 32)
             m = fmaxf(m, partial[(int64_t)s * H + c]);
+        m = fmaxf(fmaxf(m, m1), fmaxf(m2, m3));
+    }
     red[ty][tx] = m;
     __syncthreads();
     if (ty != 0 || c >= H)
@@ -174,17 +206,21 @@ __global__ void __launch_bounds__(kScaleThreads) col_scale_kernel(const float *p
 
 // The 16 column scales of one thread as pair operands of the quotient:
 // s2 = (s_a, s_b) and nr2 = (-RN(1/s_a), -RN(1/s_b)) in fp32 mode, or
-// nr2 = (-2^-k_a, -2^-k_b) in UE8M0 mode. slow: some scale is below 2^-73,
-// where Markstein's remainder could underflow; such columns take the IEEE
-// division (never with ordinary data).
+// nr2 = (-2^-k_a, -2^-k_b) in UE8M0 mode. Markstein's step needs s >= 2^-73
+// (else its remainder can underflow); a column with a smaller scale (its
+// maximum is below about 2^-64, never ordinary data) keeps s * 2^100 and
+// -RN(1/(s * 2^100)) instead, and its values are multiplied by 2^100 before
+// the division. Both scalings are exact (y stays below 448 * 2^27), so the
+// quotient is the same real number and its correct rounding the same fp32.
+// Bit i of `tiny` marks such a column.
 template <int SCALE> struct ColScales {
     uint64_t s2[kEPT / 2];
     uint64_t nr2[kEPT / 2];
-    bool slow;
+    uint32_t tiny;
 
     __device__ __forceinline__ void load(const void *scales, int col0)
     {
-        slow = false;
+        tiny = 0u;
         if (SCALE == kScaleUE8M0) {
             const uint4 b = *reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(scales) + col0);
             const uint32_t w[4] = {b.x, b.y, b.z, b.w};
@@ -199,14 +235,26 @@ template <int SCALE> struct ColScales {
             }
         } else {
             const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(scales) + col0);
+            float sc[kEPT];
 #pragma unroll
             for (int k = 0; k < kEPT / 4; ++k) {
                 const float4 v = p[k];
-                s2[2 * k] = pk(v.x, v.y);
-                s2[2 * k + 1] = pk(v.z, v.w);
-                nr2[2 * k] = pk(-__frcp_rn(v.x), -__frcp_rn(v.y));
-                nr2[2 * k + 1] = pk(-__frcp_rn(v.z), -__frcp_rn(v.w));
-                slow |= fminf(fminf(v.x, v.y), fminf(v.z, v.w)) < 0x1p-73f;
+                sc[4 * k] = v.x;
+                sc[4 * k + 1] = v.y;
+                sc[4 * k + 2] = v.z;
+                sc[4 * k + 3] = v.w;
+            }
+#pragma unroll
+            for (int j = 0; j < kEPT; ++j) {
+                if (sc[j] < 0x1p-73f) {
+                    sc[j] = __fmul_rn(sc[j], 0x1p100f);
+                    tiny |= 1u << j;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kEPT / 2; ++i) {
+                s2[i] = pk(sc[2 * i], sc[2 * i + 1]);
+                nr2[i] = pk(-__frcp_rn(sc[2 * i]), -__frcp_rn(sc[2 * i + 1]));
             }
         }
     }
@@ -218,22 +266,21 @@ template <int SCALE> struct ColScales {
 #pragma unroll
             for (int i = 0; i < kEPT / 2; ++i)
                 v[i] = mul2(ny[i], nr2[i]);
-        } else if (!slow) {
+        } else if (tiny == 0u) {
 #pragma unroll
             for (int i = 0; i < kEPT / 2; ++i)
                 v[i] = div_markstein2(ny[i], s2[i], nr2[i]);
         } else {
 #pragma unroll
-            for (int i = 0; i < kEPT / 2; ++i)
-                v[i] = pk(__fdiv_rn(-plo(ny[i]), plo(s2[i])), __fdiv_rn(-phi(ny[i]), phi(s2[i])));
+            for (int i = 0; i < kEPT / 2; ++i) {
+                const uint64_t k2 = pk((tiny >> (2 * i)) & 1u ? 0x1p100f : 1.0f,
+                                       (tiny >> (2 * i + 1)) & 1u ? 0x1p100f : 1.0f);
+                v[i] = div_markstein2(mul2(ny[i], k2), s2[i], nr2[i]);
+            }
         }
     }
 };
 
-// MAXT: the CTA size the instantiation allows. Rows up to 8192 columns take
-// 512-thread CTAs, which lets each thread hold the 32 scale registers and two
-// row blocks of loads without spilling; wider rows take 1024-thread CTAs
-// (64 registers per thread).
 template <class Src, int OUT, int SCALE, int MAXT>
 __global__ void __launch_bounds__(MAXT) col_quant_kernel(CastArgs a, OutArgs o, RowShape sh)
 {
