@@ -177,7 +177,7 @@ class SwigluQuant:
     def transposed(self, x, topk_weights=None, *, qt=None, scales=None, clamped_count=None,
                    stream=None):
         """The same op with the codes stored transposed (tk_swiglu_quant_run_transposed):
-        returns (qt [H, ld] uint8 with ld = T rounded up to 16, scales)."""
+        returns (qt [H, ld] uint8 with ld = T rounded up to 32, scales)."""
         torch = _torch()
         T = x.shape[0]
         _check_cuda(x, "x", torch.bfloat16, (T, 2 * self.hidden))

@@ -683,7 +683,7 @@ TK_API tk_status tk_swiglu_quant_transposed_size(tk_swiglu_quant_plan_t plan, in
     if (!plan->tfn)
         return fail(TK_ERR_UNSUPPORTED, "transposed codes need E4M3, group_size 32, 64 or 128 and "
                                         "hidden % 128 == 0");
-    *ld = (T + 15) / 16 * 16;
+    *ld = (T + 31) / 32 * 32;
     *qt_bytes = (size_t)plan->desc.hidden * (size_t)*ld;
     return ok();
 }
@@ -714,7 +714,7 @@ TK_API tk_status tk_swiglu_quant_run_transposed(tk_swiglu_quant_plan_t plan, int
         ++lg;
     sh.tpg_log2 = lg;
     sh.groups = (int32_t)(d.hidden / d.group_size);
-    const int64_t ldq = (T + 15) / 16 * 16;
+    const int64_t ldq = (T + 31) / 32 * 32;
     const int64_t tiles = (T + 31) / 32 * (d.hidden / 128);
     const int grid = (int)(tiles < plan->tgrid ? tiles : plan->tgrid);
     cudaError_t e = tk::launch_transpose(plan->tfn, grid, a, o, sh, ldq, static_cast<cudaStream_t>(stream));

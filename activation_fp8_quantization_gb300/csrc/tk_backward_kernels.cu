@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a,
     const int nwr = sh.tpr > 32 ? sh.tpr / 32 : 1;  // warps per row
     const float L = a.limit;
     constexpr float kNegHalfLog2e = -0.72134752044448170368f;  // -log2(e) / 2
+    const bool wide = aligned32(a.dx);   // uniform: a row's halves stay 32-byte aligned (H % 16 == 0)
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t rb = blockIdx.x; rb < nrb; rb += gridDim.x) {
@@ -127,10 +128,16 @@ __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a,
         }
         if (ok) {
             uint16_t *dxr = a.dx + row * (2 * (int64_t)a.H) + col0;
-            st_stream_128(dxr, og[0], og[1], og[2], og[3]);
-            st_stream_128(dxr + 8, og[4], og[5], og[6], og[7]);
-            st_stream_128(dxr + a.H, ou[0], ou[1], ou[2], ou[3]);
-            st_stream_128(dxr + a.H + 8, ou[4], ou[5], ou[6], ou[7]);
+            if (wide) {   // dx 32-byte aligned: every thread's 32 bytes are
+                          // one sector
+                st_stream_256(dxr, og);
+                st_stream_256(dxr + a.H, ou);
+            } else {
+                st_stream_128(dxr, og[0], og[1], og[2], og[3]);
+                st_stream_128(dxr + 8, og[4], og[5], og[6], og[7]);
+                st_stream_128(dxr + a.H, ou[0], ou[1], ou[2], ou[3]);
+                st_stream_128(dxr + a.H + 8, ou[4], ou[5], ou[6], ou[7]);
+            }
         }
         if (a.dw) {
             float part = plo(acc) + phi(acc);

@@ -100,6 +100,17 @@ __device__ __forceinline__ void st_stream_128(void *p, uint32_t a, uint32_t b, u
                  :: "l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// 32 bytes in one store (32-byte aligned): a lane writes a whole sector, so
+// L2 sees one full-sector write instead of two half-sector ones
+__device__ __forceinline__ void st_stream_256(void *p, const uint32_t (&w)[8])
+{
+    asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
 __device__ __forceinline__ void st_stream_64(void *p, uint32_t a, uint32_t b)
 {
     asm volatile("st.global.L1::no_allocate.v2.b32 [%0], {%1,%2};"

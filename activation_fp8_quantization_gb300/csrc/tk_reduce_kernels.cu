@@ -155,8 +155,12 @@ __global__ void __launch_bounds__(512) moe_reduce_kernel(ReduceArgs a)
             o[i] = to_bf16x2(plo(v), phi(v));
         }
         uint16_t *dst = static_cast<uint16_t *>(a.out) + t * (int64_t)a.H + col0;
-        st_stream_128(dst, o[0], o[1], o[2], o[3]);
-        st_stream_128(dst + 8, o[4], o[5], o[6], o[7]);
+        if (aligned32(a.out)) {   // uniform: rows of H % 16 == 0 bf16 keep 32-byte alignment
+            st_stream_256(dst, o);
+        } else {
+            st_stream_128(dst, o[0], o[1], o[2], o[3]);
+            st_stream_128(dst + 8, o[4], o[5], o[6], o[7]);
+        }
     }
 }
 
@@ -357,9 +361,16 @@ __global__ void __launch_bounds__(kReduceBulkThreads, 1) moe_reduce_bulk_kernel(
                 o[q] = to_bf16x2(plo(vg), phi(vg));
             }
             uint16_t *dst = orow + g * kG;
-            st_stream_128(dst, o[0], o[1], o[2], o[3]);
-            if constexpr (kG == 16)
-                st_stream_128(dst + 8, o[4], o[5], o[6], o[7]);
+            if constexpr (kG == 16) {
+                if (aligned32(a.out)) {
+                    st_stream_256(dst, o);
+                } else {
+                    st_stream_128(dst, o[0], o[1], o[2], o[3]);
+                    st_stream_128(dst + 8, o[4], o[5], o[6], o[7]);
+                }
+            } else {
+                st_stream_128(dst, o[0], o[1], o[2], o[3]);
+            }
         }
         __syncwarp();
         if (lane == 0)

@@ -16,9 +16,13 @@
 // eight threads per row, 16 columns each, run the fused op and the quantizer
 // of the row-major kernels (same arithmetic, same order) for two passes of 16
 // rows and store the 16 codes row-major into a shared tile. Phase 2: each
-// thread gathers the tile's 32 rows of one column and writes them as two
-// 16-byte stores, so every warp writes full 32-byte sectors of 32 rows of qT. Rows T <= t < ldq of the last tile
-// are written as zero codes; nothing at or past ldq is written.
+// thread gathers the tile's 32 rows of one column and writes them as one
+// 32-byte store (ldq is a multiple of 32, so the sector is aligned), or as two
+// 16-byte stores where qT itself is only 16-byte aligned; either way every
+// warp writes full 32-byte sectors of 32 rows of qT, but L2 receives one
+// full-sector write per thread instead of two half-sector ones. Rows
+// T <= t < ldq of the last tile are written as zero codes; nothing at or past
+// ldq is written.
 #include "tk_internal.h"
 
 namespace tk {
@@ -45,6 +49,9 @@ __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(Swig
     const int64_t ntiles = (sh.T + kTileRows - 1) / kTileRows * ncb;
     const int oc = tid & (kTileCols - 1);   // phase 2: column within the tile
     const int oh = tid >> 7;                // phase 2: rows oh*32 .. oh*32+31 (oh = 0 with 128 threads)
+    // uniform: every qT row starts 32-byte aligned, so each thread's 32 rows
+    // of one column go out as one sector-sized store
+    const bool wide = (ldq & 31) == 0 && aligned32(o.q);
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t tl = blockIdx.x; tl < ntiles; tl += gridDim.x) {
@@ -90,10 +97,14 @@ __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(Swig
         }
         const int64_t r0 = t0 + oh * 32;
         uint8_t *dst = o.q + (int64_t)(c0 + oc) * ldq + r0;
-        if (r0 < ldq)
-            st_stream_128(dst, out[0], out[1], out[2], out[3]);
-        if (r0 + 16 < ldq)
-            st_stream_128(dst + 16, out[4], out[5], out[6], out[7]);
+        if (wide && r0 + 32 <= ldq) {
+            st_stream_256(dst, out);
+        } else {
+            if (r0 < ldq)
+                st_stream_128(dst, out[0], out[1], out[2], out[3]);
+            if (r0 + 16 < ldq)
+                st_stream_128(dst + 16, out[4], out[5], out[6], out[7]);
+        }
         __syncthreads();
     }
     src.finish(a);

@@ -158,13 +158,16 @@ tk_status tk_swiglu_quant_run(tk_swiglu_quant_plan_t plan, int64_t num_tokens,
  *
  *     qt[i * ld + t] = code of row t, column i      (0 <= i < H, 0 <= t < T)
  *
- * with ld = T rounded up to a multiple of 16, so every row of qt starts
- * 16-byte aligned; qt[i * ld + t] for T <= t < ld is written as 0. This is
- * the operand layout of a following GEMM that contracts over the rows.
+ * with ld = T rounded up to a multiple of 32, so every row of qt starts
+ * 32-byte aligned (each thread of the kernel then writes one whole 32-byte
+ * sector of 32 rows with a single store); qt[i * ld + t] for T <= t < ld is
+ * written as 0. This is the operand layout of a following GEMM that
+ * contracts over the rows.
  * Requires a plan with E4M3 codes, group_size 32, 64 or 128 and H % 128 == 0
  * (TK_ERR_UNSUPPORTED otherwise). Arguments, alignment and errors are those
- * of tk_swiglu_quant_run, with qt (H * ld bytes, 16-byte aligned) in place
- * of q; the clamp counters are added to as there.
+ * of tk_swiglu_quant_run, with qt (H * ld bytes, 16-byte aligned; 32-byte
+ * aligned for the single-store form) in place of q; the clamp counters are
+ * added to as there.
  * ---------------------------------------------------------------------- */
 
 /* ld and the bytes of qt for num_tokens rows (host only). */

@@ -47,7 +47,7 @@ def test_transposed_matches_row_major_and_oracle(H, T, group, scale_fmt):
     op = tk.SwigluQuant(H, group, scale_fmt, "e4m3", True)
     (q, s, _), (qt, st, _) = _both(op, x.cuda(), w.cuda())
     _, ld = tk.tk_swiglu_quant_transposed_size(op.plan, T)
-    assert ld == (T + 15) // 16 * 16 and qt.shape == (H, ld)
+    assert ld == (T + 31) // 32 * 32 and qt.shape == (H, ld)
     qt_h = qt.cpu().numpy()
     assert np.array_equal(qt_h[:, :T].T, q.cpu().numpy())
     assert not qt_h[:, T:].any()
