@@ -118,3 +118,31 @@ def test_transposed_codes_past_4_gib():
     assert not qt[cols][:, wl.T:].any()
     del x, w, qt, st
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("scale_fmt,out_fmt", [("fp32", "e4m3"), ("ue8m0", "e2m1")])
+def test_channel_cast_past_4_gib(scale_fmt, out_fmt):
+    """The per-channel cast on a 4.9 GB bf16 input (300000 x 8192): a column's
+    result depends on that column only, so the oracle takes a slice of
+    columns over every row (the first and last chunks and chunks in
+    between), which must match bit for bit, codes of every row included."""
+    from oracle import parallel
+    T, H = 300_000, 8192
+    wl = wls.Workload("c", T, H, 0, scale_fmt, out_fmt, "col_lognormal", seed=77, op="cast", gran="channel")
+    x, _ = wls.make_inputs(wl, "cuda")
+    op = tk.QuantCast(H, 0, scale_fmt, out_fmt, "bf16", granularity="channel")
+    q, s = op(x)
+    torch.cuda.synchronize()
+    assert tk.tk_fault_word(torch.cuda.current_device()) == 0
+    for c0 in (0, 4096, H - 32):
+        xc = x[:, c0:c0 + 32].float().cpu().numpy()
+        rq, rs = parallel.quant_cols_f32(xc, scale_fmt, out_fmt)
+        gs = s[c0:c0 + 32].cpu().numpy()
+        if scale_fmt == "fp32":
+            assert np.array_equal(gs.view(np.uint32), rs.view(np.uint32)), c0
+        else:
+            assert np.array_equal(gs, rs), c0
+        gq = q[:, c0:c0 + 32].cpu().numpy() if out_fmt == "e4m3" else q[:, c0 // 2:c0 // 2 + 16].cpu().numpy()
+        assert np.array_equal(gq, rq), c0
+    del x, q, s
+    torch.cuda.empty_cache()
