@@ -23,7 +23,7 @@ from ._abi import (GRANULARITIES, IN_DTYPES, OUT_FMTS, REDUCE_IN_FMTS, SCALE_FMT
                    tk_moe_reduce_launch_info, tk_moe_reduce_run, tk_moe_reduce_validate,
                    TkError, tk_diag_unanswered_wait, tk_fault_word, tk_last_error_message, tk_quant_cast_output_sizes,
                    tk_quant_cast_plan, tk_quant_cast_plan_destroy,
-                   tk_quant_cast_run, tk_quant_cast_run_ws, tk_quant_cast_validate,
+                   tk_quant_cast_launch_info, tk_quant_cast_run, tk_quant_cast_run_ws, tk_quant_cast_validate,
                    tk_quant_cast_workspace_size, tk_status_string,
                    tk_swiglu_quant_host_pipe_create, tk_swiglu_quant_host_pipe_destroy,
                    tk_swiglu_quant_host_workspace_size, tk_swiglu_quant_launch_info,
@@ -47,7 +47,7 @@ __all__ = [
     "tk_swiglu_quant_run_mapped",
     "tk_quant_cast_validate", "tk_quant_cast_plan",
     "tk_quant_cast_plan_destroy", "tk_quant_cast_output_sizes", "tk_quant_cast_run", "tk_quant_cast_run_ws",
-    "tk_quant_cast_workspace_size", "tk_status_string",
+    "tk_quant_cast_workspace_size", "tk_quant_cast_launch_info", "tk_status_string",
     "tk_last_error_message", "tk_fault_word", "tk_diag_unanswered_wait",
 ]
 
@@ -298,9 +298,9 @@ class QuantCast:
     def workspace_bytes(self, T: int) -> int:
         return tk_quant_cast_workspace_size(self.plan, T)
 
-    def launches_per_run(self) -> int:
-        """Kernel launches one run enqueues (the per-channel cast: three)."""
-        return 3 if self.granularity == "channel" else 1
+    def launch_info(self, T: int) -> dict:
+        """Launches and kernels a run of T rows enqueues (tk_quant_cast_launch_info)."""
+        return tk_quant_cast_launch_info(self.plan, T)
 
     def __call__(self, x, *, q=None, scales=None, workspace=None, stream=None):
         torch = _torch()

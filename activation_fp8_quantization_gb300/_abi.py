@@ -91,6 +91,7 @@ SIGNATURES = {
     "tk_quant_cast_run": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP]),
     "tk_quant_cast_workspace_size": (ctypes.c_int, [_VP, ctypes.c_int64, _PSZ]),
     "tk_quant_cast_run_ws": (ctypes.c_int, [_VP, ctypes.c_int64, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
+    "tk_quant_cast_launch_info": (ctypes.c_int, [_VP, ctypes.c_int64, _PINT, _PINT]),
     "tk_moe_reduce_validate": (ctypes.c_int, [ctypes.POINTER(MoeReduceDesc)]),
     "tk_moe_reduce_plan": (ctypes.c_int, [ctypes.POINTER(MoeReduceDesc), ctypes.c_int, ctypes.POINTER(_VP)]),
     "tk_moe_reduce_plan_destroy": (ctypes.c_int, [_VP]),
@@ -276,6 +277,16 @@ def tk_quant_cast_run_ws(plan: int, num_tokens: int, x, q, scales, workspace, wo
                          stream: int | None) -> None:
     check(lib().tk_quant_cast_run_ws(plan, num_tokens, _ptr(x), _ptr(q), _ptr(scales), _ptr(workspace),
                                      workspace_bytes, stream))
+
+
+CAST_FORMS = {0: "row_quant_kernel", 1: "col_amax_kernel + col_chunk_quant_kernel",
+              2: "col_amax_kernel + col_scale_kernel + col_quant_kernel"}
+
+
+def tk_quant_cast_launch_info(plan: int, num_tokens: int) -> dict:
+    n, f = ctypes.c_int(), ctypes.c_int()
+    check(lib().tk_quant_cast_launch_info(plan, num_tokens, ctypes.byref(n), ctypes.byref(f)))
+    return {"launches": n.value, "form": f.value, "kernels": CAST_FORMS[f.value]}
 
 
 def tk_moe_reduce_validate(desc: MoeReduceDesc) -> int:

@@ -472,6 +472,7 @@ struct tk_quant_cast_plan_s {
     tk::ChannelFns cfn;
     Launch cq;
     int amax_ctas;
+    int channel_forced;   // TK_CHANNEL_KERNEL when the plan was made: 0 by size, 1 chunk, 2 split
 };
 
 // ------------------------------------------------------------------ fused op
@@ -1039,6 +1040,15 @@ TK_API tk_status tk_quant_cast_validate(const tk_quant_cast_desc *d)
 
 namespace {
 
+// Codes up to this size take the two-launch form (the chunk quantize pass on
+// the amax pass's grid, scales reduced in its prologue); larger outputs the
+// three-launch form (scale kernel, then the row quantize pass, whose CTAs
+// write whole rows in sequence). Measured on GB300 (fraction of the copy
+// bandwidth, chunk / three-launch): 8192 x 4096 E4M3 (33.5 MB of codes)
+// 0.842 / 0.785; 32768 x 4096 E2M1 (67 MB) 0.985 / 0.960; 16384 x 7168 E4M3
+// (117 MB) 0.788 / 0.881; fp32 input 8192 x 4096 0.929 / 0.930.
+constexpr size_t kChannelChunkMaxCodes = (size_t)96 << 20;
+
 // Plan the per-channel kernels: the quantize pass sized like the row kernel
 // (16 columns per thread, rows per CTA so that a CTA has about 256 threads),
 // the amax pass aiming at four CTAs per SM (each keeps 32 KB of loads in
@@ -1046,7 +1056,7 @@ namespace {
 tk_status plan_channel(const tk_quant_cast_desc *d, int device, tk_quant_cast_plan_s *p)
 {
     p->cfn = tk::channel_fns(d->in_dtype, d->out_fmt, d->scale_fmt, d->hidden);
-    if (!p->cfn.amax || !p->cfn.scale || !p->cfn.quant)
+    if (!p->cfn.amax || !p->cfn.scale || !p->cfn.quant || !p->cfn.chunk)
         return fail(TK_ERR_UNSUPPORTED, "no per-channel kernel for this combination");
     tk_status st = make_launch(device, d->hidden, 16, p->cfn.quant, kRows, 0, 0, &p->cq);
     if (st != TK_OK)
@@ -1061,12 +1071,18 @@ tk_status plan_channel(const tk_quant_cast_desc *d, int device, tk_quant_cast_pl
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, p->cfn.scale, tk::channel_scale_threads(), 0);
         if (e == cudaSuccess && occ2 < 1)
             return fail(TK_ERR_UNSUPPORTED, "the per-channel scale kernel cannot be resident");
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, p->cfn.chunk, tk::channel_amax_threads(), 0);
+        if (e == cudaSuccess && occ2 < 1)
+            return fail(TK_ERR_UNSUPPORTED, "the per-channel quantize kernel cannot be resident");
     }
     if (e != cudaSuccess)
         return cuda_fail(e, "occupancy of the per-channel kernels");
     if (occ < 1)
         return fail(TK_ERR_UNSUPPORTED, "the per-channel amax kernel cannot be resident");
     p->amax_ctas = (occ < 4 ? occ : 4) * p->cq.num_sms;
+    const char *force = getenv("TK_CHANNEL_KERNEL");
+    p->channel_forced = !force ? 0 : strcmp(force, "chunk") == 0 ? 1 : strcmp(force, "split") == 0 ? 2 : 0;
     return TK_OK;
 }
 
@@ -1086,6 +1102,8 @@ tk::ChannelLaunch channel_launch(const tk_quant_cast_plan_s *p, int64_t T)
     L.slabs = (int)((T + L.slab_rows - 1) / L.slab_rows);
     L.quant_grid = grid_for(p->cq, T);
     L.quant_block = p->cq.block;
+    const size_t q_bytes = (size_t)T * (size_t)(p->desc.out_fmt == TK_OUT_E4M3 ? p->desc.hidden : p->desc.hidden / 2);
+    L.split = p->channel_forced ? p->channel_forced == 2 : q_bytes > kChannelChunkMaxCodes;
     return L;
 }
 
@@ -1134,7 +1152,7 @@ TK_API tk_status tk_quant_cast_plan(const tk_quant_cast_desc *d, int device, tk_
                        bf16 ? tk::kCastBf16RowBytesPerCol : tk::kCastF32RowBytesPerCol, &Ls);
     if (st != TK_OK)
         return st;
-    auto *p = new (std::nothrow) tk_quant_cast_plan_s{*d, device, Ls, tk::ChannelFns{}, Launch{}, 0};
+    auto *p = new (std::nothrow) tk_quant_cast_plan_s{*d, device, Ls, tk::ChannelFns{}, Launch{}, 0, 0};
     if (!p)
         return fail(TK_ERR_INVALID_ARG, "out of host memory");
     *plan = p;
@@ -1227,6 +1245,23 @@ TK_API tk_status tk_quant_cast_workspace_size(tk_quant_cast_plan_t plan, int64_t
     if (!plan || !bytes || T < 0)
         return fail(TK_ERR_INVALID_ARG, "plan and bytes must be non-NULL and num_tokens >= 0");
     *bytes = plan->desc.granularity == TK_GRAN_PER_CHANNEL ? channel_workspace(plan, T) : 0;
+    return ok();
+}
+
+TK_API tk_status tk_quant_cast_launch_info(tk_quant_cast_plan_t plan, int64_t T, int *launches, int *form)
+{
+    if (!plan || T < 0)
+        return fail(TK_ERR_INVALID_ARG, "plan is NULL or num_tokens < 0");
+    int n = 1, f = TK_CAST_ROWS;
+    if (plan->desc.granularity == TK_GRAN_PER_CHANNEL) {
+        const bool split = channel_launch(plan, T > 0 ? T : 1).split;
+        n = split ? 3 : 2;
+        f = split ? TK_CAST_CHANNEL_SPLIT : TK_CAST_CHANNEL_CHUNK;
+    }
+    if (launches)
+        *launches = T == 0 ? 0 : n;
+    if (form)
+        *form = f;
     return ok();
 }
 

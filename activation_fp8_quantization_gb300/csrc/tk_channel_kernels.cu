@@ -5,28 +5,28 @@
 // per-channel granularity of FP8 E4M3).
 //
 // A column's scale depends on every row, so no row can be encoded before the
-// whole input has been read once: the cast reads x twice. Three launches,
-// chained by programmatic dependent launch (each waits for the previous one
-// in griddepcontrol.wait before its first global access):
+// whole input has been read once: the cast reads x twice. Two or three
+// launches, chained by programmatic dependent launch (each waits for the
+// previous one in griddepcontrol.wait before its first global access):
 //
 //  1. col_amax_kernel: CTA (c, s) takes the 512-column chunk c of the row
 //     slab s; its eight warps take the slab's rows in turn (warp w: rows
-//     w, w + 8, ...), a lane 16 columns of each (32-byte loads, four rows in
-//     flight), keeping the running |x| maximum in registers (bf16 pairs by
-//     packed max, exact). The warps' maxima meet in shared memory and the CTA
-//     writes one fp32 partial maximum per column: partial[s, col].
-//  2. col_scale_kernel: one CTA per 32 columns, 32 threads per column, each
-//     the maximum over a stride of the partials, then one shared-memory
-//     reduction: amax, then the scale by the same rules as the per-block
-//     cast (fp32 amax / Qmax correctly rounded, 1 for a zero column; UE8M0
-//     2^k, k the smallest with Qmax * 2^k >= amax).
-//  3. col_quant_kernel: the row kernel's mapping (16 columns per thread,
-//     H / 16 threads per row, a persistent grid over row blocks, the next
-//     block's loads in flight): each thread reads its 16 column scales once
-//     and keeps them, with their negated reciprocals, in registers; every
-//     value then costs one correctly rounded quotient (Markstein's
-//     correction, or an exact power-of-two multiply) and its share of a
-//     packed conversion.
+//     w, w + 8, ...), a lane 16 columns of each (32-byte loads), two sets of
+//     rows in flight, keeping the running |x| maximum in registers (bf16
+//     pairs by packed max, exact). The warps' maxima meet in shared memory
+//     and the CTA writes one fp32 partial maximum per column: partial[s, col].
+//  2. Either col_chunk_quant_kernel on the same grid: CTA (c, s) reduces the
+//     partials of its own 512 columns into their scales (the slab-0 CTA also
+//     stores them) and encodes its slab of that chunk;
+//     or col_scale_kernel (one CTA per 32 columns reduces the partials into
+//     the scales) followed by col_quant_kernel: the row kernel's mapping (16
+//     columns per thread, H / 16 threads per row, a persistent grid over row
+//     blocks, the next block's loads in flight), each thread holding its 16
+//     column scales. The first saves a launch and suits outputs that L2
+//     absorbs; the second writes whole rows in sequence, which large outputs
+//     need. Either way a value costs one correctly rounded quotient
+//     (Markstein's correction, or an exact power-of-two multiply) and its
+//     share of a packed conversion.
 #include "tk_internal.h"
 
 namespace tk {
@@ -338,6 +338,149 @@ __global__ void __launch_bounds__(MAXT) col_quant_kernel(CastArgs a, OutArgs o, 
     }
 }
 
+// Rows per load set of the chunk quantize pass (two sets in flight per
+// warp): what the registers allow beside the 16 column scales.
+template <bool BF16, int SCALE>
+constexpr int kChunkUnroll = BF16 ? (SCALE == kScaleUE8M0 ? 3 : 2) : (SCALE == kScaleUE8M0 ? 2 : 1);
+
+// The quantize pass over the amax pass's grid: CTA (c, s) takes the same
+// 512-column chunk c and row slab s. It first reduces the slabs' partial
+// maxima of its own 512 columns (warp w reads slabs w, w + 8, ...; the warps
+// meet in shared memory) into the chunk's scales, which the slab-0 CTA of the
+// chunk also writes out; so no separate scale kernel runs. It then walks its
+// slab from the last row back: the amax pass read each slab front to back,
+// so the rows it read last, the ones most likely still in L2, come first.
+template <class Src, bool BF16, int OUT, int SCALE>
+__global__ void __launch_bounds__(kAmaxThreads, 2) col_chunk_quant_kernel(CastArgs a, int64_t T, int64_t slab_rows,
+                                                                        const float *partial, int slabs, OutArgs o)
+{
+    __shared__ __align__(16) float red[kAmaxWarps][512];
+    __shared__ __align__(16) uint8_t sclbuf[512 * 4];   // the chunk's scales, in the output's format
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int chunk0 = (int)blockIdx.x * 512;
+    const int col0 = chunk0 + lane * kEPT;
+    const bool col_ok = col0 < a.H;
+    const int64_t r0 = (int64_t)blockIdx.y * slab_rows;
+    const int64_t r1 = (T - r0) < slab_rows ? T : r0 + slab_rows;
+    pdl_wait();
+    pdl_launch_dependents();
+
+    // 1. the chunk's column maxima over every slab's partial
+    {
+        float m[kEPT];
+#pragma unroll
+        for (int j = 0; j < kEPT; ++j)
+            m[j] = 0.0f;
+        if (col_ok)
+            for (int sl = warp; sl < slabs; sl += kAmaxWarps) {
+                const float4 *p = reinterpret_cast<const float4 *>(partial + (int64_t)sl * a.H + col0);
+#pragma unroll
+                for (int k = 0; k < kEPT / 4; ++k) {
+                    const float4 v = p[k];
+                    m[4 * k] = fmaxf(m[4 * k], v.x);
+                    m[4 * k + 1] = fmaxf(m[4 * k + 1], v.y);
+                    m[4 * k + 2] = fmaxf(m[4 * k + 2], v.z);
+                    m[4 * k + 3] = fmaxf(m[4 * k + 3], v.w);
+                }
+            }
+        float4 *dst = reinterpret_cast<float4 *>(&red[warp][lane * kEPT]);
+#pragma unroll
+        for (int k = 0; k < kEPT / 4; ++k)
+            dst[k] = make_float4(m[4 * k], m[4 * k + 1], m[4 * k + 2], m[4 * k + 3]);
+    }
+    __syncthreads();
+    // 2. amax -> scale, by the per-block cast's rules
+    for (int c = threadIdx.x; c < 512; c += kAmaxThreads) {
+        float m = red[0][c];
+#pragma unroll
+        for (int w = 1; w < kAmaxWarps; ++w)
+            m = fmaxf(m, red[w][c]);
+        const bool out_col = blockIdx.y == 0 && chunk0 + c < a.H;
+        if (SCALE == kScaleUE8M0) {
+            const uint8_t byte = (uint8_t)(ue8m0_exponent<OUT>(m) + 127);
+            sclbuf[c] = byte;
+            if (out_col)
+                static_cast<uint8_t *>(o.scales)[chunk0 + c] = byte;
+        } else {
+            float sc;
+            if (m >= 0x1p-64f) {
+                sc = div_markstein1(m, Fmt<OUT>::kQmax, Fmt<OUT>::kRcpQmax);
+            } else {
+                sc = __fdiv_rn(m, Fmt<OUT>::kQmax);
+                if (sc == 0.0f)
+                    sc = 1.0f;
+            }
+            reinterpret_cast<float *>(sclbuf)[c] = sc;
+            if (out_col)
+                static_cast<float *>(o.scales)[chunk0 + c] = sc;
+        }
+    }
+    __syncthreads();
+    ColScales<SCALE> cs;
+    cs.load(sclbuf, lane * kEPT);
+
+    // 3. the slab's rows, last first; warp w takes rows r1-1-w, r1-1-w-8, ...
+    Src src;
+    constexpr int U = kChunkUnroll<BF16, SCALE>;
+    constexpr int64_t kStep = (int64_t)U * kAmaxWarps;
+    typename Src::Regs va[U], vb[U];
+    auto row_of = [&](int64_t j, int u) { return r1 - 1 - warp - (j + u) * kAmaxWarps; };
+    auto fetch = [&](int64_t j, typename Src::Regs (&v)[U]) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t row = row_of(j, u);
+            if (col_ok && row >= r0)
+                Src::load(a, row, col0, v[u]);
+            else
+                Src::zero(v[u]);
+        }
+    };
+    auto encode = [&](int64_t j, const typename Src::Regs (&v)[U]) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t row = row_of(j, u);
+            if (!col_ok || row < r0)
+                continue;
+            uint64_t ny[kEPT / 2];
+            float amax_unused = 0.0f;
+            src.produce(a, v[u], true, ny, amax_unused);
+            uint64_t q[kEPT / 2];
+            cs.divide(ny, q);
+            if (OUT == kOutE4M3) {
+                uint32_t w[4];
+                e4m3_words(q, w);
+                st_stream_128(o.q + row * (int64_t)a.H + col0, w[0], w[1], w[2], w[3]);
+            } else {
+                const uint32_t w0 = cvt_e2m1x8(q[0], q[1], q[2], q[3]);
+                const uint32_t w1 = cvt_e2m1x8(q[4], q[5], q[6], q[7]);
+                st_stream_64(o.q + row * (int64_t)(a.H / 2) + col0 / 2, w0, w1);
+            }
+        }
+    };
+    // rows per warp: ceil((r1 - r0 - warp) / 8)
+    const int64_t nrow = (r1 - r0 - warp + kAmaxWarps - 1) / kAmaxWarps;
+    int64_t j = 0;
+    fetch(j, va);
+    while (j < nrow) {
+        fetch(j + U, vb);
+        encode(j, va);
+        j += U;
+        if (j >= nrow)
+            break;
+        fetch(j + U, va);
+        encode(j, vb);
+        j += U;
+    }
+}
+
+template <class Src, bool BF16, int OUT>
+const void *chunk_pick(int scale_fmt)
+{
+    return scale_fmt == kScaleF32 ? reinterpret_cast<const void *>(&col_chunk_quant_kernel<Src, BF16, OUT, kScaleF32>)
+                                  : reinterpret_cast<const void *>(&col_chunk_quant_kernel<Src, BF16, OUT, kScaleUE8M0>);
+}
+
 template <class Src, int OUT, int MAXT>
 const void *quant_pick(int scale_fmt)
 {
@@ -392,6 +535,12 @@ ChannelFns channel_fns(int in_dtype, int out_fmt, int scale_fmt, int64_t hidden)
     const bool wide = hidden > 8192;   // more than 512 threads per row
     f.quant = in_dtype == 0 ? quant_pick_out<CastBf16Src>(out_fmt, scale_fmt, wide)
                             : quant_pick_out<CastF32Src>(out_fmt, scale_fmt, wide);
+    if (in_dtype == 0)
+        f.chunk = out_fmt == kOutE4M3 ? chunk_pick<CastBf16Src, true, kOutE4M3>(scale_fmt)
+                                      : chunk_pick<CastBf16Src, true, kOutE2M1>(scale_fmt);
+    else
+        f.chunk = out_fmt == kOutE4M3 ? chunk_pick<CastF32Src, false, kOutE4M3>(scale_fmt)
+                                      : chunk_pick<CastF32Src, false, kOutE2M1>(scale_fmt);
     return f;
 }
 
@@ -408,8 +557,16 @@ cudaError_t launch_channel(const ChannelFns &f, const ChannelLaunch &L, const Ca
     cudaError_t e = launch_grid(f.amax, dim3(L.chunks, L.slabs), kAmaxThreads, args1, stream);
     if (e != cudaSuccess)
         return e;
+    const int nparts = L.slabs;   // partial maxima per column
+    if (!L.split) {
+        const float *cpart = partial;
+        int slabs = nparts;
+        OutArgs o_ = o;
+        void *args2[] = {&a_, &T, &slab_rows, &cpart, &slabs, &o_};
+        return launch_grid(f.chunk, dim3(L.chunks, L.slabs), kAmaxThreads, args2, stream);
+    }
     const float *cpart = partial;
-    int slabs = L.slabs, H = a.H;
+    int slabs = nparts, H = a.H;
     void *sc = o.scales;
     void *args2[] = {&cpart, &slabs, &H, &sc};
     e = launch_grid(f.scale, dim3((H + 31) / 32), kScaleThreads, args2, stream);

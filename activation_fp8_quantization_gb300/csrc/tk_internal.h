@@ -30,6 +30,7 @@ struct ChannelFns {
     const void *amax;
     const void *scale;
     const void *quant;
+    const void *chunk;   // the quantize pass on the amax pass's grid, scales reduced in its prologue
 };
 // One run's launch shape: the amax pass runs (chunks x slabs) CTAs, each over
 // slab_rows rows of a 512-column chunk; the quantize pass is a persistent
@@ -41,6 +42,7 @@ struct ChannelLaunch {
     int64_t slab_rows;
     int quant_grid;
     int quant_block;
+    bool split;   // three launches (amax, scale, row quantize) instead of two (amax, chunk quantize)
 };
 ChannelFns channel_fns(int in_dtype, int out_fmt, int scale_fmt, int64_t hidden);
 int channel_amax_threads();

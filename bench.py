@@ -462,12 +462,10 @@ class FusedBench:
             return "transpose_quant_kernel"
         if self.wl.op == "swiglu":
             return self.op.launch_info(self.wl.T)["kernel"]
-        if self.wl.channel:
-            return "col_amax_kernel + col_scale_kernel + col_quant_kernel"
-        return "row_quant_kernel"
+        return self.op.launch_info(self.wl.T)["kernels"]
 
     def launches_per_step(self) -> int:
-        return self.op.launches_per_run() if self.wl.op == "cast" else 1
+        return self.op.launch_info(self.wl.T)["launches"] if self.wl.op == "cast" else 1
 
 
 def time_steady(fb: FusedBench, min_ms: float, sample_clocks: bool) -> dict:

@@ -347,8 +347,8 @@ tk_status tk_quant_cast_run(tk_quant_cast_plan_t plan, int64_t num_tokens, const
 /* Bytes of device workspace tk_quant_cast_run_ws needs for num_tokens rows
  * (host only): 0 for per-token and per-block plans; for a per-channel plan
  * one fp32 partial column maximum per row slab of the first pass and column,
- * at most ceil(4 * SMs / ceil(H / 512)) * H * 4 bytes (4 MiB at H = 7168 on
- * 152 SMs, independent of T beyond a few thousand rows). */
+ * at most ceil(4 * SMs / ceil(H / 512)) * H * 4 bytes (about 1.3 MB at
+ * H = 7168 on 152 SMs, independent of T beyond a few thousand rows). */
 tk_status tk_quant_cast_workspace_size(tk_quant_cast_plan_t plan, int64_t num_tokens, size_t *bytes);
 
 /* Enqueue the cast with a caller-owned workspace (any granularity).
@@ -362,10 +362,25 @@ tk_status tk_quant_cast_workspace_size(tk_quant_cast_plan_t plan, int64_t num_to
  *                       is left holding intermediate values.
  * A per-channel column scale depends on every row, so the cast reads x
  * twice: one launch takes column maxima over row slabs into the workspace,
- * one reduces them to the scales, one encodes every row (three kernels,
- * stream-ordered). num_tokens == 0 is a no-op (no scale is written). */
+ * then either one launch reduces them per 512-column chunk and encodes
+ * (outputs up to 96 MiB of codes) or two launches reduce them to the scales
+ * and encode every row (larger outputs); stream-ordered. num_tokens == 0 is
+ * a no-op (no scale is written). */
 tk_status tk_quant_cast_run_ws(tk_quant_cast_plan_t plan, int64_t num_tokens, const void *x, void *q,
                                void *scales, void *workspace, size_t workspace_bytes, void *stream);
+
+/* What a cast run of num_tokens rows enqueues (host only): *launches kernel
+ * launches (0 when num_tokens == 0) and *form: TK_CAST_ROWS (one launch; per
+ * token or per block), TK_CAST_CHANNEL_CHUNK (per channel: the amax pass,
+ * then the quantize pass on the same grid, which reduces its own scales) or
+ * TK_CAST_CHANNEL_SPLIT (per channel: the amax pass, the scale kernel, the
+ * row quantize pass). Either output pointer may be NULL. */
+typedef enum tk_cast_form {
+    TK_CAST_ROWS = 0,
+    TK_CAST_CHANNEL_CHUNK = 1,
+    TK_CAST_CHANNEL_SPLIT = 2
+} tk_cast_form;
+tk_status tk_quant_cast_launch_info(tk_quant_cast_plan_t plan, int64_t num_tokens, int *launches, int *form);
 
 /* ------------------------------------------------------------------------
  * Weighted top-k combine after the expert GEMMs

@@ -20,6 +20,15 @@ from activation_fp8_quantization_gb300 import workloads as wls
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True, params=["chunk", "split"])
+def channel_kernel(request, monkeypatch):
+    """Every test runs on both forms of the cast (read when a plan is made):
+    the chunk quantize pass, which reduces its scales itself, and the scale
+    kernel followed by the row quantize pass."""
+    monkeypatch.setenv("TK_CHANNEL_KERNEL", request.param)
+    return request.param
+
+
 def _shaped_input(T, H, in_dtype, seed):
     rng = np.random.default_rng(seed)
     v = rng.standard_normal((T, H)) * np.exp2(rng.integers(-40, 40, (1, H)))
@@ -150,3 +159,21 @@ def test_channel_argument_errors():
     q2, s2 = op2(x)
     torch.cuda.synchronize()
     assert bool((s2 == 1.0).all()) and not bool(q2.any())
+
+
+def test_channel_launch_info(channel_kernel, monkeypatch):
+    """The plan picks the form by the size of the codes (96 MiB), unless
+    TK_CHANNEL_KERNEL forces one; launch_info reports the choice."""
+    monkeypatch.delenv("TK_CHANNEL_KERNEL")
+    op = tk.QuantCast(7168, 0, "ue8m0", "e4m3", "bf16", granularity="channel")
+    assert op.launch_info(0)["launches"] == 0
+    small = op.launch_info(8192)               # 56 MiB of codes
+    big = op.launch_info(16384)                # 112 MiB
+    assert (small["form"], small["launches"]) == (1, 2)
+    assert (big["form"], big["launches"]) == (2, 3)
+    monkeypatch.setenv("TK_CHANNEL_KERNEL", channel_kernel)
+    forced = tk.QuantCast(7168, 0, "ue8m0", "e4m3", "bf16", granularity="channel")
+    want = 1 if channel_kernel == "chunk" else 2
+    assert forced.launch_info(8192)["form"] == want and forced.launch_info(16384)["form"] == want
+    per_block = tk.QuantCast(7168, 128, "ue8m0", "e4m3", "bf16")
+    assert per_block.launch_info(100)["launches"] == 1 and per_block.launch_info(100)["form"] == 0
