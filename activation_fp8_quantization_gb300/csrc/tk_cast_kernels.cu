@@ -5,26 +5,27 @@ namespace tk {
 
 namespace {
 template <class Src, int OUT, int SCALE, bool CTA>
-const void *fn()
+const void *fn(bool pf)
 {
-    return reinterpret_cast<const void *>(&row_quant_kernel<Src, OUT, SCALE, CTA>);
+    return pf ? reinterpret_cast<const void *>(&row_quant_kernel<Src, OUT, SCALE, CTA, true>)
+              : reinterpret_cast<const void *>(&row_quant_kernel<Src, OUT, SCALE, CTA, false>);
 }
 
 template <class Src, int OUT>
-const void *pick(int scale_fmt, bool cta)
+const void *pick(int scale_fmt, bool cta, bool pf)
 {
     if (scale_fmt == kScaleF32)
-        return cta ? fn<Src, OUT, kScaleF32, true>() : fn<Src, OUT, kScaleF32, false>();
-    return cta ? fn<Src, OUT, kScaleUE8M0, true>() : fn<Src, OUT, kScaleUE8M0, false>();
+        return cta ? fn<Src, OUT, kScaleF32, true>(pf) : fn<Src, OUT, kScaleF32, false>(pf);
+    return cta ? fn<Src, OUT, kScaleUE8M0, true>(pf) : fn<Src, OUT, kScaleUE8M0, false>(pf);
 }
 
 template <class Src>
-const void *pick_out(int out_fmt, int scale_fmt, bool cta)
+const void *pick_out(int out_fmt, int scale_fmt, bool cta, bool pf)
 {
     if (out_fmt == kOutE4M3)
-        return pick<Src, kOutE4M3>(scale_fmt, cta);
+        return pick<Src, kOutE4M3>(scale_fmt, cta, pf);
     if (out_fmt == kOutE2M1)
-        return pick<Src, kOutE2M1>(scale_fmt, cta);
+        return pick<Src, kOutE2M1>(scale_fmt, cta, pf);
     return nullptr;
 }
 template <class Src>
@@ -69,12 +70,12 @@ const void *cast_stream_fn(int in_dtype, int out_fmt, int scale_fmt)
     return nullptr;
 }
 
-const void *cast_kernel_fn(int in_dtype, int out_fmt, int scale_fmt, bool cta_reduce)
+const void *cast_kernel_fn(int in_dtype, int out_fmt, int scale_fmt, bool cta_reduce, bool prefetch)
 {
     if (in_dtype == 0)
-        return pick_out<CastBf16Src>(out_fmt, scale_fmt, cta_reduce);
+        return pick_out<CastBf16Src>(out_fmt, scale_fmt, cta_reduce, prefetch);
     if (in_dtype == 1)
-        return pick_out<CastF32Src>(out_fmt, scale_fmt, cta_reduce);
+        return pick_out<CastF32Src>(out_fmt, scale_fmt, cta_reduce, prefetch);
     return nullptr;
 }
 

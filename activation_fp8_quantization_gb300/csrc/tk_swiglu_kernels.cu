@@ -5,17 +5,18 @@ namespace tk {
 
 namespace {
 template <int OUT, int SCALE, bool CLAMP, bool CTA>
-const void *fn()
+const void *fn(bool pf)
 {
-    return reinterpret_cast<const void *>(&row_quant_kernel<SwigluSrc<CLAMP>, OUT, SCALE, CTA>);
+    return pf ? reinterpret_cast<const void *>(&row_quant_kernel<SwigluSrc<CLAMP>, OUT, SCALE, CTA, true>)
+              : reinterpret_cast<const void *>(&row_quant_kernel<SwigluSrc<CLAMP>, OUT, SCALE, CTA, false>);
 }
 
 template <int OUT, int SCALE>
-const void *pick(bool clamp, bool cta)
+const void *pick(bool clamp, bool cta, bool pf)
 {
     if (clamp)
-        return cta ? fn<OUT, SCALE, true, true>() : fn<OUT, SCALE, true, false>();
-    return cta ? fn<OUT, SCALE, false, true>() : fn<OUT, SCALE, false, false>();
+        return cta ? fn<OUT, SCALE, true, true>(pf) : fn<OUT, SCALE, true, false>(pf);
+    return cta ? fn<OUT, SCALE, false, true>(pf) : fn<OUT, SCALE, false, false>(pf);
 }
 template <int OUT, int SCALE>
 const void *stream_fn(bool clamp)
@@ -49,14 +50,14 @@ const void *swiglu_stream_fn(int out_fmt, int scale_fmt, bool clamp)
     return nullptr;
 }
 
-const void *swiglu_kernel_fn(int out_fmt, int scale_fmt, bool clamp, bool cta_reduce)
+const void *swiglu_kernel_fn(int out_fmt, int scale_fmt, bool clamp, bool cta_reduce, bool prefetch)
 {
     if (out_fmt == kOutE4M3)
-        return scale_fmt == kScaleF32 ? pick<kOutE4M3, kScaleF32>(clamp, cta_reduce)
-                                      : pick<kOutE4M3, kScaleUE8M0>(clamp, cta_reduce);
+        return scale_fmt == kScaleF32 ? pick<kOutE4M3, kScaleF32>(clamp, cta_reduce, prefetch)
+                                      : pick<kOutE4M3, kScaleUE8M0>(clamp, cta_reduce, prefetch);
     if (out_fmt == kOutE2M1)
-        return scale_fmt == kScaleF32 ? pick<kOutE2M1, kScaleF32>(clamp, cta_reduce)
-                                      : pick<kOutE2M1, kScaleUE8M0>(clamp, cta_reduce);
+        return scale_fmt == kScaleF32 ? pick<kOutE2M1, kScaleF32>(clamp, cta_reduce, prefetch)
+                                      : pick<kOutE2M1, kScaleUE8M0>(clamp, cta_reduce, prefetch);
     return nullptr;
 }
 
