@@ -474,8 +474,10 @@ struct tk_swiglu_quant_plan_s {
     tk_swiglu_quant_desc desc;
     int device;
     Launches Ls;
-    // transposed-codes kernel (null where the shape does not allow it)
+    // transposed-codes kernel (null where the shape does not allow it), and
+    // its form that prefetches its first tile (runs with few tiles per CTA)
     const void *tfn;
+    const void *tfn_pf;
     int tgrid;
 };
 
@@ -533,11 +535,12 @@ TK_API tk_status tk_swiglu_quant_plan(const tk_swiglu_quant_desc *d, int device,
     Ls.rows.fn_pf = tk::swiglu_kernel_fn(d->out_fmt, d->scale_fmt, clamp, geo.cta_reduce, true);
     // The transposed-codes kernel: E4M3, groups of 32, 64 or 128 columns
     // inside its 128-column tiles.
-    const void *tfn = nullptr;
+    const void *tfn = nullptr, *tfn_pf = nullptr;
     int tgrid = 0;
     if (d->out_fmt == TK_OUT_E4M3 && d->hidden % 128 == 0 &&
         (d->group_size == 32 || d->group_size == 64 || d->group_size == 128)) {
-        tfn = tk::transpose_kernel_fn(d->scale_fmt, clamp);
+        tfn = tk::transpose_kernel_fn(d->scale_fmt, clamp, false);
+        tfn_pf = tk::transpose_kernel_fn(d->scale_fmt, clamp, true);
         int occ = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, tfn, tk::transpose_threads(), 0);
         if (e != cudaSuccess)
@@ -546,7 +549,7 @@ TK_API tk_status tk_swiglu_quant_plan(const tk_swiglu_quant_desc *d, int device,
         if (tgrid < 1)
             tfn = nullptr;
     }
-    auto *p = new (std::nothrow) tk_swiglu_quant_plan_s{*d, device, Ls, tfn, tgrid};
+    auto *p = new (std::nothrow) tk_swiglu_quant_plan_s{*d, device, Ls, tfn, tfn_pf, tgrid};
     if (!p)
         return fail(TK_ERR_INVALID_ARG, "out of host memory");
     *plan = p;
@@ -735,7 +738,8 @@ TK_API tk_status tk_swiglu_quant_run_transposed(tk_swiglu_quant_plan_t plan, int
     const int64_t ldq = (T + 31) / 32 * 32;
     const int64_t tiles = (T + 31) / 32 * (d.hidden / 128);
     const int grid = (int)(tiles < plan->tgrid ? tiles : plan->tgrid);
-    cudaError_t e = tk::launch_transpose(plan->tfn, grid, a, o, sh, ldq, static_cast<cudaStream_t>(stream));
+    const void *fn = tiles <= 32 * (int64_t)grid ? plan->tfn_pf : plan->tfn;
+    cudaError_t e = tk::launch_transpose(fn, grid, a, o, sh, ldq, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the transposed kernel");
     return ok();
@@ -1578,6 +1582,7 @@ struct tk_swiglu_backward_plan_s {
     tk_swiglu_backward_desc desc;
     int device;
     const void *fn;
+    const void *fn_pf;   // the form that prefetches its first row block (runs with few row blocks per CTA)
     int block, tpr, rpc, tpg_log2, groups, max_grid;
     unsigned *fault;
 };
@@ -1635,7 +1640,8 @@ TK_API tk_status tk_swiglu_backward_plan(const tk_swiglu_backward_desc *d, int d
     tk_swiglu_backward_plan_s p{};
     p.desc = *d;
     p.device = device;
-    p.fn = tk::backward_kernel_fn(d->use_clamp != 0, d->recompute_quant != 0, d->out_fmt, d->scale_fmt);
+    p.fn = tk::backward_kernel_fn(d->use_clamp != 0, d->recompute_quant != 0, d->out_fmt, d->scale_fmt, false);
+    p.fn_pf = tk::backward_kernel_fn(d->use_clamp != 0, d->recompute_quant != 0, d->out_fmt, d->scale_fmt, true);
     p.tpr = (int)(d->hidden / tk::kEPT);
     p.rpc = p.tpr >= 256 ? 1 : 256 / p.tpr;
     p.block = ((p.tpr * p.rpc + 31) / 32) * 32;   // <= 512 for hidden <= 8192
@@ -1716,7 +1722,8 @@ TK_API tk_status tk_swiglu_backward_run(tk_swiglu_backward_plan_t plan, int64_t 
                           plan->fault, layout, scale_ld(layout, d.scale_fmt, T)};
     const int64_t nrb = (T + plan->rpc - 1) / plan->rpc;
     const int grid = (int)(nrb < plan->max_grid ? nrb : plan->max_grid);
-    cudaError_t e = tk::launch_backward(plan->fn, grid, plan->block, a, o, sh, static_cast<cudaStream_t>(stream));
+    const void *fn = nrb <= 32 * (int64_t)grid ? plan->fn_pf : plan->fn;
+    cudaError_t e = tk::launch_backward(fn, grid, plan->block, a, o, sh, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the backward kernel");
     return ok();

@@ -36,7 +36,7 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
 // left to itself the compiler gives the clamping, recomputing forms over 100,
 // which halves the CTAs per SM and was measured 25% slower than the few
 // bytes of spills the cap costs.
-template <bool CLAMP, bool RECOMPUTE, int OUT, int SCALE>
+template <bool CLAMP, bool RECOMPUTE, int OUT, int SCALE, bool PREFETCH>
 __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a, OutArgs o, RowShape sh)
 {
     __shared__ float red[2][16];   // per-warp partial dw, double-buffered by row block
@@ -54,6 +54,14 @@ __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a,
     const float L = a.limit;
     constexpr float kNegHalfLog2e = -0.72134752044448170368f;  // -log2(e) / 2
     const bool wide = aligned32(a.dx);   // uniform: a row's halves stay 32-byte aligned (H % 16 == 0)
+    // PREFETCH (the plan's choice where a CTA has few row blocks): the first
+    // row block's x and dy into L2 before waiting on the previous kernel
+    if (PREFETCH && slot_ok && (int64_t)blockIdx.x < nrb && (int64_t)blockIdx.x * sh.rpc + slot < sh.T) {
+        const int64_t row = (int64_t)blockIdx.x * sh.rpc + slot;
+        prefetch_l2(a.x + row * (2 * (int64_t)a.H) + col0);
+        prefetch_l2(a.x + row * (2 * (int64_t)a.H) + a.H + col0);
+        prefetch_l2(a.dy + row * (int64_t)a.H + col0);
+    }
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t rb = blockIdx.x; rb < nrb; rb += gridDim.x) {
@@ -170,26 +178,33 @@ __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a,
     }
 }
 
-template <bool CLAMP>
+template <bool CLAMP, bool PF>
 const void *pick_recompute(int out_fmt, int scale_fmt)
 {
     if (out_fmt == kOutE4M3)
         return scale_fmt == kScaleF32
-                   ? reinterpret_cast<const void *>(&swiglu_backward_kernel<CLAMP, true, kOutE4M3, kScaleF32>)
-                   : reinterpret_cast<const void *>(&swiglu_backward_kernel<CLAMP, true, kOutE4M3, kScaleUE8M0>);
+                   ? reinterpret_cast<const void *>(&swiglu_backward_kernel<CLAMP, true, kOutE4M3, kScaleF32, PF>)
+                   : reinterpret_cast<const void *>(&swiglu_backward_kernel<CLAMP, true, kOutE4M3, kScaleUE8M0, PF>);
     return scale_fmt == kScaleF32
-               ? reinterpret_cast<const void *>(&swiglu_backward_kernel<CLAMP, true, kOutE2M1, kScaleF32>)
-               : reinterpret_cast<const void *>(&swiglu_backward_kernel<CLAMP, true, kOutE2M1, kScaleUE8M0>);
+               ? reinterpret_cast<const void *>(&swiglu_backward_kernel<CLAMP, true, kOutE2M1, kScaleF32, PF>)
+               : reinterpret_cast<const void *>(&swiglu_backward_kernel<CLAMP, true, kOutE2M1, kScaleUE8M0, PF>);
+}
+
+template <bool PF>
+const void *pick_backward(bool clamp, bool recompute, int out_fmt, int scale_fmt)
+{
+    if (!recompute)
+        return clamp ? reinterpret_cast<const void *>(&swiglu_backward_kernel<true, false, kOutE4M3, kScaleF32, PF>)
+                     : reinterpret_cast<const void *>(&swiglu_backward_kernel<false, false, kOutE4M3, kScaleF32, PF>);
+    return clamp ? pick_recompute<true, PF>(out_fmt, scale_fmt) : pick_recompute<false, PF>(out_fmt, scale_fmt);
 }
 
 }  // namespace
 
-const void *backward_kernel_fn(bool clamp, bool recompute, int out_fmt, int scale_fmt)
+const void *backward_kernel_fn(bool clamp, bool recompute, int out_fmt, int scale_fmt, bool prefetch)
 {
-    if (!recompute)
-        return clamp ? reinterpret_cast<const void *>(&swiglu_backward_kernel<true, false, kOutE4M3, kScaleF32>)
-                     : reinterpret_cast<const void *>(&swiglu_backward_kernel<false, false, kOutE4M3, kScaleF32>);
-    return clamp ? pick_recompute<true>(out_fmt, scale_fmt) : pick_recompute<false>(out_fmt, scale_fmt);
+    return prefetch ? pick_backward<true>(clamp, recompute, out_fmt, scale_fmt)
+                    : pick_backward<false>(clamp, recompute, out_fmt, scale_fmt);
 }
 
 cudaError_t launch_backward(const void *fn, int grid, int block, const BackwardArgs &a, const OutArgs &o,

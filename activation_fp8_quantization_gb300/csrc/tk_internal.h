@@ -104,7 +104,7 @@ constexpr int kReduceMetaBytes = 8 * 32 * 8;   // the producer's metadata ring (
 constexpr int kReduceMaxStages = 16;
 
 // Fused op with the codes written transposed (E4M3, groups of 32/64/128).
-const void *transpose_kernel_fn(int scale_fmt, bool clamp);
+const void *transpose_kernel_fn(int scale_fmt, bool clamp, bool prefetch);
 int transpose_threads();
 cudaError_t launch_transpose(const void *fn, int grid, const SwigluArgs &a, const OutArgs &o, const RowShape &sh,
                              int64_t ldq, cudaStream_t stream);
@@ -119,7 +119,7 @@ struct BackwardArgs {
     float limit;          // clamp limit (clamping instantiations)
     int32_t H;
 };
-const void *backward_kernel_fn(bool clamp, bool recompute, int out_fmt, int scale_fmt);
+const void *backward_kernel_fn(bool clamp, bool recompute, int out_fmt, int scale_fmt, bool prefetch);
 cudaError_t launch_backward(const void *fn, int grid, int block, const BackwardArgs &a, const OutArgs &o,
                             const RowShape &sh, cudaStream_t stream);
 

@@ -35,7 +35,7 @@ constexpr int kTileStride = 144;   // bytes per shared row: 16-byte aligned, con
 constexpr int kTransposeThreads = 128;
 constexpr int kPassRows = kTransposeThreads / 8;
 
-template <int SCALE, bool CLAMP>
+template <int SCALE, bool CLAMP, bool PREFETCH>
 __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(SwigluArgs a, OutArgs o, RowShape sh,
                                                                               int64_t ldq)
 {
@@ -52,6 +52,18 @@ __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(Swig
     // uniform: every qT row starts 32-byte aligned, so each thread's 32 rows
     // of one column go out as one sector-sized store
     const bool wide = (ldq & 31) == 0 && aligned32(o.q);
+    // PREFETCH (the plan's choice where a CTA has few tiles): the first
+    // tile's rows into L2 before waiting on the previous kernel
+    if (PREFETCH && (int64_t)blockIdx.x < ntiles) {
+        const int64_t tb = blockIdx.x / ncb;
+        const int c0 = (int)(blockIdx.x - tb * ncb) * kTileCols;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const int64_t row = tb * kTileRows + p * kPassRows + rr;
+            if (row < sh.T)
+                SwigluSrc<CLAMP>::prefetch(a, row, c0 + cc);
+        }
+    }
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t tl = blockIdx.x; tl < ntiles; tl += gridDim.x) {
@@ -112,13 +124,21 @@ __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(Swig
 
 }  // namespace
 
-const void *transpose_kernel_fn(int scale_fmt, bool clamp)
+namespace {
+template <bool PF>
+const void *transpose_pick(int scale_fmt, bool clamp)
 {
     if (scale_fmt == kScaleF32)
-        return clamp ? reinterpret_cast<const void *>(&transpose_quant_kernel<kScaleF32, true>)
-                     : reinterpret_cast<const void *>(&transpose_quant_kernel<kScaleF32, false>);
-    return clamp ? reinterpret_cast<const void *>(&transpose_quant_kernel<kScaleUE8M0, true>)
-                 : reinterpret_cast<const void *>(&transpose_quant_kernel<kScaleUE8M0, false>);
+        return clamp ? reinterpret_cast<const void *>(&transpose_quant_kernel<kScaleF32, true, PF>)
+                     : reinterpret_cast<const void *>(&transpose_quant_kernel<kScaleF32, false, PF>);
+    return clamp ? reinterpret_cast<const void *>(&transpose_quant_kernel<kScaleUE8M0, true, PF>)
+                 : reinterpret_cast<const void *>(&transpose_quant_kernel<kScaleUE8M0, false, PF>);
+}
+}  // namespace
+
+const void *transpose_kernel_fn(int scale_fmt, bool clamp, bool prefetch)
+{
+    return prefetch ? transpose_pick<true>(scale_fmt, clamp) : transpose_pick<false>(scale_fmt, clamp);
 }
 
 int transpose_threads() { return kTransposeThreads; }
