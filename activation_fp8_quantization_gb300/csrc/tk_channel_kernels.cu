@@ -88,7 +88,7 @@ template <> struct AbsMax<false> {
     }
 };
 
-template <class Src, bool BF16>
+template <class Src, bool BF16, bool PREFETCH>
 __global__ void __launch_bounds__(kAmaxThreads, 2) col_amax_kernel(CastArgs a, int64_t T, int64_t slab_rows,
                                                                float *partial)
 {
@@ -100,6 +100,14 @@ __global__ void __launch_bounds__(kAmaxThreads, 2) col_amax_kernel(CastArgs a, i
     const bool col_ok = col0 < a.H;
     const int64_t r0 = (int64_t)blockIdx.y * slab_rows;
     const int64_t r1 = (T - r0) < slab_rows ? T : r0 + slab_rows;
+    // PREFETCH (short slabs, where the first rows' latency is a visible part
+    // of the launch): the warp's first set of rows into L2 before the wait
+    if (PREFETCH && col_ok)
+        for (int u = 0; u < kAmaxUnroll<BF16>; ++u) {
+            const int64_t row = r0 + warp + (int64_t)u * kAmaxWarps;
+            if (row < r1)
+                Src::prefetch(a, row, col0);
+        }
     pdl_wait();
     pdl_launch_dependents();
     AbsMax<BF16> acc;
@@ -529,8 +537,10 @@ ChannelFns channel_fns(int in_dtype, int out_fmt, int scale_fmt, int64_t hidden)
         return f;
     if (scale_fmt != kScaleF32 && scale_fmt != kScaleUE8M0)
         return f;
-    f.amax = in_dtype == 0 ? reinterpret_cast<const void *>(&col_amax_kernel<CastBf16Src, true>)
-                           : reinterpret_cast<const void *>(&col_amax_kernel<CastF32Src, false>);
+    f.amax = in_dtype == 0 ? reinterpret_cast<const void *>(&col_amax_kernel<CastBf16Src, true, false>)
+                           : reinterpret_cast<const void *>(&col_amax_kernel<CastF32Src, false, false>);
+    f.amax_pf = in_dtype == 0 ? reinterpret_cast<const void *>(&col_amax_kernel<CastBf16Src, true, true>)
+                              : reinterpret_cast<const void *>(&col_amax_kernel<CastF32Src, false, true>);
     f.scale = out_fmt == kOutE4M3 ? scale_pick<kOutE4M3>(scale_fmt) : scale_pick<kOutE2M1>(scale_fmt);
     const bool wide = hidden > 8192;   // more than 512 threads per row
     f.quant = in_dtype == 0 ? quant_pick_out<CastBf16Src>(out_fmt, scale_fmt, wide)
@@ -554,7 +564,9 @@ cudaError_t launch_channel(const ChannelFns &f, const ChannelLaunch &L, const Ca
     int64_t T = sh.T, slab_rows = L.slab_rows;
     float *part = partial;
     void *args1[] = {&a_, &T, &slab_rows, &part};
-    cudaError_t e = launch_grid(f.amax, dim3(L.chunks, L.slabs), kAmaxThreads, args1, stream);
+    // short slabs (each warp at most eight row sets): the prefetching form
+    const void *amax = slab_rows <= 8 * 4 * kAmaxWarps ? f.amax_pf : f.amax;
+    cudaError_t e = launch_grid(amax, dim3(L.chunks, L.slabs), kAmaxThreads, args1, stream);
     if (e != cudaSuccess)
         return e;
     const int nparts = L.slabs;   // partial maxima per column

@@ -33,6 +33,7 @@ struct ChannelFns {
     const void *scale;
     const void *quant;
     const void *chunk;   // the quantize pass on the amax pass's grid, scales reduced in its prologue
+    const void *amax_pf;   // the amax pass's form that prefetches its first rows (short slabs)
 };
 // One run's launch shape: the amax pass runs (chunks x slabs) CTAs, each over
 // slab_rows rows of a 512-column chunk; the quantize pass is a persistent
