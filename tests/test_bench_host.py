@@ -36,3 +36,19 @@ def test_family_hash_covers_only_its_sources(tmp_path, monkeypatch):
     assert bench.kernel_source_hash("swiglu_quant") == h
     (csrc / "tk_kernels.cuh").write_text("int changed = 2;\n")          # a shared header
     assert bench.kernel_source_hash("swiglu_quant") != h
+
+
+def test_family_sources_exist_and_cover_every_kernel_file():
+    """Every kernel file belongs to some profile family, and every family's
+    files exist, so a committed profile's hash always names real sources."""
+    import os
+    csrc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "activation_fp8_quantization_gb300", "csrc")
+    listed = set()
+    for fam, files in bench.FAMILY_SOURCES.items():
+        for f in files:
+            assert os.path.exists(os.path.join(csrc, f)), (fam, f)
+            listed.add(f)
+    kernels = {n for n in os.listdir(csrc) if n.endswith("_kernels.cu") and n != "tk_diag_kernels.cu"}
+    assert kernels <= listed, kernels - listed
+    assert set(bench.PROFILE_FAMILY.values()) == set(bench.FAMILY_SOURCES)
