@@ -1324,13 +1324,13 @@ TK_API tk_status tk_quant_cast_run_ws(tk_quant_cast_plan_t plan, int64_t T, cons
 struct tk_moe_reduce_plan_s {
     tk_moe_reduce_desc desc;
     int device;
-    const void *fn;
+    const void *fn, *fn_pf;   // fn_pf: the form that prefetches its first task into L2
     int block, rpc, tpr, max_grid;
     unsigned *fault;
     // bulk kernel (has_bulk: the shape allows it)
     bool has_bulk;
     int forced;   // 0: by alignment, 1: register kernel, 2: bulk kernel where allowed
-    const void *bulk_fn;
+    const void *bulk_fn, *bulk_fn_pf;
     int nchunks, wc, stages, slot_bytes, rb, sb, smem, bulk_grid;
 };
 
@@ -1401,16 +1401,18 @@ ReduceLaunch reduce_launch(const tk_moe_reduce_plan_s *p, int64_t T, const void 
     const bool bulk = p->has_bulk && wanted && aligned(y, 16) && (!fp8 || aligned(y_scale, 16));
     ReduceLaunch L{};
     L.bulk = bulk;
+    // the prefetching forms where a CTA has at most 32 tasks (its first
+    // ones are then a large enough share to be worth sending ahead)
     if (bulk) {
         const int64_t tasks = T * p->nchunks;
-        L.fn = p->bulk_fn;
         L.grid = (int)(tasks < p->bulk_grid ? (tasks > 0 ? tasks : 1) : p->bulk_grid);
+        L.fn = tasks <= 32 * (int64_t)L.grid ? p->bulk_fn_pf : p->bulk_fn;
         L.block = tk::kReduceBulkThreads;
         L.smem = p->smem;
     } else {
         const int64_t ntb = (T + p->rpc - 1) / p->rpc;
-        L.fn = p->fn;
         L.grid = (int)(ntb < p->max_grid ? (ntb > 0 ? ntb : 1) : p->max_grid);
+        L.fn = ntb <= 32 * (int64_t)L.grid ? p->fn_pf : p->fn;
         L.block = p->block;
         L.smem = 0;
     }
@@ -1457,7 +1459,8 @@ TK_API tk_status tk_moe_reduce_plan(const tk_moe_reduce_desc *d, int device, tk_
     tk_moe_reduce_plan_s p{};
     p.desc = *d;
     p.device = device;
-    p.fn = tk::moe_reduce_kernel_fn(d->in_fmt);
+    p.fn = tk::moe_reduce_kernel_fn(d->in_fmt, false);
+    p.fn_pf = tk::moe_reduce_kernel_fn(d->in_fmt, true);
     p.tpr = (int)(d->hidden / tk::kEPT);
     p.rpc = p.tpr >= 256 ? 1 : 256 / p.tpr;
     p.block = ((p.tpr * p.rpc + 31) / 32) * 32;   // <= 512 for hidden <= 8192
@@ -1480,8 +1483,11 @@ TK_API tk_status tk_moe_reduce_plan(const tk_moe_reduce_desc *d, int device, tk_
         return cuda_fail(e, "querying the device");
     p.has_bulk = plan_reduce_bulk(&p, optin);
     if (p.has_bulk) {
-        p.bulk_fn = tk::moe_reduce_bulk_kernel_fn(d->in_fmt);
+        p.bulk_fn = tk::moe_reduce_bulk_kernel_fn(d->in_fmt, false);
+        p.bulk_fn_pf = tk::moe_reduce_bulk_kernel_fn(d->in_fmt, true);
         e = cudaFuncSetAttribute(p.bulk_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(p.bulk_fn_pf, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem);
         int bocc = 0;
         if (e == cudaSuccess)
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bocc, p.bulk_fn, tk::kReduceBulkThreads, p.smem);

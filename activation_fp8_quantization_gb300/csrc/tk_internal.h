@@ -128,8 +128,8 @@ cudaError_t launch_backward(const void *fn, int grid, int block, const BackwardA
 // sets bit 0 of *fault (the bounded waits' failure path, for tests).
 cudaError_t launch_unanswered_wait(unsigned *fault, uint32_t tries, cudaStream_t stream);
 
-const void *moe_reduce_kernel_fn(int in_fmt);
-const void *moe_reduce_bulk_kernel_fn(int in_fmt);
+const void *moe_reduce_kernel_fn(int in_fmt, bool prefetch);
+const void *moe_reduce_bulk_kernel_fn(int in_fmt, bool prefetch);
 cudaError_t launch_moe_reduce(const void *fn, int grid, int block, int smem, const ReduceArgs &a,
                               cudaStream_t stream);
 

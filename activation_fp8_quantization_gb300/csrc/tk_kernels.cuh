@@ -887,6 +887,13 @@ __device__ __forceinline__ uint32_t bf16x2_ne_mask(uint32_t a, uint32_t b)
     asm("set.ne.u32.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
+// lane-wise max(|a|, |b|), its sign bit the xor of a's and b's
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
 
 struct Regs32x2 {
     uint32_t g[8];
@@ -964,23 +971,49 @@ struct SwigluSrc {
         const uint64_t w2n = splat(-r.w);
         if (CLAMP && a.packed_clamp) {
             // The limit is a bf16 value, so clamping the bf16 inputs is exact
-            // and two lanes go per instruction. A lane's clamp is recorded as
-            // one bit (bit i of its half for pair i); popc counts them.
+            // and two lanes go per instruction. Most threads hold no value
+            // beyond the limit: the packed max of the gate values, and of the
+            // up values' magnitudes, shows that for each half (14 instructions
+            // for the thread's 32 inputs), and only a half that has one is
+            // clamped and counted. A lane's clamp is recorded as one bit (bit
+            // i of its half for pair i); popc counts them.
             const uint32_t L2 = a.limit2, nL2 = a.limit2 ^ 0x80008000u;
-            uint32_t mg = 0, mu = 0;
+            uint32_t g[8], u[8];
+            uint32_t gm = r.g[0], um = r.u[0];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const uint32_t bit = 0x00010001u << i;
-                mg |= bf16x2_gt_mask(r.g[i], L2) & bit;
-                const uint32_t gc = bf16x2_min(r.g[i], L2);
-                const uint32_t uc = bf16x2_max(bf16x2_min(r.u[i], L2), nL2);
-                mu |= bf16x2_ne_mask(uc, r.u[i]) & bit;
-                ny[i] = neg_swiglu2(bf16_lo(gc), bf16_hi(gc), bf16_lo(uc), bf16_hi(uc), w2n);
-                amax = fmaxf(amax, fmaxf(fabsf(plo(ny[i])), fabsf(phi(ny[i]))));
+                g[i] = r.g[i];
+                u[i] = r.u[i];
+                if (i) {
+                    gm = bf16x2_max(gm, g[i]);
+                    um = bf16x2_max_abs(um, u[i]);
+                }
             }
-            if (ok) {
-                cnt_g += __popc(mg);
-                cnt_u += __popc(mu);
+            if (bf16x2_gt_mask(gm, L2)) {
+                uint32_t mg = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    mg |= bf16x2_gt_mask(g[i], L2) & (0x00010001u << i);
+                    g[i] = bf16x2_min(g[i], L2);
+                }
+                if (ok)
+                    cnt_g += __popc(mg);
+            }
+            if (bf16x2_gt_mask(um & 0x7FFF7FFFu, L2)) {
+                uint32_t mu = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t uc = bf16x2_max(bf16x2_min(u[i], L2), nL2);
+                    mu |= bf16x2_ne_mask(uc, u[i]) & (0x00010001u << i);
+                    u[i] = uc;
+                }
+                if (ok)
+                    cnt_u += __popc(mu);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                ny[i] = neg_swiglu2(bf16_lo(g[i]), bf16_hi(g[i]), bf16_lo(u[i]), bf16_hi(u[i]), w2n);
+                amax = fmaxf(amax, fmaxf(fabsf(plo(ny[i])), fabsf(phi(ny[i]))));
             }
             return;
         }

@@ -101,7 +101,7 @@ __device__ __forceinline__ uint32_t to_bf16x2(float lo, float hi)
 
 // At most 512 threads per CTA (H <= 8192), which leaves room for four
 // slices in flight per thread without spilling.
-template <int IN>
+template <int IN, bool PREFETCH>
 __global__ void __launch_bounds__(512) moe_reduce_kernel(ReduceArgs a)
 {
     const int tid = threadIdx.x;
@@ -110,6 +110,20 @@ __global__ void __launch_bounds__(512) moe_reduce_kernel(ReduceArgs a)
     const bool slot_ok = slot < a.rpc;
     const int col0 = lr * kEPT;
     const int64_t ntb = (a.T + a.rpc - 1) / a.rpc;
+    // PREFETCH (the plan's choice where a CTA has few token blocks): the
+    // first token block's expert slices into L2 before waiting on the
+    // previous kernel. The positions are read past L1 (.cg), so no stale
+    // line stays behind for the reads after the wait; an address is only a
+    // hint here and is used only when it lies inside y.
+    if (PREFETCH && slot_ok && (int64_t)blockIdx.x * a.rpc + slot < a.T) {
+        const int64_t t = (int64_t)blockIdx.x * a.rpc + slot;
+        for (int k = 0; k < a.K; ++k) {
+            const int32_t p = __ldcg(a.pos + t * a.K + k);
+            if (p >= 0 && p < a.R)
+                prefetch_l2(static_cast<const uint8_t *>(a.y) +
+                            ((int64_t)p * a.H + col0) * (IN == kReduceInBf16 ? 2 : 1));
+        }
+    }
     pdl_wait();
     pdl_launch_dependents();
     for (int64_t tb = blockIdx.x; tb < ntb; tb += gridDim.x) {
@@ -187,7 +201,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // copies and metadata) plus the copied bytes; empty[s] takes one arrival per
 // consumer warp. All consumer warps take every task in turn, so no warp
 // waits more than one phase ahead of a barrier.
-template <int IN>
+template <int IN, bool PREFETCH>
 __global__ void __launch_bounds__(kReduceBulkThreads, 1) moe_reduce_bulk_kernel(ReduceArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -206,6 +220,23 @@ __global__ void __launch_bounds__(kReduceBulkThreads, 1) moe_reduce_bulk_kernel(
             mbar_init(empty + i, kReduceConsumerWarps);
         }
         fence_mbar_init();
+    }
+    // PREFETCH (the plan's choice where a CTA has few tasks): the producer
+    // warp sends the chunks of its first `stages` tasks into L2 before
+    // waiting on the previous kernel (positions read past L1, as above; a
+    // hint only, and only for a position inside y).
+    if (PREFETCH && warp == 0 && lane < a.K) {
+        for (int i = 0; i < S; ++i) {
+            const int64_t task = blockIdx.x + (int64_t)i * gridDim.x;
+            if (task >= ntasks)
+                break;
+            const int64_t t = task / a.nchunks;
+            const int c = (int)(task - t * a.nchunks);
+            const int32_t p = __ldcg(a.pos + t * a.K + lane);
+            if (p >= 0 && p < a.R)
+                bulk_prefetch_l2(static_cast<const uint8_t *>(a.y) + ((int64_t)p * a.H + (int64_t)c * a.wc) * kElt,
+                                 (uint32_t)a.rb);
+        }
     }
     __syncthreads();
     pdl_wait();
@@ -384,21 +415,25 @@ __global__ void __launch_bounds__(kReduceBulkThreads, 1) moe_reduce_bulk_kernel(
 
 }  // namespace
 
-const void *moe_reduce_kernel_fn(int in_fmt)
+const void *moe_reduce_kernel_fn(int in_fmt, bool prefetch)
 {
     if (in_fmt == kReduceInBf16)
-        return reinterpret_cast<const void *>(&moe_reduce_kernel<kReduceInBf16>);
+        return prefetch ? reinterpret_cast<const void *>(&moe_reduce_kernel<kReduceInBf16, true>)
+                        : reinterpret_cast<const void *>(&moe_reduce_kernel<kReduceInBf16, false>);
     if (in_fmt == kReduceInE4M3)
-        return reinterpret_cast<const void *>(&moe_reduce_kernel<kReduceInE4M3>);
+        return prefetch ? reinterpret_cast<const void *>(&moe_reduce_kernel<kReduceInE4M3, true>)
+                        : reinterpret_cast<const void *>(&moe_reduce_kernel<kReduceInE4M3, false>);
     return nullptr;
 }
 
-const void *moe_reduce_bulk_kernel_fn(int in_fmt)
+const void *moe_reduce_bulk_kernel_fn(int in_fmt, bool prefetch)
 {
     if (in_fmt == kReduceInBf16)
-        return reinterpret_cast<const void *>(&moe_reduce_bulk_kernel<kReduceInBf16>);
+        return prefetch ? reinterpret_cast<const void *>(&moe_reduce_bulk_kernel<kReduceInBf16, true>)
+                        : reinterpret_cast<const void *>(&moe_reduce_bulk_kernel<kReduceInBf16, false>);
     if (in_fmt == kReduceInE4M3)
-        return reinterpret_cast<const void *>(&moe_reduce_bulk_kernel<kReduceInE4M3>);
+        return prefetch ? reinterpret_cast<const void *>(&moe_reduce_bulk_kernel<kReduceInE4M3, true>)
+                        : reinterpret_cast<const void *>(&moe_reduce_bulk_kernel<kReduceInE4M3, false>);
     return nullptr;
 }
 
