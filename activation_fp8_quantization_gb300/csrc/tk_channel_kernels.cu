@@ -17,12 +17,13 @@
 //     and the CTA writes one fp32 partial maximum per column: partial[s, col].
 //  2. Either col_chunk_quant_kernel on the same grid: CTA (c, s) reduces the
 //     partials of its own 512 columns into their scales (the slab-0 CTA also
-//     stores them) and encodes its slab of that chunk;
+//     stores them) and encodes its slab of that chunk, last row first, where
+//     the amax pass has left the slab's last rows in L2 (evict_last);
 //     or col_scale_kernel (one CTA per 32 columns reduces the partials into
 //     the scales) followed by col_quant_kernel: the row kernel's mapping (16
 //     columns per thread, H / 16 threads per row, a persistent grid over row
-//     blocks, the next block's loads in flight), each thread holding its 16
-//     column scales. The first saves a launch and suits outputs that L2
+//     blocks from the last one back, the next block's loads in flight), each
+//     thread holding its 16 column scales. The first saves a launch and suits outputs that L2
 //     absorbs; the second writes whole rows in sequence, which large outputs
 //     need. Either way a value costs one correctly rounded quotient
 //     (Markstein's correction, or an exact power-of-two multiply) and its
@@ -88,9 +89,44 @@ template <> struct AbsMax<false> {
     }
 };
 
-template <class Src, bool BF16, bool PREFETCH>
+// 32-byte read-only loads with an L2 eviction priority (EV 1: evict_first,
+// 2: evict_last). Before the chunk quantize pass, the amax pass marks the
+// rows that pass reads first (the end of each slab) evict_last and the rest
+// evict_first, so that what L2 keeps between the passes is what is reread
+// soonest; the chunk pass reads evict_first, which also takes the kept lines
+// back to the lowest priority once they have been used. (Before the row
+// quantize pass, whose input does not fit L2 anyway, plain loads measured
+// faster than any split of the priorities.)
+template <int EV>
+__device__ __forceinline__ void ld_ev_256(const void *p, uint32_t (&r)[8])
+{
+    if (EV == 2)
+        asm("ld.global.nc.L1::no_allocate.L2::evict_last.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+            : "l"(p));
+    else
+        asm("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+            : "l"(p));
+}
+
+template <int EV, class Src>
+__device__ __forceinline__ void load_ev(const CastArgs &a, int64_t row, int col0, typename Src::Regs &r)
+{
+    if constexpr (Src::kRowBytesPerCol == 2) {
+        ld_ev_256<EV>(static_cast<const uint16_t *>(a.x) + row * (int64_t)a.H + col0, r.v);
+    } else {
+        const float *p = static_cast<const float *>(a.x) + row * (int64_t)a.H + col0;
+        uint32_t (&lo)[8] = *reinterpret_cast<uint32_t (*)[8]>(&r.v[0]);
+        uint32_t (&hi)[8] = *reinterpret_cast<uint32_t (*)[8]>(&r.v[8]);
+        ld_ev_256<EV>(p, lo);
+        ld_ev_256<EV>(p + 8, hi);
+    }
+}
+
+template <class Src, bool BF16, bool PREFETCH, bool KEEP>
 __global__ void __launch_bounds__(kAmaxThreads, 2) col_amax_kernel(CastArgs a, int64_t T, int64_t slab_rows,
-                                                               float *partial)
+                                                               float *partial, int64_t keep_slab)
 {
     __shared__ __align__(16) float red[kAmaxWarps][512];
     const int warp = threadIdx.x >> 5;
@@ -121,10 +157,16 @@ __global__ void __launch_bounds__(kAmaxThreads, 2) col_amax_kernel(CastArgs a, i
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t row = r + (int64_t)u * kAmaxWarps;
-            if (col_ok && row < r1)
-                Src::load(a, row, col0, v[u]);
-            else
+            if (col_ok && row < r1) {
+                if (!KEEP)
+                    Src::load(a, row, col0, v[u]);
+                else if (row - r0 >= slab_rows - keep_slab)
+                    load_ev<2, Src>(a, row, col0, v[u]);
+                else
+                    load_ev<1, Src>(a, row, col0, v[u]);
+            } else {
                 Src::zero(v[u]);
+            }
         }
     };
     auto reduce = [&](const typename Src::Regs (&v)[U]) {
@@ -305,7 +347,9 @@ __global__ void __launch_bounds__(MAXT) col_quant_kernel(CastArgs a, OutArgs o, 
     cs.load(o.scales, slot_ok ? col0 : 0);
     typename Src::Regs ra, rb_regs;
     const int64_t step = gridDim.x;
-    auto row_of = [&](int64_t b) { return b * sh.rpc + slot; };
+    // the last row block first: the amax pass read the bottom rows last, so
+    // those are the ones most likely still in L2
+    auto row_of = [&](int64_t b) { return (nrb - 1 - b) * sh.rpc + slot; };
     auto valid = [&](int64_t b) { return slot_ok && b < nrb && row_of(b) < sh.T; };
     auto fetch = [&](int64_t b, typename Src::Regs &r) {
         if (valid(b))
@@ -439,7 +483,7 @@ __global__ void __launch_bounds__(kAmaxThreads, 2) col_chunk_quant_kernel(CastAr
         for (int u = 0; u < U; ++u) {
             const int64_t row = row_of(j, u);
             if (col_ok && row >= r0)
-                Src::load(a, row, col0, v[u]);
+                load_ev<1, Src>(a, row, col0, v[u]);
             else
                 Src::zero(v[u]);
         }
@@ -537,10 +581,14 @@ ChannelFns channel_fns(int in_dtype, int out_fmt, int scale_fmt, int64_t hidden)
         return f;
     if (scale_fmt != kScaleF32 && scale_fmt != kScaleUE8M0)
         return f;
-    f.amax = in_dtype == 0 ? reinterpret_cast<const void *>(&col_amax_kernel<CastBf16Src, true, false>)
-                           : reinterpret_cast<const void *>(&col_amax_kernel<CastF32Src, false, false>);
-    f.amax_pf = in_dtype == 0 ? reinterpret_cast<const void *>(&col_amax_kernel<CastBf16Src, true, true>)
-                              : reinterpret_cast<const void *>(&col_amax_kernel<CastF32Src, false, true>);
+    f.amax = in_dtype == 0 ? reinterpret_cast<const void *>(&col_amax_kernel<CastBf16Src, true, false, false>)
+                           : reinterpret_cast<const void *>(&col_amax_kernel<CastF32Src, false, false, false>);
+    f.amax_pf = in_dtype == 0 ? reinterpret_cast<const void *>(&col_amax_kernel<CastBf16Src, true, true, false>)
+                              : reinterpret_cast<const void *>(&col_amax_kernel<CastF32Src, false, true, false>);
+    f.amax_keep = in_dtype == 0 ? reinterpret_cast<const void *>(&col_amax_kernel<CastBf16Src, true, false, true>)
+                                : reinterpret_cast<const void *>(&col_amax_kernel<CastF32Src, false, false, true>);
+    f.amax_keep_pf = in_dtype == 0 ? reinterpret_cast<const void *>(&col_amax_kernel<CastBf16Src, true, true, true>)
+                                   : reinterpret_cast<const void *>(&col_amax_kernel<CastF32Src, false, true, true>);
     f.scale = out_fmt == kOutE4M3 ? scale_pick<kOutE4M3>(scale_fmt) : scale_pick<kOutE2M1>(scale_fmt);
     const bool wide = hidden > 8192;   // more than 512 threads per row
     f.quant = in_dtype == 0 ? quant_pick_out<CastBf16Src>(out_fmt, scale_fmt, wide)
@@ -563,9 +611,12 @@ cudaError_t launch_channel(const ChannelFns &f, const ChannelLaunch &L, const Ca
     CastArgs a_ = a;
     int64_t T = sh.T, slab_rows = L.slab_rows;
     float *part = partial;
-    void *args1[] = {&a_, &T, &slab_rows, &part};
-    // short slabs (each warp at most eight row sets): the prefetching form
-    const void *amax = slab_rows <= 8 * 4 * kAmaxWarps ? f.amax_pf : f.amax;
+    int64_t keep_slab = L.keep_rows;
+    void *args1[] = {&a_, &T, &slab_rows, &part, &keep_slab};
+    // short slabs (each warp at most eight row sets): the prefetching form;
+    // before the chunk quantize pass, the form that sets L2 priorities
+    const bool pf = slab_rows <= 8 * 4 * kAmaxWarps;
+    const void *amax = L.split ? (pf ? f.amax_pf : f.amax) : (pf ? f.amax_keep_pf : f.amax_keep);
     cudaError_t e = launch_grid(amax, dim3(L.chunks, L.slabs), kAmaxThreads, args1, stream);
     if (e != cudaSuccess)
         return e;

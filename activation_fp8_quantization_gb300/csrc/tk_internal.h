@@ -34,6 +34,7 @@ struct ChannelFns {
     const void *quant;
     const void *chunk;   // the quantize pass on the amax pass's grid, scales reduced in its prologue
     const void *amax_pf;   // the amax pass's form that prefetches its first rows (short slabs)
+    const void *amax_keep, *amax_keep_pf;   // the same two with L2 priorities for the chunk quantize pass
 };
 // One run's launch shape: the amax pass runs (chunks x slabs) CTAs, each over
 // slab_rows rows of a 512-column chunk; the quantize pass is a persistent
@@ -46,6 +47,7 @@ struct ChannelLaunch {
     int quant_grid;
     int quant_block;
     bool split;   // three launches (amax, scale, row quantize) instead of two (amax, chunk quantize)
+    int64_t keep_rows;   // two-launch form: rows at the end of each slab the amax pass loads evict_last
 };
 ChannelFns channel_fns(int in_dtype, int out_fmt, int scale_fmt, int64_t hidden);
 int channel_amax_threads();
