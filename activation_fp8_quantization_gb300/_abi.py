@@ -280,7 +280,8 @@ def tk_quant_cast_run_ws(plan: int, num_tokens: int, x, q, scales, workspace, wo
 
 
 CAST_FORMS = {0: "row_quant_kernel", 1: "col_amax_kernel + col_chunk_quant_kernel",
-              2: "col_amax_kernel + col_scale_kernel + col_quant_kernel"}
+              2: "col_amax_kernel + col_scale_kernel + col_quant_kernel", 3: "block_stream_kernel",
+              4: "warp_stream_kernel"}
 
 
 def tk_quant_cast_launch_info(plan: int, num_tokens: int) -> dict:

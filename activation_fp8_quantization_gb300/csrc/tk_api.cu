@@ -333,6 +333,9 @@ struct Launches {
     bool has_stream;
     bool has_block;
     int64_t block_min;
+    // standalone cast: the block ring runs inputs of block_lo..block_hi bytes
+    // (row_bytes per row), the row kernel all others; block_hi = 0: unused
+    int64_t block_lo, block_hi, row_bytes;
     int forced;   // 0: by size, 1: rows, 2: warp stream, 3: block ring
 };
 
@@ -348,9 +351,23 @@ struct Launches {
 // so about 32 blocks per CTA without the clamp and 16 with it where the row
 // kernel packs two or more rows per CTA, and 8 where it holds one row per CTA
 // (wide rows, which it runs less efficiently). The standalone cast, with a
-// third of the fused op's arithmetic per byte, was faster on the row kernel at
-// every size tried (8192 x 4096 and 16384 x 7168), so its plans never pick the
-// block kernel.
+// third of the fused op's arithmetic per byte, is not issue-bound on the row
+// kernel; the block ring only shortens its start-up, and on long runs its
+// steady rate is lower. Measured on GB300 (bf16 input, us, row kernel /
+// block kernel):
+//   width 4096, fp32 scales: 4096 rows 9.49/10.59, 8192 17.37/16.91,
+//     16384 32.72/31.08, 32768 63.74/59.76, 65536 124.1/127.3 (117.7/134.1)
+//   width 7168, UE8M0: 2048 rows 8.62/8.64, 4096 15.86/14.00, 16384
+//     55.01/51.91, 24576 81.12/84.59, 32768 107.1/115.6, 49152 158.8/175.7
+//   width 2048, fp32 scales: 8192 rows 9.50/10.61, 16384 17.35/16.88
+//   width 4096, 1x32 E2M1: 4096 rows 8.27/8.86, 8192 15.11/13.95, 32768
+//     54.67/50.82
+// and fp32 input, width 4096: 8192 rows 26.00/26.89, 16384 51.96/50.49,
+// 32768 103.9/97.5. So the cast takes the block ring for inputs of 48 to
+// 288 MiB (bf16) or 160 to 640 MiB (fp32), the row kernel otherwise.
+constexpr int64_t kCastBlockLoBf16 = (int64_t)48 << 20, kCastBlockHiBf16 = (int64_t)288 << 20;
+constexpr int64_t kCastBlockLoF32 = (int64_t)160 << 20, kCastBlockHiF32 = (int64_t)640 << 20;
+
 int64_t block_min_per_cta(const Launch &rows, bool clamp)
 {
     if (rows.rpc < 2)
@@ -366,6 +383,10 @@ const Launch &pick(const Launches &Ls, int64_t T)
         return Ls.has_stream ? Ls.stream : Ls.rows;
     if (Ls.forced == 3)
         return Ls.has_block ? Ls.block : Ls.rows;
+    if (Ls.has_block && Ls.block_hi > 0) {
+        const int64_t in = T * Ls.row_bytes;
+        return in >= Ls.block_lo && in <= Ls.block_hi ? Ls.block : Ls.rows;
+    }
     if (!Ls.has_block || Ls.block_min <= 0)
         return Ls.rows;
     const int64_t nblk = (T + Ls.block.rpc - 1) / Ls.block.rpc;
@@ -1204,6 +1225,9 @@ TK_API tk_status tk_quant_cast_plan(const tk_quant_cast_desc *d, int device, tk_
     if (st != TK_OK)
         return st;
     Ls.rows.fn_pf = tk::cast_kernel_fn(d->in_dtype, d->out_fmt, d->scale_fmt, geo.cta_reduce, true);
+    Ls.row_bytes = d->hidden * (bf16 ? 2 : 4);
+    Ls.block_lo = bf16 ? kCastBlockLoBf16 : kCastBlockLoF32;
+    Ls.block_hi = bf16 ? kCastBlockHiBf16 : kCastBlockHiF32;
     auto *p = new (std::nothrow) tk_quant_cast_plan_s{*d, device, Ls, tk::ChannelFns{}, Launch{}, 0, 0};
     if (!p)
         return fail(TK_ERR_INVALID_ARG, "out of host memory");
@@ -1309,6 +1333,9 @@ TK_API tk_status tk_quant_cast_launch_info(tk_quant_cast_plan_t plan, int64_t T,
         const bool split = channel_launch(plan, T > 0 ? T : 1).split;
         n = split ? 3 : 2;
         f = split ? TK_CAST_CHANNEL_SPLIT : TK_CAST_CHANNEL_CHUNK;
+    } else {
+        const Launch &L = pick(plan->Ls, T > 0 ? T : 1);
+        f = L.kind == kBlockStream ? TK_CAST_BLOCK_RING : L.kind == kWarpStream ? TK_CAST_WARP_STREAM : TK_CAST_ROWS;
     }
     if (launches)
         *launches = T == 0 ? 0 : n;

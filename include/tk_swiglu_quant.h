@@ -370,15 +370,20 @@ tk_status tk_quant_cast_run_ws(tk_quant_cast_plan_t plan, int64_t num_tokens, co
                                void *scales, void *workspace, size_t workspace_bytes, void *stream);
 
 /* What a cast run of num_tokens rows enqueues (host only): *launches kernel
- * launches (0 when num_tokens == 0) and *form: TK_CAST_ROWS (one launch; per
- * token or per block), TK_CAST_CHANNEL_CHUNK (per channel: the amax pass,
- * then the quantize pass on the same grid, which reduces its own scales) or
- * TK_CAST_CHANNEL_SPLIT (per channel: the amax pass, the scale kernel, the
- * row quantize pass). Either output pointer may be NULL. */
+ * launches (0 when num_tokens == 0) and *form. Per token or per block, one
+ * launch of the kernel the plan picks for that many rows: TK_CAST_ROWS (the
+ * row-block kernel), TK_CAST_BLOCK_RING (the block-ring kernel, for inputs of
+ * a middle size band) or TK_CAST_WARP_STREAM (the warp-stream kernel, only
+ * when forced). Per channel: TK_CAST_CHANNEL_CHUNK (the amax pass, then the
+ * quantize pass on the same grid, which reduces its own scales) or
+ * TK_CAST_CHANNEL_SPLIT (the amax pass, the scale kernel, the row quantize
+ * pass). Either output pointer may be NULL. */
 typedef enum tk_cast_form {
     TK_CAST_ROWS = 0,
     TK_CAST_CHANNEL_CHUNK = 1,
-    TK_CAST_CHANNEL_SPLIT = 2
+    TK_CAST_CHANNEL_SPLIT = 2,
+    TK_CAST_BLOCK_RING = 3,
+    TK_CAST_WARP_STREAM = 4
 } tk_cast_form;
 tk_status tk_quant_cast_launch_info(tk_quant_cast_plan_t plan, int64_t num_tokens, int *launches, int *form);
 

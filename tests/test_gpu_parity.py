@@ -405,6 +405,32 @@ def test_host_pipe_errors():
 
 # ------------------------------------------- both kernels on the same shapes
 
+def test_cast_plan_picks_the_kernel_by_input_size(monkeypatch):
+    """The per-token / per-block cast runs the block ring for inputs of 48 to
+    288 MiB (bf16) or 160 to 640 MiB (fp32) and the row kernel otherwise;
+    per-token scales at widths a warp group cannot cover have only the row
+    kernel; TK_KERNEL forces one."""
+    op = tk.QuantCast(4096, 128, "fp32", "e4m3", "bf16")
+    assert op.launch_info(1024)["kernels"] == "row_quant_kernel"
+    assert op.launch_info(6143)["kernels"] == "row_quant_kernel"      # just under 48 MiB
+    assert op.launch_info(6144)["kernels"] == "block_stream_kernel"   # 48 MiB
+    assert op.launch_info(8192)["form"] == 3 and op.launch_info(8192)["launches"] == 1
+    assert op.launch_info(36864)["kernels"] == "block_stream_kernel"  # 288 MiB
+    assert op.launch_info(36865)["kernels"] == "row_quant_kernel"
+    assert op.launch_info(65536)["kernels"] == "row_quant_kernel"
+    f32 = tk.QuantCast(4096, 128, "fp32", "e4m3", "fp32")
+    assert f32.launch_info(8192)["form"] == 0 and f32.launch_info(16384)["form"] == 3
+    assert f32.launch_info(65536)["form"] == 0
+    assert tk.QuantCast(4096, 0, "fp32", "e4m3", "bf16").launch_info(16384)["form"] == 0
+    assert tk.QuantCast(1040, 16, "fp32", "e4m3", "bf16").launch_info(1 << 16)["form"] == 0
+    monkeypatch.setenv("TK_KERNEL", "block")
+    assert tk.QuantCast(4096, 128, "fp32", "e4m3", "bf16").launch_info(100)["form"] == 3
+    monkeypatch.setenv("TK_KERNEL", "stream")
+    assert tk.QuantCast(4096, 128, "fp32", "e4m3", "bf16").launch_info(8192)["kernels"] == "warp_stream_kernel"
+    monkeypatch.setenv("TK_KERNEL", "rows")
+    assert tk.QuantCast(4096, 128, "fp32", "e4m3", "bf16").launch_info(8192)["form"] == 0
+
+
 def test_plan_picks_the_kernel_by_batch_size(monkeypatch):
     # The block-ring kernel applies to widths that are multiples of 512 whose
     # scale groups fit in 512 columns, and runs once every resident CTA has
