@@ -9,7 +9,11 @@
 #include <new>
 #include <string>
 
+#include "tk_backward.h"
+#include "tk_channel.h"
 #include "tk_internal.h"
+#include "tk_reduce.h"
+#include "tk_transpose.h"
 #include "tk_swiglu_quant.h"
 
 #define TK_API extern "C" __attribute__((visibility("default")))
@@ -1703,8 +1707,11 @@ TK_API tk_status tk_swiglu_backward_plan(const tk_swiglu_backward_desc *d, int d
     tk_swiglu_backward_plan_s p{};
     p.desc = *d;
     p.device = device;
-    p.fn = tk::backward_kernel_fn(d->use_clamp != 0, d->recompute_quant != 0, d->out_fmt, d->scale_fmt, false);
-    p.fn_pf = tk::backward_kernel_fn(d->use_clamp != 0, d->recompute_quant != 0, d->out_fmt, d->scale_fmt, true);
+    uint32_t limit_bits = 0;
+    memcpy(&limit_bits, &d->clamp_limit, sizeof limit_bits);
+    const int clamp_mode = !d->use_clamp ? 0 : (limit_bits & 0xffffu) == 0 ? 2 : 1;
+    p.fn = tk::backward_kernel_fn(clamp_mode, d->recompute_quant != 0, d->out_fmt, d->scale_fmt, false);
+    p.fn_pf = tk::backward_kernel_fn(clamp_mode, d->recompute_quant != 0, d->out_fmt, d->scale_fmt, true);
     p.tpr = (int)(d->hidden / tk::kEPT);
     p.rpc = p.tpr >= 256 ? 1 : 256 / p.tpr;
     p.block = ((p.tpr * p.rpc + 31) / 32) * 32;   // <= 512 for hidden <= 8192
@@ -1779,6 +1786,9 @@ TK_API tk_status tk_swiglu_backward_run(tk_swiglu_backward_plan_t plan, int64_t 
     a.dw = dw;
     a.limit = d.use_clamp ? d.clamp_limit : 0.0f;
     a.H = (int32_t)d.hidden;
+    uint32_t limit_bits = 0;
+    memcpy(&limit_bits, &a.limit, sizeof limit_bits);
+    a.limit2 = (limit_bits >> 16) * 0x00010001u;
     tk::OutArgs o{static_cast<uint8_t *>(q), scales};
     const int32_t layout = d.recompute_quant ? d.scale_layout : TK_SCALE_ROW_MAJOR;
     const tk::RowShape sh{T, (int32_t)d.hidden, plan->tpr, plan->tpg_log2, plan->rpc, plan->groups, 0, 0,

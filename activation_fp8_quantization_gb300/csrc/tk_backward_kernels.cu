@@ -19,7 +19,7 @@
 // dw's row sum is reduced in a fixed order (xor shuffles within a warp,
 // then the warps of a row in index order through shared memory), so it is
 // deterministic.
-#include "tk_internal.h"
+#include "tk_backward.h"
 
 namespace tk {
 
@@ -32,11 +32,15 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
     return r;
 }
 
+// CLAMP: 0 none; 1 in fp32 (any limit); 2 on the bf16 pairs (a limit that
+// is a bf16 value, so the clamp is exact there): two lanes per instruction,
+// and the lanes past the limit kept as 16-bit masks that zero their bf16
+// gradients at the end (+0, as the fp32 form writes).
 // Registers are capped at 64 (two 512-thread or four 256-thread CTAs per SM):
 // left to itself the compiler gives the clamping, recomputing forms over 100,
 // which halves the CTAs per SM and was measured 25% slower than the few
 // bytes of spills the cap costs.
-template <bool CLAMP, bool RECOMPUTE, int OUT, int SCALE, bool PREFETCH>
+template <int CLAMP, bool RECOMPUTE, int OUT, int SCALE, bool PREFETCH>
 __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a, OutArgs o, RowShape sh)
 {
     __shared__ float red[2][16];   // per-warp partial dw, double-buffered by row block
@@ -89,10 +93,19 @@ __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a,
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float g0 = bf16_lo(gr[i]), g1 = bf16_hi(gr[i]);
-            float u0 = bf16_lo(ur[i]), u1 = bf16_hi(ur[i]);
+            uint32_t gi = gr[i], ui = ur[i], mg = 0u, mu = 0u;
+            if (CLAMP == 2) {
+                const uint32_t gc = bf16x2_min(gi, a.limit2);
+                const uint32_t uc = bf16x2_max(bf16x2_min(ui, a.limit2), a.limit2 ^ 0x80008000u);
+                mg = bf16x2_ne_mask(gc, gi);   // g > L
+                mu = bf16x2_ne_mask(uc, ui);   // |u| > L
+                gi = gc;
+                ui = uc;
+            }
+            float g0 = bf16_lo(gi), g1 = bf16_hi(gi);
+            float u0 = bf16_lo(ui), u1 = bf16_hi(ui);
             bool pg0 = true, pg1 = true, pu0 = true, pu1 = true;
-            if (CLAMP) {
+            if (CLAMP == 1) {
                 pg0 = !(g0 > L);
                 pg1 = !(g1 > L);
                 pu0 = !(fabsf(u0) > L);
@@ -126,12 +139,12 @@ __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a,
             const uint64_t dw_ = mul2(d, w2);
             uint64_t dg = mul2(mul2(dw_, uu), dsilu);
             uint64_t du = mul2(dw_, silu);
-            if (CLAMP) {
+            if (CLAMP == 1) {
                 dg = pk(pg0 ? plo(dg) : 0.0f, pg1 ? phi(dg) : 0.0f);
                 du = pk(pu0 ? plo(du) : 0.0f, pu1 ? phi(du) : 0.0f);
             }
-            og[i] = bf16x2_rn(plo(dg), phi(dg));
-            ou[i] = bf16x2_rn(plo(du), phi(du));
+            og[i] = bf16x2_rn(plo(dg), phi(dg)) & ~mg;
+            ou[i] = bf16x2_rn(plo(du), phi(du)) & ~mu;
             acc = fma2(d, su, acc);
         }
         if (ok) {
@@ -178,7 +191,7 @@ __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a,
     }
 }
 
-template <bool CLAMP, bool PF>
+template <int CLAMP, bool PF>
 const void *pick_recompute(int out_fmt, int scale_fmt)
 {
     if (out_fmt == kOutE4M3)
@@ -190,18 +203,27 @@ const void *pick_recompute(int out_fmt, int scale_fmt)
                : reinterpret_cast<const void *>(&swiglu_backward_kernel<CLAMP, true, kOutE2M1, kScaleUE8M0, PF>);
 }
 
-template <bool PF>
-const void *pick_backward(bool clamp, bool recompute, int out_fmt, int scale_fmt)
+template <int CLAMP, bool PF>
+const void *pick_plain(bool recompute, int out_fmt, int scale_fmt)
 {
     if (!recompute)
-        return clamp ? reinterpret_cast<const void *>(&swiglu_backward_kernel<true, false, kOutE4M3, kScaleF32, PF>)
-                     : reinterpret_cast<const void *>(&swiglu_backward_kernel<false, false, kOutE4M3, kScaleF32, PF>);
-    return clamp ? pick_recompute<true, PF>(out_fmt, scale_fmt) : pick_recompute<false, PF>(out_fmt, scale_fmt);
+        return reinterpret_cast<const void *>(&swiglu_backward_kernel<CLAMP, false, kOutE4M3, kScaleF32, PF>);
+    return pick_recompute<CLAMP, PF>(out_fmt, scale_fmt);
+}
+
+template <bool PF>
+const void *pick_backward(int clamp, bool recompute, int out_fmt, int scale_fmt)
+{
+    if (clamp == 2)
+        return pick_plain<2, PF>(recompute, out_fmt, scale_fmt);
+    if (clamp == 1)
+        return pick_plain<1, PF>(recompute, out_fmt, scale_fmt);
+    return pick_plain<0, PF>(recompute, out_fmt, scale_fmt);
 }
 
 }  // namespace
 
-const void *backward_kernel_fn(bool clamp, bool recompute, int out_fmt, int scale_fmt, bool prefetch)
+const void *backward_kernel_fn(int clamp, bool recompute, int out_fmt, int scale_fmt, bool prefetch)
 {
     return prefetch ? pick_backward<true>(clamp, recompute, out_fmt, scale_fmt)
                     : pick_backward<false>(clamp, recompute, out_fmt, scale_fmt);

@@ -28,7 +28,7 @@
 //     need. Either way a value costs one correctly rounded quotient
 //     (Markstein's correction, or an exact power-of-two multiply) and its
 //     share of a packed conversion.
-#include "tk_internal.h"
+#include "tk_channel.h"
 
 namespace tk {
 

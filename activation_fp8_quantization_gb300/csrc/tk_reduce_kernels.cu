@@ -31,7 +31,7 @@
 //    (E4M3) loads are in flight per thread.
 #include <cuda_fp16.h>
 
-#include "tk_internal.h"
+#include "tk_reduce.h"
 
 namespace tk {
 

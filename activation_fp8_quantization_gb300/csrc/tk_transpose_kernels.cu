@@ -23,7 +23,7 @@
 // full-sector write per thread instead of two half-sector ones. Rows
 // T <= t < ldq of the last tile are written as zero codes; nothing at or past
 // ldq is written.
-#include "tk_internal.h"
+#include "tk_transpose.h"
 
 namespace tk {
 

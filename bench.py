@@ -849,10 +849,10 @@ def _code_only(text: str) -> str:
 FAMILY_SOURCES = {
     "swiglu_quant": ["tk_kernels.cuh", "tk_internal.h", "tk_swiglu_kernels.cu"],
     "quant_cast": ["tk_kernels.cuh", "tk_internal.h", "tk_cast_kernels.cu"],
-    "channel_cast": ["tk_kernels.cuh", "tk_internal.h", "tk_channel_kernels.cu"],
-    "transposed_quant": ["tk_kernels.cuh", "tk_internal.h", "tk_transpose_kernels.cu"],
-    "moe_reduce": ["tk_kernels.cuh", "tk_internal.h", "tk_reduce_kernels.cu"],
-    "swiglu_backward": ["tk_kernels.cuh", "tk_internal.h", "tk_backward_kernels.cu"],
+    "channel_cast": ["tk_kernels.cuh", "tk_internal.h", "tk_channel.h", "tk_channel_kernels.cu"],
+    "transposed_quant": ["tk_kernels.cuh", "tk_internal.h", "tk_transpose.h", "tk_transpose_kernels.cu"],
+    "moe_reduce": ["tk_kernels.cuh", "tk_internal.h", "tk_reduce.h", "tk_reduce_kernels.cu"],
+    "swiglu_backward": ["tk_kernels.cuh", "tk_internal.h", "tk_backward.h", "tk_backward_kernels.cu"],
 }
 
 

@@ -98,7 +98,7 @@ def test_backward_small_parity(name):
     print(name, rows, "rows: dx identical %.6f" % same)
 
 
-@pytest.mark.parametrize("clamp", [None, 1.5])
+@pytest.mark.parametrize("clamp", [None, 1.5, 1.3])   # 1.5 is a bf16 value (bf16-pair clamp), 1.3 is not (fp32)
 @pytest.mark.parametrize("weights", [True, False])
 @pytest.mark.parametrize("H", [16, 32, 64, 128, 256, 512, 1536, 3072, 7168, 8192])
 def test_backward_shapes(H, weights, clamp):

@@ -175,6 +175,42 @@ def _bf16(a):
     return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
 
 
+def _bf16_neighbours(v):
+    """The bf16 values just below, at (if representable) and just above v."""
+    b = torch.tensor([v], dtype=torch.float32).to(torch.bfloat16).view(torch.int16).item() & 0xFFFF
+    near = sorted({(b - 1) & 0xFFFF, b, (b + 1) & 0xFFFF})
+    return torch.tensor(near, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).float().tolist()
+
+
+@pytest.mark.parametrize("kernel", ["rows", "stream", "block"])
+@pytest.mark.parametrize("limit", [3.0, 2.7182817, 0.1])
+@pytest.mark.parametrize("H,group,scale_fmt,out_fmt", [(2048, 128, "ue8m0", "e4m3"), (512, 32, "ue8m0", "e2m1"),
+                                                       (1024, 0, "fp32", "e4m3")])
+def test_clamp_limits_bf16_and_not(H, group, scale_fmt, out_fmt, limit, kernel, monkeypatch):
+    """A limit that is a bf16 value is applied on the bf16 pairs, any other in
+    fp32; both give the oracle's codes, scales and counts. Values at the
+    limit's bf16 neighbours, at +-limit and past it in both halves, and rows
+    with no value near the limit (the test that skips clamping)."""
+    monkeypatch.setenv("TK_KERNEL", kernel)
+    rng = np.random.default_rng(int(limit * 1000) + H + group)
+    T = 67
+    v = rng.standard_normal((T, 2 * H)).astype(np.float32) * 0.5 * limit
+    near = _bf16_neighbours(limit)
+    cand = np.array(near + [-x for x in near] + [4 * limit, -4 * limit, limit, -limit], np.float32)
+    for r in range(0, T, 3):   # every third row holds planted values in both halves
+        cols = rng.choice(2 * H, size=24, replace=False)
+        v[r, cols] = rng.choice(cand, size=24)
+    x = _bf16(v)
+    w = torch.from_numpy(rng.uniform(0.0, 1.0, T).astype(np.float32))
+    op = tk.SwigluQuant(H, group, scale_fmt, out_fmt, True, limit, True)
+    counts = torch.zeros(2, dtype=torch.int64, device="cuda")
+    q, s = _run(op, x.cuda(), w.cuda(), counts)
+    ref = oracle.swiglu_quant(wls.bf16_bits(x), w.numpy(), group, scale_fmt, out_fmt, clamp=limit, want_y=True)
+    compare(q.cpu().numpy(), s.cpu().numpy(), ref, group, scale_fmt, out_fmt).check((H, group, limit))
+    assert counts.cpu().tolist() == ref["counts"].tolist()
+    assert min(ref["counts"].tolist()) > 0
+
+
 @pytest.mark.parametrize("kernel", ["rows", "stream", "block"])
 def test_special_rows(kernel, monkeypatch):
     monkeypatch.setenv("TK_KERNEL", kernel)
