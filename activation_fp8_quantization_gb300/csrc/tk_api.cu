@@ -521,7 +521,10 @@ struct tk_swiglu_quant_plan_s {
     // its form that prefetches its first tile (runs with few tiles per CTA)
     const void *tfn;
     const void *tfn_pf;
+    const void *tfn_pf2;   // prefetches each next tile too (few tiles per CTA)
     int tgrid;
+    int tgrid2;   // resident CTAs of tfn_pf2
+    int tpf;      // TK_TRANSPOSE_PF=0|1|2 when the plan was made (forces a form), else -1
 };
 
 struct tk_quant_cast_plan_s {
@@ -578,21 +581,29 @@ TK_API tk_status tk_swiglu_quant_plan(const tk_swiglu_quant_desc *d, int device,
     Ls.rows.fn_pf = tk::swiglu_kernel_fn(d->out_fmt, d->scale_fmt, clamp, geo.cta_reduce, true);
     // The transposed-codes kernel: E4M3, groups of 32, 64 or 128 columns
     // inside its 128-column tiles.
-    const void *tfn = nullptr, *tfn_pf = nullptr;
-    int tgrid = 0;
+    const void *tfn = nullptr, *tfn_pf = nullptr, *tfn_pf2 = nullptr;
+    int tgrid = 0, tgrid2 = 0;
     if (d->out_fmt == TK_OUT_E4M3 && d->hidden % 128 == 0 &&
         (d->group_size == 32 || d->group_size == 64 || d->group_size == 128)) {
-        tfn = tk::transpose_kernel_fn(d->scale_fmt, clamp, false);
-        tfn_pf = tk::transpose_kernel_fn(d->scale_fmt, clamp, true);
+        tfn = tk::transpose_kernel_fn(d->scale_fmt, clamp, 0);
+        tfn_pf = tk::transpose_kernel_fn(d->scale_fmt, clamp, 1);
+        tfn_pf2 = tk::transpose_kernel_fn(d->scale_fmt, clamp, 2);
         int occ = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, tfn, tk::transpose_threads(), 0);
         if (e != cudaSuccess)
             return cuda_fail(e, "occupancy of the transposed kernel");
         tgrid = occ * Ls.rows.num_sms;
-        if (tgrid < 1)
+        int occ2 = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, tfn_pf2, tk::transpose_threads(), 0);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "occupancy of the transposed kernel");
+        tgrid2 = occ2 * Ls.rows.num_sms;
+        if (tgrid < 1 || tgrid2 < 1)
             tfn = nullptr;
     }
-    auto *p = new (std::nothrow) tk_swiglu_quant_plan_s{*d, device, Ls, tfn, tfn_pf, tgrid};
+    const int tpf = env_int("TK_TRANSPOSE_PF", -1);
+    auto *p = new (std::nothrow) tk_swiglu_quant_plan_s{*d, device, Ls, tfn, tfn_pf, tfn_pf2, tgrid, tgrid2,
+                                                        tpf >= 0 && tpf <= 2 ? tpf : -1};
     if (!p)
         return fail(TK_ERR_INVALID_ARG, "out of host memory");
     *plan = p;
@@ -780,8 +791,23 @@ TK_API tk_status tk_swiglu_quant_run_transposed(tk_swiglu_quant_plan_t plan, int
     sh.groups = (int32_t)(d.hidden / d.group_size);
     const int64_t ldq = (T + 31) / 32 * 32;
     const int64_t tiles = (T + 31) / 32 * (d.hidden / 128);
-    const int grid = (int)(tiles < plan->tgrid ? tiles : plan->tgrid);
-    const void *fn = tiles <= 32 * (int64_t)grid ? plan->tfn_pf : plan->tfn;
+    // Prefetching forms: without the clamp the first tile and each next one
+    // always; with it the same at up to 8 tiles per CTA, the first tile only
+    // at up to 32, none beyond. Measured on GB300 (µs; none / first tile only
+    // / each next tile too): 8192 rows of width 2048 17.80/17.37/15.89,
+    // 100003 rows of width 3072 (70 tiles per CTA) 264.6/264.5/262.3, 32768
+    // rows of width 2048 with the clamp and outliers (15 tiles per CTA)
+    // -/60.62/62.29; over 2048 to 32768 rows at widths 2048 and 3072 the
+    // next-tile form was never slower without the clamp, and with it faster
+    // up to 16384 rows (8 tiles per CTA).
+    const int mode = plan->tpf >= 0                              ? plan->tpf
+                     : !d.use_clamp                              ? 2
+                     : tiles <= 8 * (int64_t)plan->tgrid2        ? 2
+                     : tiles <= 32 * (int64_t)plan->tgrid        ? 1
+                                                                 : 0;
+    const int gmax = mode == 2 ? plan->tgrid2 : plan->tgrid;
+    const int grid = (int)(tiles < gmax ? tiles : gmax);
+    const void *fn = mode == 2 ? plan->tfn_pf2 : mode == 1 ? plan->tfn_pf : plan->tfn;
     cudaError_t e = tk::launch_transpose(fn, grid, a, o, sh, ldq, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the transposed kernel");

@@ -6,7 +6,8 @@
 namespace tk {
 
 // Fused op with the codes written transposed (E4M3, groups of 32/64/128).
-const void *transpose_kernel_fn(int scale_fmt, bool clamp, bool prefetch);
+// prefetch: 0 none, 1 the first tile, 2 the first and then each next tile
+const void *transpose_kernel_fn(int scale_fmt, bool clamp, int prefetch);
 int transpose_threads();
 cudaError_t launch_transpose(const void *fn, int grid, const SwigluArgs &a, const OutArgs &o, const RowShape &sh,
                              int64_t ldq, cudaStream_t stream);

@@ -35,7 +35,9 @@ constexpr int kTileStride = 144;   // bytes per shared row: 16-byte aligned, con
 constexpr int kTransposeThreads = 128;
 constexpr int kPassRows = kTransposeThreads / 8;
 
-template <int SCALE, bool CLAMP, bool PREFETCH>
+// PREFETCH: 0 none; 1 the first tile's rows into L2 before the dependency
+// wait; 2 that and, at each tile, the CTA's next tile's rows.
+template <int SCALE, bool CLAMP, int PREFETCH>
 __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(SwigluArgs a, OutArgs o, RowShape sh,
                                                                               int64_t ldq)
 {
@@ -52,9 +54,9 @@ __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(Swig
     // uniform: every qT row starts 32-byte aligned, so each thread's 32 rows
     // of one column go out as one sector-sized store
     const bool wide = (ldq & 31) == 0 && aligned32(o.q);
-    // PREFETCH (the plan's choice where a CTA has few tiles): the first
+    // PREFETCH >= 1 (the plan's choice where a CTA has few tiles): the first
     // tile's rows into L2 before waiting on the previous kernel
-    if (PREFETCH && (int64_t)blockIdx.x < ntiles) {
+    if (PREFETCH >= 1 && (int64_t)blockIdx.x < ntiles) {
         const int64_t tb = blockIdx.x / ncb;
         const int c0 = (int)(blockIdx.x - tb * ncb) * kTileCols;
 #pragma unroll
@@ -78,6 +80,19 @@ __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(Swig
                 SwigluSrc<CLAMP>::load(a, row, c0 + cc, regs[p]);
             else
                 SwigluSrc<CLAMP>::zero(regs[p]);
+        }
+        if (PREFETCH == 2) {   // the CTA's next tile into L2 while this one is worked on
+            const int64_t tn = tl + gridDim.x;
+            if (tn < ntiles) {
+                const int64_t tbn = tn / ncb;
+                const int c0n = (int)(tn - tbn * ncb) * kTileCols;
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int64_t row = tbn * kTileRows + p * kPassRows + rr;
+                    if (row < sh.T)
+                        SwigluSrc<CLAMP>::prefetch(a, row, c0n + cc);
+                }
+            }
         }
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
@@ -125,7 +140,7 @@ __global__ void __launch_bounds__(kTransposeThreads) transpose_quant_kernel(Swig
 }  // namespace
 
 namespace {
-template <bool PF>
+template <int PF>
 const void *transpose_pick(int scale_fmt, bool clamp)
 {
     if (scale_fmt == kScaleF32)
@@ -136,9 +151,11 @@ const void *transpose_pick(int scale_fmt, bool clamp)
 }
 }  // namespace
 
-const void *transpose_kernel_fn(int scale_fmt, bool clamp, bool prefetch)
+const void *transpose_kernel_fn(int scale_fmt, bool clamp, int prefetch)
 {
-    return prefetch ? transpose_pick<true>(scale_fmt, clamp) : transpose_pick<false>(scale_fmt, clamp);
+    if (prefetch == 2)
+        return transpose_pick<2>(scale_fmt, clamp);
+    return prefetch == 1 ? transpose_pick<1>(scale_fmt, clamp) : transpose_pick<0>(scale_fmt, clamp);
 }
 
 int transpose_threads() { return kTransposeThreads; }
