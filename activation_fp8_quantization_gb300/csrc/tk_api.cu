@@ -1676,6 +1676,8 @@ struct tk_swiglu_backward_plan_s {
     int device;
     const void *fn;
     const void *fn_pf;   // the form that prefetches its first row block (runs with few row blocks per CTA)
+    const void *fn_pf2;  // the form that also prefetches each next row block
+    int pf_forced;       // TK_BACKWARD_PF=0|1|2 when the plan was made, else -1
     int block, tpr, rpc, tpg_log2, groups, max_grid;
     unsigned *fault;
 };
@@ -1736,8 +1738,13 @@ TK_API tk_status tk_swiglu_backward_plan(const tk_swiglu_backward_desc *d, int d
     uint32_t limit_bits = 0;
     memcpy(&limit_bits, &d->clamp_limit, sizeof limit_bits);
     const int clamp_mode = !d->use_clamp ? 0 : (limit_bits & 0xffffu) == 0 ? 2 : 1;
-    p.fn = tk::backward_kernel_fn(clamp_mode, d->recompute_quant != 0, d->out_fmt, d->scale_fmt, false);
-    p.fn_pf = tk::backward_kernel_fn(clamp_mode, d->recompute_quant != 0, d->out_fmt, d->scale_fmt, true);
+    p.fn = tk::backward_kernel_fn(clamp_mode, d->recompute_quant != 0, d->out_fmt, d->scale_fmt, 0);
+    p.fn_pf = tk::backward_kernel_fn(clamp_mode, d->recompute_quant != 0, d->out_fmt, d->scale_fmt, 1);
+    p.fn_pf2 = tk::backward_kernel_fn(clamp_mode, d->recompute_quant != 0, d->out_fmt, d->scale_fmt, 2);
+    {
+        const int f = env_int("TK_BACKWARD_PF", -1);
+        p.pf_forced = f >= 0 && f <= 2 ? f : -1;
+    }
     p.tpr = (int)(d->hidden / tk::kEPT);
     p.rpc = p.tpr >= 256 ? 1 : 256 / p.tpr;
     p.block = ((p.tpr * p.rpc + 31) / 32) * 32;   // <= 512 for hidden <= 8192
@@ -1821,7 +1828,17 @@ TK_API tk_status tk_swiglu_backward_run(tk_swiglu_backward_plan_t plan, int64_t 
                           plan->fault, layout, scale_ld(layout, d.scale_fmt, T)};
     const int64_t nrb = (T + plan->rpc - 1) / plan->rpc;
     const int grid = (int)(nrb < plan->max_grid ? nrb : plan->max_grid);
-    const void *fn = nrb <= 32 * (int64_t)grid ? plan->fn_pf : plan->fn;
+    // Prefetching forms by row blocks per CTA: the first block and each next
+    // one at up to 8, the first only at up to 32. Measured on GB300 at width
+    // 2048 (µs, first block only / each next block too): 8192 rows (6.7
+    // blocks per CTA) 30.15/28.68 without the clamp, 32.22/30.80 with it;
+    // 32768 rows (27 per CTA) 110.97/129.30 and 110.88/128.91 (UE8M0, clamp):
+    // with many blocks per CTA the extra prefetches cost more than they hide.
+    const int mode = plan->pf_forced >= 0        ? plan->pf_forced
+                     : nrb <= 8 * (int64_t)grid  ? 2
+                     : nrb <= 32 * (int64_t)grid ? 1
+                                                 : 0;
+    const void *fn = mode == 2 ? plan->fn_pf2 : mode == 1 ? plan->fn_pf : plan->fn;
     cudaError_t e = tk::launch_backward(fn, grid, plan->block, a, o, sh, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, "launch of the backward kernel");

@@ -17,7 +17,8 @@ struct BackwardArgs {
     uint32_t limit2;      // the limit as bf16 in both halves (clamp on bf16 pairs)
 };
 // clamp: 0 none, 1 in fp32 (any limit), 2 on bf16 pairs (a limit that is a bf16 value)
-const void *backward_kernel_fn(int clamp, bool recompute, int out_fmt, int scale_fmt, bool prefetch);
+// prefetch: 0 none, 1 the first row block, 2 the first and then each next one
+const void *backward_kernel_fn(int clamp, bool recompute, int out_fmt, int scale_fmt, int prefetch);
 cudaError_t launch_backward(const void *fn, int grid, int block, const BackwardArgs &a, const OutArgs &o,
                             const RowShape &sh, cudaStream_t stream);
 

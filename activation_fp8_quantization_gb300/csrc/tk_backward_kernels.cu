@@ -40,7 +40,7 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
 // left to itself the compiler gives the clamping, recomputing forms over 100,
 // which halves the CTAs per SM and was measured 25% slower than the few
 // bytes of spills the cap costs.
-template <int CLAMP, bool RECOMPUTE, int OUT, int SCALE, bool PREFETCH>
+template <int CLAMP, bool RECOMPUTE, int OUT, int SCALE, int PREFETCH>
 __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a, OutArgs o, RowShape sh)
 {
     __shared__ float red[2][16];   // per-warp partial dw, double-buffered by row block
@@ -58,9 +58,9 @@ __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a,
     const float L = a.limit;
     constexpr float kNegHalfLog2e = -0.72134752044448170368f;  // -log2(e) / 2
     const bool wide = aligned32(a.dx);   // uniform: a row's halves stay 32-byte aligned (H % 16 == 0)
-    // PREFETCH (the plan's choice where a CTA has few row blocks): the first
+    // PREFETCH >= 1 (the plan's choice where a CTA has few row blocks): the first
     // row block's x and dy into L2 before waiting on the previous kernel
-    if (PREFETCH && slot_ok && (int64_t)blockIdx.x < nrb && (int64_t)blockIdx.x * sh.rpc + slot < sh.T) {
+    if (PREFETCH >= 1 && slot_ok && (int64_t)blockIdx.x < nrb && (int64_t)blockIdx.x * sh.rpc + slot < sh.T) {
         const int64_t row = (int64_t)blockIdx.x * sh.rpc + slot;
         prefetch_l2(a.x + row * (2 * (int64_t)a.H) + col0);
         prefetch_l2(a.x + row * (2 * (int64_t)a.H) + a.H + col0);
@@ -80,6 +80,14 @@ __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a,
             ld_stream_256(a.dy + row * (int64_t)a.H + col0, dr);
             if (a.w)
                 w = __ldg(a.w + row);
+            // PREFETCH == 2: the CTA's next row block into L2 while this one
+            // is worked on
+            const int64_t nrow = row + (int64_t)gridDim.x * sh.rpc;
+            if (PREFETCH == 2 && nrow < sh.T) {
+                prefetch_l2(xr + (int64_t)gridDim.x * sh.rpc * (2 * (int64_t)a.H));
+                prefetch_l2(xr + (int64_t)gridDim.x * sh.rpc * (2 * (int64_t)a.H) + a.H);
+                prefetch_l2(a.dy + nrow * (int64_t)a.H + col0);
+            }
         } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -191,7 +199,7 @@ __global__ void __launch_bounds__(512, 2) swiglu_backward_kernel(BackwardArgs a,
     }
 }
 
-template <int CLAMP, bool PF>
+template <int CLAMP, int PF>
 const void *pick_recompute(int out_fmt, int scale_fmt)
 {
     if (out_fmt == kOutE4M3)
@@ -203,7 +211,7 @@ const void *pick_recompute(int out_fmt, int scale_fmt)
                : reinterpret_cast<const void *>(&swiglu_backward_kernel<CLAMP, true, kOutE2M1, kScaleUE8M0, PF>);
 }
 
-template <int CLAMP, bool PF>
+template <int CLAMP, int PF>
 const void *pick_plain(bool recompute, int out_fmt, int scale_fmt)
 {
     if (!recompute)
@@ -211,7 +219,7 @@ const void *pick_plain(bool recompute, int out_fmt, int scale_fmt)
     return pick_recompute<CLAMP, PF>(out_fmt, scale_fmt);
 }
 
-template <bool PF>
+template <int PF>
 const void *pick_backward(int clamp, bool recompute, int out_fmt, int scale_fmt)
 {
     if (clamp == 2)
@@ -223,10 +231,12 @@ const void *pick_backward(int clamp, bool recompute, int out_fmt, int scale_fmt)
 
 }  // namespace
 
-const void *backward_kernel_fn(int clamp, bool recompute, int out_fmt, int scale_fmt, bool prefetch)
+const void *backward_kernel_fn(int clamp, bool recompute, int out_fmt, int scale_fmt, int prefetch)
 {
-    return prefetch ? pick_backward<true>(clamp, recompute, out_fmt, scale_fmt)
-                    : pick_backward<false>(clamp, recompute, out_fmt, scale_fmt);
+    if (prefetch == 2)
+        return pick_backward<2>(clamp, recompute, out_fmt, scale_fmt);
+    return prefetch == 1 ? pick_backward<1>(clamp, recompute, out_fmt, scale_fmt)
+                         : pick_backward<0>(clamp, recompute, out_fmt, scale_fmt);
 }
 
 cudaError_t launch_backward(const void *fn, int grid, int block, const BackwardArgs &a, const OutArgs &o,
