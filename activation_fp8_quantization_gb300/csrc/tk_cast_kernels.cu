@@ -5,14 +5,16 @@ namespace tk {
 
 namespace {
 template <class Src, int OUT, int SCALE, bool CTA>
-const void *fn(bool pf)
+const void *fn(int pf)
 {
-    return pf ? reinterpret_cast<const void *>(&row_quant_kernel<Src, OUT, SCALE, CTA, true>)
-              : reinterpret_cast<const void *>(&row_quant_kernel<Src, OUT, SCALE, CTA, false>);
+    if (pf == 2)
+        return reinterpret_cast<const void *>(&row_quant_kernel<Src, OUT, SCALE, CTA, 2>);
+    return pf == 1 ? reinterpret_cast<const void *>(&row_quant_kernel<Src, OUT, SCALE, CTA, 1>)
+                   : reinterpret_cast<const void *>(&row_quant_kernel<Src, OUT, SCALE, CTA, 0>);
 }
 
 template <class Src, int OUT>
-const void *pick(int scale_fmt, bool cta, bool pf)
+const void *pick(int scale_fmt, bool cta, int pf)
 {
     if (scale_fmt == kScaleF32)
         return cta ? fn<Src, OUT, kScaleF32, true>(pf) : fn<Src, OUT, kScaleF32, false>(pf);
@@ -20,7 +22,7 @@ const void *pick(int scale_fmt, bool cta, bool pf)
 }
 
 template <class Src>
-const void *pick_out(int out_fmt, int scale_fmt, bool cta, bool pf)
+const void *pick_out(int out_fmt, int scale_fmt, bool cta, int pf)
 {
     if (out_fmt == kOutE4M3)
         return pick<Src, kOutE4M3>(scale_fmt, cta, pf);
@@ -70,7 +72,7 @@ const void *cast_stream_fn(int in_dtype, int out_fmt, int scale_fmt)
     return nullptr;
 }
 
-const void *cast_kernel_fn(int in_dtype, int out_fmt, int scale_fmt, bool cta_reduce, bool prefetch)
+const void *cast_kernel_fn(int in_dtype, int out_fmt, int scale_fmt, bool cta_reduce, int prefetch)
 {
     if (in_dtype == 0)
         return pick_out<CastBf16Src>(out_fmt, scale_fmt, cta_reduce, prefetch);

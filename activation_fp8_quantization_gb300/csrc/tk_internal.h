@@ -8,19 +8,20 @@
 
 namespace tk {
 
-// Entry of the fused op's row-block kernel (any width; `prefetch`: the form
+// Entry of the fused op's row-block kernel (any width; `prefetch` 1: the form
 // that brings its first row block into L2 before waiting on the previous
-// kernel), of its warp-stream kernel or of its block-ring kernel (widths a
-// multiple of 512) for a format / scale / clamp combination; nullptr if there
-// is none.
-const void *swiglu_kernel_fn(int out_fmt, int scale_fmt, bool clamp, bool cta_reduce, bool prefetch);
+// kernel; 2 is not built for the fused op), of its warp-stream kernel or of
+// its block-ring kernel (widths a multiple of 512) for a format / scale /
+// clamp combination; nullptr if there is none.
+const void *swiglu_kernel_fn(int out_fmt, int scale_fmt, bool clamp, bool cta_reduce, int prefetch);
 const void *swiglu_stream_fn(int out_fmt, int scale_fmt, bool clamp);
 const void *swiglu_block_fn(int out_fmt, int scale_fmt, bool clamp);   // block_stream_kernel
 cudaError_t launch_swiglu(const void *fn, int grid, int block, size_t smem, const SwigluArgs &a,
                           const OutArgs &o, const RowShape &sh, cudaStream_t stream);
 
-// Same for the standalone cast (in_dtype: 0 bf16, 1 fp32).
-const void *cast_kernel_fn(int in_dtype, int out_fmt, int scale_fmt, bool cta_reduce, bool prefetch);
+// Same for the standalone cast (in_dtype: 0 bf16, 1 fp32); its row kernel
+// also has `prefetch` 2: the first row block and each next one into L2.
+const void *cast_kernel_fn(int in_dtype, int out_fmt, int scale_fmt, bool cta_reduce, int prefetch);
 const void *cast_stream_fn(int in_dtype, int out_fmt, int scale_fmt);
 const void *cast_block_fn(int in_dtype, int out_fmt, int scale_fmt);
 cudaError_t launch_cast(const void *fn, int grid, int block, size_t smem, const CastArgs &a,

@@ -498,7 +498,9 @@ __device__ __forceinline__ void quantize_store(const uint64_t (&ny)[kEPT / 2], f
 // General form: any H that is a multiple of 16, any group size, and one scale
 // per row with a CTA-wide reduction. Each thread keeps the next row block's
 // loads (64 bytes) in flight while it computes the current one.
-template <class Src, int OUT, int SCALE, bool CTA_REDUCE, bool PREFETCH = false>
+// PREFETCH: 0 none; 1 the first row block into L2 before the dependency
+// wait; 2 that and, with each block's loads, the block after it into L2.
+template <class Src, int OUT, int SCALE, bool CTA_REDUCE, int PREFETCH = 0>
 __global__ void __launch_bounds__(kMaxThreads)
 row_quant_kernel(typename Src::Args a, OutArgs o, RowShape sh)
 {
@@ -517,7 +519,7 @@ row_quant_kernel(typename Src::Args a, OutArgs o, RowShape sh)
     // PREFETCH (the plan's choice where a CTA has few row blocks, so that the
     // first one's latency is a visible part of the launch): bring the first
     // row block into L2 before waiting on the previous kernel.
-    if (PREFETCH && slot_ok && (int64_t)blockIdx.x < nrb && (int64_t)blockIdx.x * sh.rpc + slot < sh.T)
+    if (PREFETCH >= 1 && slot_ok && (int64_t)blockIdx.x < nrb && (int64_t)blockIdx.x * sh.rpc + slot < sh.T)
         Src::prefetch(a, (int64_t)blockIdx.x * sh.rpc + slot, col0);
     pdl_wait();
     pdl_launch_dependents();
@@ -532,6 +534,8 @@ row_quant_kernel(typename Src::Args a, OutArgs o, RowShape sh)
             Src::load(a, row_of(b), col0, r);
         else
             Src::zero(r);
+        if (PREFETCH == 2 && valid(b + step))
+            Src::prefetch(a, row_of(b + step), col0);
     };
     int it = 0;
     auto compute = [&](int64_t b, const typename Src::Regs &r) {
