@@ -185,3 +185,32 @@ def test_unanswered_wait_rejects_tries_out_of_range():
         with pytest.raises(tk.TkError) as e:
             tk.tk_diag_unanswered_wait(0, tries, None)
         assert e.value.status == 1
+
+
+def _enum_values(name):
+    """{constant: value} of `typedef enum <name> {...}` in the header."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef enum %s \{(.*?)\}" % name, text, flags=re.S).group(1)
+    return {k: int(v) for k, v in re.findall(r"\b(TK_[A-Z0-9_]+)\s*=\s*(\d+)", body)}
+
+
+def test_binding_tables_match_the_header_enums():
+    """The Python binding's name tables carry the header's enum values, so a
+    value added or renumbered on one side only fails here."""
+    assert {v: k for k, v in _abi.STATUS_NAMES.items()} == _enum_values("tk_status")
+    assert _enum_values("tk_scale_fmt") == {"TK_SCALE_" + k.upper(): v for k, v in _abi.SCALE_FMTS.items()}
+    assert _enum_values("tk_out_fmt") == {"TK_OUT_" + k.upper(): v for k, v in _abi.OUT_FMTS.items()}
+    assert _enum_values("tk_in_dtype") == {"TK_IN_" + k.upper(): v for k, v in _abi.IN_DTYPES.items()}
+    assert sorted(_enum_values("tk_scale_layout").values()) == sorted(_abi.SCALE_LAYOUTS.values())
+    assert sorted(_enum_values("tk_granularity").values()) == sorted(_abi.GRANULARITIES.values())
+    assert sorted(_enum_values("tk_reduce_in_fmt").values()) == sorted(_abi.REDUCE_IN_FMTS.values())
+    kinds = _enum_values("tk_kernel_kind")
+    assert sorted(kinds.values()) == sorted(_abi.KERNEL_NAMES)
+    assert kinds["TK_KERNEL_BLOCK_RING"] == 2 and _abi.KERNEL_NAMES[2] == "block_stream_kernel"
+    forms = _enum_values("tk_cast_form")
+    assert sorted(forms.values()) == sorted(_abi.CAST_FORMS)
+    assert _abi.CAST_FORMS[forms["TK_CAST_ROWS"]] == "row_quant_kernel"
+    assert _abi.CAST_FORMS[forms["TK_CAST_BLOCK_RING"]] == "block_stream_kernel"
+    assert _abi.CAST_FORMS[forms["TK_CAST_WARP_STREAM"]] == "warp_stream_kernel"
+    assert "col_chunk_quant_kernel" in _abi.CAST_FORMS[forms["TK_CAST_CHANNEL_CHUNK"]]
+    assert "col_scale_kernel" in _abi.CAST_FORMS[forms["TK_CAST_CHANNEL_SPLIT"]]
