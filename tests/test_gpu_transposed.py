@@ -89,14 +89,22 @@ def test_transposed_clamp_counters():
     assert c1.cpu().tolist() == ref["counts"].tolist() == c0.cpu().tolist()
 
 
-def test_transposed_full_bench_workload():
-    """The benchmark workload at full size: equal to the row-major kernel's output."""
-    wl = wls.WORKLOADS["moe_T8192_H2048_g128"]
+@pytest.mark.parametrize("name", ["moe_T8192_H2048_g128", "moe_T32768_H2048_g128_ue8m0_clamp7",
+                                  "ragged_T100003_H3072_g128"])
+def test_transposed_full_bench_workload(name):
+    """The workloads `bench.py --transposed` times, at full size and in its
+    launch configuration (the plan's prefetch form and grid): every code and
+    scale equal to the row-major kernel's output (itself compared with the
+    oracle at full size), the clamp counters too, the padding zero."""
+    wl = wls.WORKLOADS[name]
     x, w = wls.make_inputs(wl, "cuda")
-    op = tk.SwigluQuant(wl.H, wl.group, wl.scale_fmt, wl.out_fmt, True)
-    (q, s, _), (qt, st, _) = _both(op, x, w)
+    op = tk.SwigluQuant(wl.H, wl.group, wl.scale_fmt, wl.out_fmt, True, wl.clamp, wl.clamp is not None)
+    (q, s, c0), (qt, st, c1) = _both(op, x, w)
     assert torch.equal(qt[:, :wl.T].t(), q)
+    assert not bool(qt[:, wl.T:].any())
     assert torch.equal(st, s)
+    if wl.clamp is not None:
+        assert c0.cpu().tolist() == c1.cpu().tolist()
     assert tk.tk_fault_word(torch.cuda.current_device()) == 0
 
 
